@@ -1,0 +1,360 @@
+"""Plain float64 CPU oracle for the decoupled-momentum (DeMo / FlexDeMo) step.
+
+TEST INFRASTRUCTURE ONLY.  This module is the slow, obviously-correct
+statement of what the GPU library computes.  Only the test-suite, the
+smoke check and the CPU-baseline / reference legs of the benchmark may import
+it.  It shares no code, tables, constants or helpers with the CUDA path, and it
+never imports the product package.
+
+Sources (cited by page title and section):
+
+* "DeToNATION: Decoupled Torch Network-Aware Training on Interlinked Online
+  Nodes" (Paper-Notes, AAAI 2026), section "方法详解", subsection "1. FlexDeMo
+  优化器", Algorithm 1 -- the per-shard step:
+  step 3 momentum accumulate, step 4 extract fast components, step 5 subtract
+  them from the momentum, step 6 synchronise q in the replication group R,
+  step 7 parameter update with the synchronised Q.
+* Same page, subsection "2. 复制方案 (Replication Schemes)", scheme table --
+  DeMo (DCT-II, indices sent), Random (shared seed, no indices), Striding
+  (equally spaced, no indices), DiLoCo (full sync every n steps).
+* Same page, subsection "3. Sign 函数与超参数分析" -- ternary sign before
+  sync, chunk size 32, TopK 4.
+* "DeMo: Decoupled Momentum Optimization" (arXiv 2411.19870), abstract --
+  orthonormal transform (DCT) + top-k, momentum subtraction as error feedback.
+
+Readings where the pages leave a step open (each one is listed in the design
+notes of the repository):
+
+* DCT: the orthonormal 1-D DCT-II of every length-32 chunk (Ahmed, Natarajan
+  & Rao 1974), inverse = transpose (DCT-III).
+* top-k key |X_u|; exact ties go to the lowest u.  The payload lists the kept
+  coefficients in ASCENDING u order (a canonical wire order).
+* error feedback subtracts the UNSIGNED q; the sign (ternary, sign(0) = 0) is
+  applied only to the transmitted values, in every mode when the flag is set.
+* scatter-mean divides each slot by the number of replicas that sent it.
+* Random: k draws per chunk by partial Fisher-Yates over the 32 positions; draw
+  j uses H(seed, step, chunk, j) built from splitmix64 and Lemire's
+  multiply-shift range reduction.  Payload in draw order.
+* Striding: stride n_s = 32 / k, offset = step mod n_s.
+* DiLoCo: the whole momentum is sent on steps with (step + 1) mod H == 0 and
+  nothing otherwise; theta moves only on those steps.
+* beta and lr are rounded to float32 first (the GPU computes in float32).
+
+Parity status: every function here is pinned by the CPU tests
+(``tests/test_oracle_pins.py``) against closed forms, a library DCT, brute
+force and published splitmix64 outputs, except the composed multi-step
+trajectory, which is "parity unpinned" beyond those per-step pins: the pages
+print no worked example.
+"""
+
+import math
+
+import numpy as np
+
+CHUNK = 32
+
+MODE_DEMO = 0
+MODE_RANDOM = 1
+MODE_STRIDE = 2
+MODE_DILOCO = 3
+MODE_NAMES = {MODE_DEMO: "demo", MODE_RANDOM: "random", MODE_STRIDE: "stride", MODE_DILOCO: "diloco"}
+
+NEAR_TIE_REL = 1e-6
+
+_M64 = (1 << 64) - 1
+_GAMMA = 0x9E3779B97F4A7C15  # splitmix64 increment (golden-ratio constant)
+
+
+# ----------------------------------------------------------------------------
+# float32 rounding of the step constants
+# ----------------------------------------------------------------------------
+
+def f32(x):
+    """The float64 value of ``x`` rounded to float32 (the GPU's beta / lr)."""
+    return float(np.float32(x))
+
+
+# ----------------------------------------------------------------------------
+# The orthonormal DCT-II of one chunk
+# ----------------------------------------------------------------------------
+
+def dct_matrix(C=CHUNK):
+    """Orthonormal DCT-II matrix D[u][i] = a_u cos(pi (2i+1) u / (2C)).
+
+    a_0 = sqrt(1/C), a_u = sqrt(2/C) for u >= 1.  X = D x is the transform of a
+    chunk x and x = D^T X its inverse (DeMo abstract: an orthonormal
+    transform such as the DCT; DeToNATION notes, replication table, DeMo row:
+    DCT-II).
+    """
+    D = np.empty((C, C), dtype=np.float64)
+    for u in range(C):
+        a = math.sqrt((1.0 if u == 0 else 2.0) / C)
+        for i in range(C):
+            D[u, i] = a * math.cos(math.pi * (2 * i + 1) * u / (2 * C))
+    return D
+
+
+_D = dct_matrix()
+
+
+# ----------------------------------------------------------------------------
+# splitmix64 and the shared-seed index generator
+# ----------------------------------------------------------------------------
+
+def splitmix64_mix(z):
+    """The splitmix64 output function applied to the state ``z`` + gamma.
+
+    splitmix64 (Steele, Lea & Flood, OOPSLA 2014; Vigna's public-domain C
+    version): state += 0x9e3779b97f4a7c15, then two xor-shift-multiply rounds
+    and a final xor-shift.  Calling this on s, s+gamma, s+2 gamma, ... yields
+    the generator's output stream for seed s.
+    """
+    z = (z + _GAMMA) & _M64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _M64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _M64
+    return z ^ (z >> 31)
+
+
+def splitmix64_stream(seed, count):
+    """First ``count`` outputs of a splitmix64 generator seeded with ``seed``."""
+    out = []
+    state = seed & _M64
+    for _ in range(count):
+        out.append(splitmix64_mix(state))
+        state = (state + _GAMMA) & _M64
+    return out
+
+
+def index_hash(seed, step, chunk, j):
+    """H(s, t, c, j) = sm(sm(sm(sm(s) ^ t) ^ c) ^ j) on 64-bit words.
+
+    The shared seed makes every replica draw the same positions, so no index
+    is transmitted (DeToNATION notes, replication table, Random row: indices
+    are not sent because the seed is shared).
+    """
+    h = splitmix64_mix(seed & _M64)
+    h = splitmix64_mix(h ^ (step & _M64))
+    h = splitmix64_mix(h ^ (chunk & _M64))
+    return splitmix64_mix(h ^ (j & _M64))
+
+
+def random_positions(seed, step, chunk, k, C=CHUNK):
+    """k distinct positions of one chunk, in draw order (partial Fisher-Yates).
+
+    Draw j takes r_j = floor(hi32(H) * (C - j) / 2^32) (Lemire's multiply-shift
+    reduction to [0, C - j)) and picks the r_j-th still-free position counting
+    upward from 0.
+    """
+    free = list(range(C))
+    pos = []
+    for j in range(k):
+        h = index_hash(seed, step, chunk, j)
+        r = ((h >> 32) * (C - j)) >> 32
+        pos.append(free.pop(r))
+    return pos
+
+
+def stride_positions(step, k, C=CHUNK):
+    """Equally spaced positions o + n_s j, n_s = C / k, o = step mod n_s."""
+    if C % k != 0:
+        raise ValueError("striding needs k to divide the chunk size")
+    ns = C // k
+    o = step % ns
+    return [o + ns * j for j in range(k)]
+
+
+def diloco_is_sync(step, period):
+    """DiLoCo sends the full momentum once every ``period`` steps."""
+    return (step + 1) % period == 0
+
+
+# ----------------------------------------------------------------------------
+# Top-k by magnitude
+# ----------------------------------------------------------------------------
+
+def topk_select(X, k):
+    """Per row of X, the k slots of largest |X_u|; exact ties go to the lowest u.
+
+    Returns (kept [rows, k] in ascending u, order [rows, C]) where ``order`` is
+    the full ranking by the key (-|X_u|, u) (a stable sort keeps equal keys in
+    index order).  DeMo abstract: the transform is followed by a top-k
+    sparsification.
+    """
+    X = np.atleast_2d(np.asarray(X, dtype=np.float64))
+    order = np.argsort(-np.abs(X), axis=1, kind="stable")
+    kept = np.sort(order[:, :k], axis=1)
+    return kept, order
+
+
+# ----------------------------------------------------------------------------
+# One replica's encode: momentum, extraction, error feedback, payload
+# ----------------------------------------------------------------------------
+
+def _ternary_sign(v):
+    return np.sign(v)  # -1, 0 or +1; sign(0) = 0
+
+
+def encode(m, g, beta, k, mode, sign, seed=0, step=0, period=8, chunk_ids=None):
+    """Algorithm 1 steps 3-5 for one replica, plus the payload of step 6.
+
+    m, g: float64 arrays of length n (n a multiple of 32); g holds the exact
+    float32 / bfloat16 gradient values.  Returns a dict with
+
+    * ``m``: the new momentum (after the subtraction of q),
+    * ``q``: the extracted component, [nc, 32],
+    * ``vals``: payload values ([nc, k]; DiLoCo: [nc, 32] on sync steps, None
+      otherwise), signed when ``sign`` is set,
+    * ``idx``: payload indices [nc, k] (DeMo only, ascending u), else None,
+    * ``pos``: the positions selected in each chunk ([nc, k]; DiLoCo: all 32),
+    * ``X``: the DCT coefficients (DeMo only),
+    * ``near_tie``: bool [nc], chunks whose selection or sign is decided by a
+      gap below 1e-6 of the chunk's largest coefficient (DeMo only).
+    """
+    m = np.asarray(m, dtype=np.float64)
+    g = np.asarray(g, dtype=np.float64)
+    n = m.shape[0]
+    assert n % CHUNK == 0
+    nc = n // CHUNK
+    if chunk_ids is None:
+        chunk_ids = np.arange(nc, dtype=np.int64)
+
+    # Step 3: momentum accumulate, m <- beta m + Delta.
+    x = (f32(beta) * m + g).reshape(nc, CHUNK)
+
+    q = np.zeros_like(x)
+    out = {"X": None, "idx": None, "near_tie": np.zeros(nc, dtype=bool)}
+
+    if mode == MODE_DEMO:
+        # Step 4: DCT-II of every chunk, keep the top-k by magnitude.
+        X = x @ _D.T  # X[c, u] = sum_i D[u, i] x[c, i]
+        kept, order = topk_select(X, k)
+        mag = np.abs(X)
+        rows = np.arange(nc)[:, None]
+        Xs = np.zeros_like(X)
+        Xs[rows, kept] = X[rows, kept]
+        q = Xs @ _D  # inverse transform of the kept coefficients
+        vals = X[rows, kept]
+        # Near-tie diagnostics (for parity checks against a float32 kernel).
+        srt = np.take_along_axis(mag, order, axis=1)
+        top = srt[:, 0]
+        tie = np.zeros(nc, dtype=bool)
+        if k < CHUNK:
+            tie |= (srt[:, k - 1] - srt[:, k]) <= NEAR_TIE_REL * top
+        if sign:
+            tie |= (np.abs(vals) <= NEAR_TIE_REL * top[:, None]).any(axis=1)
+        out.update(X=X, idx=kept.astype(np.int64), pos=kept.astype(np.int64), near_tie=tie)
+    elif mode in (MODE_RANDOM, MODE_STRIDE):
+        pos = np.empty((nc, k), dtype=np.int64)
+        for row in range(nc):
+            if mode == MODE_RANDOM:
+                pos[row] = random_positions(seed, step, int(chunk_ids[row]), k)
+            else:
+                pos[row] = stride_positions(step, k)
+        rows = np.arange(nc)[:, None]
+        q[rows, pos] = x[rows, pos]
+        vals = x[rows, pos]
+        out.update(pos=pos)
+    elif mode == MODE_DILOCO:
+        if diloco_is_sync(step, period):
+            q = x.copy()
+            vals = x.copy()
+            out.update(pos=np.tile(np.arange(CHUNK), (nc, 1)))
+        else:
+            vals = None
+            out.update(pos=None)
+    else:
+        raise ValueError("unknown mode")
+
+    if vals is not None and sign:
+        vals = _ternary_sign(vals)
+
+    # Step 5: m <- m - q (the unsigned extracted component).
+    out["m"] = (x - q).reshape(n)
+    out["q"] = q
+    out["vals"] = vals
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Combine the replicas' payloads and update the parameters
+# ----------------------------------------------------------------------------
+
+def scatter_mean(vals_list, pos_list, nc):
+    """Per chunk and slot: sum of the replicas' values / number of senders.
+
+    Replicas are summed in order r = 0..R-1; empty slots stay 0.
+    """
+    S = np.zeros((nc, CHUNK), dtype=np.float64)
+    cnt = np.zeros((nc, CHUNK), dtype=np.int64)
+    rows = np.arange(nc)
+    for vals, pos in zip(vals_list, pos_list):
+        if vals is None:
+            continue
+        for j in range(pos.shape[1]):
+            S[rows, pos[:, j]] += vals[:, j]
+            cnt[rows, pos[:, j]] += 1
+    Y = np.zeros_like(S)
+    nz = cnt > 0
+    Y[nz] = S[nz] / cnt[nz]
+    return Y, cnt
+
+
+def decode_update(theta, vals_list, pos_list, lr, mode):
+    """Algorithm 1 step 6 (combine) and step 7 (theta <- theta - lr Q).
+
+    DeMo: Q = D^T Y (inverse DCT of the scatter-mean); the other schemes send
+    values in the parameter domain, so Q = Y.
+    """
+    theta = np.asarray(theta, dtype=np.float64)
+    n = theta.shape[0]
+    nc = n // CHUNK
+    Y, cnt = scatter_mean(vals_list, pos_list, nc)
+    Q = Y @ _D if mode == MODE_DEMO else Y
+    new_theta = theta - f32(lr) * Q.reshape(n)
+    return new_theta, Q, Y, cnt
+
+
+def step(theta, ms, gs, *, beta, lr, k, mode, sign, seed=0, step_idx=0, period=8, chunk_ids=None):
+    """One full step over R replicas: encode every replica, combine, update.
+
+    Returns (theta_new, [m_r new], info) where info holds the payloads, Q and
+    the per-replica near-tie flags.
+    """
+    encs = [
+        encode(m, g, beta, k, mode, sign, seed=seed, step=step_idx, period=period, chunk_ids=chunk_ids)
+        for m, g in zip(ms, gs)
+    ]
+    vals_list = [e["vals"] for e in encs]
+    pos_list = [e["pos"] for e in encs]
+    new_theta, Q, Y, cnt = decode_update(theta, vals_list, pos_list, lr, mode)
+    info = {
+        "encodes": encs,
+        "Q": Q,
+        "Y": Y,
+        "cnt": cnt,
+        "near_tie": np.any([e["near_tie"] for e in encs], axis=0),
+    }
+    return new_theta, [e["m"] for e in encs], info
+
+
+# ----------------------------------------------------------------------------
+# Wire-format size (bytes per replica) of one step's payload
+# ----------------------------------------------------------------------------
+
+def payload_bytes(mode, n, k, step=0, period=8, idx_bytes_per_entry=1):
+    """(value bytes, index bytes) one replica sends for a step.
+
+    DeMo sends k float32 values and k indices per chunk; Random and Striding
+    send only the k values (indices come from the shared seed / the step);
+    DiLoCo sends the n float32 momentum values on sync steps and nothing
+    otherwise (DeToNATION notes, replication table, the column on whether a
+    scheme must send its indices).
+    """
+    nc = n // CHUNK
+    if mode == MODE_DEMO:
+        return nc * k * 4, nc * k * idx_bytes_per_entry
+    if mode in (MODE_RANDOM, MODE_STRIDE):
+        return nc * k * 4, 0
+    if mode == MODE_DILOCO:
+        return (n * 4 if diloco_is_sync(step, period) else 0), 0
+    raise ValueError("unknown mode")

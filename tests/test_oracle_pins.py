@@ -1,0 +1,404 @@
+"""Pins of the float64 oracle against facts that do not come from the oracle itself.
+
+Each pin checks the oracle against mathematics the pages fix (orthonormality,
+closed forms, a library DCT computed by an FFT route, brute force over all
+subsets, hand-computed scatter-means, the published splitmix64 stream, exact
+reductions to momentum-free SGD).  The planted-mistake tests at the end swap a
+plausible bug into the oracle and check that some pin fails.
+"""
+
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle.demo_ref as ref
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+C = ref.CHUNK
+
+
+def rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+# ----------------------------------------------------------------------------
+# Pin functions (return None, raise AssertionError on failure); each is run on
+# the real oracle and, below, on planted mutants.
+# ----------------------------------------------------------------------------
+
+def pin_dct_orthonormal():
+    D = ref._D
+    assert np.abs(D @ D.T - np.eye(C)).max() < 1e-12
+    assert np.abs(D.T @ D - np.eye(C)).max() < 1e-12
+
+
+def pin_dct_vs_fft_library():
+    sp = pytest.importorskip("scipy.fft")
+    x = rng(1).standard_normal((64, C))
+    enc = ref.encode(np.zeros(64 * C), x.reshape(-1), 0.0, C, ref.MODE_DEMO, False)
+    assert np.abs(enc["X"] - sp.dct(x, type=2, norm="ortho", axis=1)).max() < 1e-12
+
+
+def pin_dc_coefficient():
+    a = 0.7
+    enc = ref.encode(np.zeros(C), np.full(C, a), 0.0, 1, ref.MODE_DEMO, False)
+    X = enc["X"][0]
+    assert abs(X[0] - a * math.sqrt(C)) < 1e-12
+    assert np.abs(X[1:]).max() < 1e-12 * a
+    assert list(enc["idx"][0]) == [0]
+
+
+def pin_single_cosine():
+    # x_i = cos(pi (2i+1) u0 / 64): sum_i cos^2 = 16, so X_{u0} = (1/4) * 16 = 4 and all
+    # other coefficients vanish (textbook orthogonality of the DCT-II basis).
+    for u0 in (1, 5, 17, 31):
+        x = np.array([math.cos(math.pi * (2 * i + 1) * u0 / 64) for i in range(C)])
+        enc = ref.encode(np.zeros(C), x, 0.0, 1, ref.MODE_DEMO, False)
+        X = enc["X"][0]
+        assert abs(X[u0] - 4.0) < 1e-12
+        X[u0] = 0.0
+        assert np.abs(X).max() < 1e-12
+
+
+def brute_topk(X, k):
+    """All C(n, k) subsets: maximise sum |X_u|, then the lexicographically smallest."""
+    best, best_key = None, None
+    for S in itertools.combinations(range(len(X)), k):
+        key = (-sum(abs(X[u]) for u in S), S)
+        if best_key is None or key < best_key:
+            best, best_key = S, key
+    return list(best)
+
+
+def pin_topk_bruteforce():
+    r = rng(2)
+    for trial in range(60):
+        L = 8 if trial % 2 else 10
+        X = r.integers(-3, 4, size=L).astype(np.float64)  # many exact ties
+        for k in range(1, 5):
+            kept, _ = ref.topk_select(X, k)
+            assert list(kept[0]) == brute_topk(X, k), (X, k)
+
+
+def pin_k32_zero_residual():
+    r = rng(3)
+    m = r.standard_normal(4 * C)
+    g = r.standard_normal(4 * C)
+    enc = ref.encode(m, g, 0.9, C, ref.MODE_DEMO, False)
+    assert np.abs(enc["m"]).max() < 1e-12
+    assert np.abs(enc["vals"] - enc["X"]).max() == 0.0
+
+
+def pin_parseval_and_projection():
+    sp = pytest.importorskip("scipy.fft")
+    r = rng(4)
+    m = r.standard_normal(16 * C)
+    g = r.standard_normal(16 * C)
+    for sign in (False, True):
+        enc = ref.encode(m, g, 0.5, 4, ref.MODE_DEMO, sign)
+        x = (float(np.float32(0.5)) * m + g).reshape(-1, C)
+        q = enc["q"]
+        res = enc["m"].reshape(-1, C)
+        # ||x||^2 = ||q||^2 + ||x - q||^2 (q is an orthogonal projection of x)
+        lhs = (x * x).sum(1)
+        rhs = (q * q).sum(1) + (res * res).sum(1)
+        assert np.abs(lhs - rhs).max() < 1e-10 * lhs.max()
+        # the residual's spectrum (FFT route) is zero on the kept slots and X elsewhere
+        Rspec = sp.dct(res, type=2, norm="ortho", axis=1)
+        Xspec = sp.dct(x, type=2, norm="ortho", axis=1)
+        rows = np.arange(x.shape[0])[:, None]
+        assert np.abs(Rspec[rows, enc["idx"]]).max() < 1e-12
+        Xspec[rows, enc["idx"]] = 0.0
+        assert np.abs(Rspec - Xspec).max() < 1e-12
+
+
+def pin_sgd_reduction():
+    # R = 1, k = 32, sign off: every step drains m, so theta_{t+1} = theta_t - lr g_t.
+    r = rng(5)
+    n = 8 * C
+    for mode in (ref.MODE_DEMO, ref.MODE_RANDOM, ref.MODE_STRIDE):
+        theta = r.standard_normal(n)
+        m = np.zeros(n)
+        for t in range(3):
+            g = r.standard_normal(n)
+            th2, (m2,), _ = ref.step(theta, [m], [g], beta=0.9, lr=0.1, k=C, mode=mode, sign=False,
+                                     seed=7, step_idx=t)
+            assert np.abs(th2 - (theta - float(np.float32(0.1)) * g)).max() < 1e-12
+            assert np.abs(m2).max() < 1e-12
+            theta, m = th2, m2
+
+
+def pin_replica_mean_identical():
+    r = rng(6)
+    n = 6 * C
+    m = r.standard_normal(n)
+    g = r.standard_normal(n)
+    theta = r.standard_normal(n)
+    for mode, k in ((ref.MODE_DEMO, 4), (ref.MODE_RANDOM, 8), (ref.MODE_STRIDE, 4)):
+        th1, _, info1 = ref.step(theta, [m], [g], beta=0.9, lr=0.1, k=k, mode=mode, sign=False, seed=3)
+        th3, _, info3 = ref.step(theta, [m] * 3, [g] * 3, beta=0.9, lr=0.1, k=k, mode=mode, sign=False,
+                                 seed=3)
+        # the mean of R identical payloads is the payload itself, so Q equals q
+        assert np.abs(info3["Q"] - info1["encodes"][0]["q"]).max() < 1e-12
+        assert np.abs(th3 - th1).max() < 1e-12
+
+
+def pin_scatter_mean_hand_example():
+    # chunk 0: replica 0 sends (u=1, 2.0), (u=5, -1.0); replica 1 sends (u=1, 4.0), (u=7, 3.0)
+    # chunk 1: replica 0 sends (u=0, 1.0), (u=31, 1.0); replica 1 sends (u=2, -2.0), (u=31, 0.0)
+    vals = [np.array([[2.0, -1.0], [1.0, 1.0]]), np.array([[4.0, 3.0], [-2.0, 0.0]])]
+    pos = [np.array([[1, 5], [0, 31]]), np.array([[1, 7], [2, 31]])]
+    Y, cnt = ref.scatter_mean(vals, pos, 2)
+    want = np.zeros((2, C))
+    want[0, 1], want[0, 5], want[0, 7] = 3.0, -1.0, 3.0
+    want[1, 0], want[1, 2], want[1, 31] = 1.0, -2.0, 0.5
+    assert np.array_equal(Y, want)
+    assert cnt[0, 1] == 2 and cnt[0, 5] == 1 and cnt[1, 31] == 2 and cnt.sum() == 8
+
+
+def pin_sign_values():
+    r = rng(7)
+    n = 32 * C
+    ms = [r.standard_normal(n), r.standard_normal(n)]
+    gs = [r.standard_normal(n), r.standard_normal(n)]
+    _, _, info = ref.step(r.standard_normal(n), ms, gs, beta=0.9, lr=0.1, k=4, mode=ref.MODE_DEMO, sign=True)
+    assert set(np.unique(info["Y"])) <= {-1.0, -0.5, 0.0, 0.5, 1.0}
+    for e in info["encodes"]:
+        assert set(np.unique(e["vals"])) <= {-1.0, 0.0, 1.0}
+
+
+def pin_splitmix64_published():
+    lines = [l for l in open(os.path.join(GOLDEN, "splitmix64_seed1234567.txt")) if not l.startswith("#")]
+    seed = int(lines[0].split()[1])
+    want = [int(l) for l in lines[1:] if l.strip()]
+    assert ref.splitmix64_stream(seed, len(want)) == want
+
+
+def pin_random_positions():
+    for c in range(200):
+        for k in (1, 4, 8, 32):
+            p = ref.random_positions(11, 3, c, k)
+            assert len(p) == k and len(set(p)) == k and all(0 <= x < C for x in p)
+            # draw j does not depend on k: a shorter draw is a prefix
+            assert p == ref.random_positions(11, 3, c, C)[:k]
+    # Lemire's reduction stays in range at the hash extremes: floor((2^32-1)(32-j)/2^32) = 31-j
+    for j in range(C):
+        assert (((1 << 32) - 1) * (C - j)) >> 32 == C - 1 - j
+    # first-draw and ordered-pair frequencies are uniform (chi-square, fixed seed)
+    N = 20000
+    counts1 = np.zeros(C)
+    pairs = np.zeros((C, C))
+    for c in range(N):
+        p = ref.random_positions(0, 1, c, 2)
+        counts1[p[0]] += 1
+        pairs[p[0], p[1]] += 1
+    e1 = N / C
+    chi1 = ((counts1 - e1) ** 2 / e1).sum()
+    assert chi1 < 70.0  # 31 dof: p ~ 1e-4 at 70
+    off = ~np.eye(C, dtype=bool)
+    assert (pairs[~off] == 0).all()
+    e2 = N / (C * (C - 1))
+    chi2 = ((pairs[off] - e2) ** 2 / e2).sum()
+    assert chi2 < 1160.0  # 991 dof: mean 991, sd ~44.5
+
+
+def pin_stride_coverage():
+    for k in (1, 2, 4, 8, 16, 32):
+        ns = C // k
+        for t0 in (0, 5, 13):
+            seen = []
+            for t in range(t0, t0 + ns):
+                seen += ref.stride_positions(t, k)
+            assert sorted(seen) == list(range(C))
+
+
+def pin_diloco_closed_form():
+    r = rng(8)
+    n = 4 * C
+    H = 8
+    beta = 0.9
+    b = float(np.float32(beta))  # computed here, not through the oracle
+    theta0 = r.standard_normal(n)
+    theta, m = theta0.copy(), np.zeros(n)
+    gs = [r.standard_normal(n) for _ in range(2 * H)]
+    for t in range(2 * H):
+        th2, (m2,), info = ref.step(theta, [m], [gs[t]], beta=beta, lr=0.25, k=1, mode=ref.MODE_DILOCO,
+                                    sign=False, step_idx=t, period=H)
+        if (t + 1) % H:
+            assert np.array_equal(th2, theta)  # theta moves only on sync steps
+            assert info["encodes"][0]["vals"] is None
+        else:
+            acc = sum(b ** (H - 1 - j) * gs[t - H + 1 + j] for j in range(H))
+            assert np.abs(info["encodes"][0]["vals"].reshape(-1) - acc).max() < 1e-12
+            assert np.abs(th2 - (theta - float(np.float32(0.25)) * acc)).max() < 1e-12
+            assert np.abs(m2).max() == 0.0
+        theta, m = th2, m2
+
+
+def pin_payload_bytes():
+    n = 1 << 20
+    for k in (1, 2, 4, 8):
+        dv, di = ref.payload_bytes(ref.MODE_DEMO, n, k, idx_bytes_per_entry=4)
+        rv, ri = ref.payload_bytes(ref.MODE_RANDOM, n, k)
+        assert (dv + di) / (rv + ri) == 2.0  # Random needs half of DeMo's bytes (4-byte indices)
+        dv, di = ref.payload_bytes(ref.MODE_DEMO, n, k, idx_bytes_per_entry=1)
+        assert (dv + di) / (rv + ri) == 1.25
+    assert ref.payload_bytes(ref.MODE_DILOCO, n, 1, step=7, period=8) == (4 * n, 0)
+    assert ref.payload_bytes(ref.MODE_DILOCO, n, 1, step=6, period=8) == (0, 0)
+
+
+ALL_PINS = [
+    pin_dct_orthonormal, pin_dct_vs_fft_library, pin_dc_coefficient, pin_single_cosine,
+    pin_topk_bruteforce, pin_k32_zero_residual, pin_parseval_and_projection, pin_sgd_reduction,
+    pin_replica_mean_identical, pin_scatter_mean_hand_example, pin_sign_values, pin_splitmix64_published,
+    pin_random_positions, pin_stride_coverage, pin_diloco_closed_form, pin_payload_bytes,
+]
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin()
+
+
+def test_near_tie_flags_constant_chunk():
+    # A constant chunk has one nonzero coefficient; with k = 4 the 4th and 5th
+    # magnitudes are both 0, so the oracle flags the chunk as a near-tie.
+    enc = ref.encode(np.zeros(C), np.full(C, 1.5), 0.0, 4, ref.MODE_DEMO, True)
+    assert enc["near_tie"][0]
+    enc = ref.encode(np.zeros(C), rng(9).standard_normal(C), 0.0, 4, ref.MODE_DEMO, False)
+    assert not enc["near_tie"][0]
+
+
+# ----------------------------------------------------------------------------
+# Planted mistakes: each mutant must make at least one pin fail.
+# ----------------------------------------------------------------------------
+
+def _fails(pins):
+    for p in pins:
+        try:
+            p()
+        except AssertionError:
+            return True
+    return False
+
+
+def test_mutant_transposed_basis(monkeypatch):
+    monkeypatch.setattr(ref, "_D", ref._D.T.copy())
+    assert _fails([pin_dc_coefficient, pin_single_cosine, pin_dct_vs_fft_library])
+
+
+def test_mutant_unnormalised_dc(monkeypatch):
+    D = ref._D.copy()
+    D[0] *= math.sqrt(2.0)  # a_0 = sqrt(2/C) instead of sqrt(1/C)
+    monkeypatch.setattr(ref, "_D", D)
+    assert _fails([pin_dct_orthonormal])
+    assert _fails([pin_dc_coefficient])
+
+
+def test_mutant_unstable_topk(monkeypatch):
+    def bad(X, k):
+        # ties broken toward the HIGHEST index
+        X = np.atleast_2d(np.asarray(X, dtype=np.float64))
+        cols = np.broadcast_to(-np.arange(X.shape[1]), X.shape)
+        order = np.lexsort((cols, -np.abs(X)), axis=1)
+        return np.sort(order[:, :k], axis=1), order
+
+    monkeypatch.setattr(ref, "topk_select", bad)
+    assert _fails([pin_topk_bruteforce])
+
+
+def test_mutant_mean_over_R(monkeypatch):
+    orig = ref.scatter_mean
+
+    def bad(vals_list, pos_list, nc):
+        Y, cnt = orig(vals_list, pos_list, nc)
+        S = Y * cnt
+        return S / len(vals_list), cnt
+
+    monkeypatch.setattr(ref, "scatter_mean", bad)
+    assert _fails([pin_scatter_mean_hand_example])
+
+
+def test_mutant_signed_feedback(monkeypatch):
+    # error feedback subtracting the signed values instead of q
+    orig = ref.encode
+
+    def bad(m, g, beta, k, mode, sign, **kw):
+        out = orig(m, g, beta, k, mode, sign, **kw)
+        if sign and mode == ref.MODE_DEMO:
+            x = (ref.f32(beta) * np.asarray(m) + np.asarray(g)).reshape(-1, C)
+            Xs = np.zeros_like(out["X"])
+            rows = np.arange(x.shape[0])[:, None]
+            Xs[rows, out["idx"]] = out["vals"]
+            out["q"] = Xs @ ref._D
+            out["m"] = (x - out["q"]).reshape(-1)
+        return out
+
+    monkeypatch.setattr(ref, "encode", bad)
+    assert _fails([pin_parseval_and_projection])
+
+
+def test_mutant_no_removal_in_fisher_yates(monkeypatch):
+    def bad(seed, step, chunk, k, C=C):
+        free = list(range(C))
+        out = []
+        for j in range(k):
+            h = ref.index_hash(seed, step, chunk, j)
+            out.append(free[((h >> 32) * (C - j)) >> 32])
+        return out
+
+    monkeypatch.setattr(ref, "random_positions", bad)
+    assert _fails([pin_random_positions])
+
+
+def test_mutant_stride_without_offset(monkeypatch):
+    monkeypatch.setattr(ref, "stride_positions", lambda step, k, C=C: [(C // k) * j for j in range(k)])
+    assert _fails([pin_stride_coverage])
+
+
+def test_mutant_dropped_beta(monkeypatch):
+    monkeypatch.setattr(ref, "f32", lambda x: 1.0 if x == 0.9 else float(np.float32(x)))
+    assert _fails([pin_diloco_closed_form])
+
+
+def test_mutant_wrong_hash_constant(monkeypatch):
+    monkeypatch.setattr(ref, "_GAMMA", 0x9E3779B97F4A7C13)
+    assert _fails([pin_splitmix64_published])
+
+
+# ----------------------------------------------------------------------------
+# Regression fixtures written by tests/golden/make_golden.py (oracle only)
+# ----------------------------------------------------------------------------
+
+def test_golden_random_positions_unchanged():
+    for line in open(os.path.join(GOLDEN, "random_positions_seed0.txt")):
+        if line.startswith("#"):
+            continue
+        head, pos = line.split(":")
+        seed, step, chunk = map(int, head.split())
+        assert ref.random_positions(seed, step, chunk, 8) == [int(p) for p in pos.split()]
+
+
+def test_golden_demo_step_unchanged():
+    import importlib.util
+
+    spec = importlib.util.spec_from_file_location("make_golden", os.path.join(GOLDEN, "make_golden.py"))
+    mg = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mg)
+    theta, gs = mg.tiny_inputs()
+    th1, _, info = ref.step(theta, [np.zeros_like(theta)] * 2, gs, beta=0.999, lr=1e-3, k=4,
+                            mode=ref.MODE_DEMO, sign=True)
+    idx, th = {}, []
+    for line in open(os.path.join(GOLDEN, "demo_step_tiny.txt")):
+        if line.startswith("idx"):
+            head, vals = line.split(":")
+            _, r, c = head.split()
+            idx[(int(r), int(c))] = [int(v) for v in vals.split()]
+        elif line.startswith("theta1"):
+            th.append(float(line.split()[1]))
+    for (r, c), want in idx.items():
+        assert list(info["encodes"][r]["idx"][c]) == want
+    assert np.array_equal(np.array(th), th1)
