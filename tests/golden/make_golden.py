@@ -50,7 +50,7 @@ def main():
             for c in range(e["idx"].shape[0]):
                 f.write(f"idx {r} {c} : {' '.join(map(str, e['idx'][c]))}\n")
         for v in th1:
-            f.write(f"theta1 {v!r}\n")
+            f.write(f"theta1 {float(v)!r}\n")
 
 
 if __name__ == "__main__":
