@@ -1,1 +1,179 @@
-"""GB300-native decoupled-momentum (DeMo / FlexDeMo) shard step."""
+"""GB300-native decoupled-momentum (DeMo / FlexDeMo) shard step.
+
+A thin ctypes binding over the C ABI of ``libdemo_gb300.so`` (declared in
+``include/demo.h``): it checks tensors, passes their device pointers and the
+current CUDA stream, and raises :class:`DemoError` on a negative status.  Every
+step of the computation runs in the library's CUDA kernels; there is no CPU
+path.  The library is loaded on first use and must have been built
+(``python -m decoupled_momentum_optimizer_gb300.build``).
+"""
+
+import ctypes
+import os
+
+MODES = {"demo": 0, "random": 1, "stride": 2, "diloco": 3}
+GRAD_F32, GRAD_BF16 = 0, 1
+CHUNK = 32
+MAX_REPLICAS = 64
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdemo_gb300.so")
+
+_c_i64, _c_u64, _c_vp = ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p
+_SIGS = {
+    "demo_init": (ctypes.c_int, [ctypes.c_int]),
+    "demo_payload_bytes": (ctypes.c_size_t, [ctypes.c_int, _c_i64, ctypes.c_int, ctypes.c_int, _c_u64, ctypes.c_int,
+                                             ctypes.POINTER(ctypes.c_size_t)]),
+    "demo_encode": (ctypes.c_int, [_c_vp, ctypes.c_int, _c_vp, _c_i64, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_u64, _c_u64, _c_vp, _c_vp, _c_vp]),
+    "demo_decode_update": (ctypes.c_int, [_c_vp, _c_i64, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                          ctypes.c_int, _c_vp, _c_vp, ctypes.c_int, _c_u64, _c_u64, _c_vp]),
+    "demo_step": (ctypes.c_int, [_c_vp, _c_i64, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_vp, ctypes.c_int, _c_vp, ctypes.c_int,
+                                 _c_u64, _c_u64, _c_vp]),
+    "demo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "demo_device_fault": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint)]),
+}
+
+_lib = None
+_inited = set()
+
+
+class DemoError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        name = lib().demo_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{what}: {name}" if what else name)
+
+
+def lib():
+    """The loaded C library (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with python -m decoupled_momentum_optimizer_gb300.build")
+        try:  # load the CUDA runtime the way torch does, so both share one runtime
+            import torch  # noqa: F401
+        except ImportError:  # pragma: no cover
+            pass
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status, what):
+    if status != 0:
+        raise DemoError(status, what)
+
+
+def init(device=None):
+    """demo_init for ``device`` (default: torch's current device)."""
+    import torch
+
+    if device is None:
+        device = torch.cuda.current_device()
+    device = torch.device("cuda", device).index if not isinstance(device, int) else device
+    if device not in _inited:
+        _check(lib().demo_init(device), "demo_init")
+        _inited.add(device)
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t, dtypes, name, n=None):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device (there is no CPU path)")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if n is not None and t.numel() != n:
+        raise ValueError(f"{name} has {t.numel()} elements, expected {n}")
+    return t.data_ptr()
+
+
+def _grad_dtype(g):
+    import torch
+
+    return GRAD_BF16 if g.dtype == torch.bfloat16 else GRAD_F32
+
+
+def _mode(mode):
+    return MODES[mode] if isinstance(mode, str) else int(mode)
+
+
+def payload_bytes(mode, n, k, step=0, diloco_period=8):
+    """(value bytes, index bytes) one replica sends for a step."""
+    ib = ctypes.c_size_t(0)
+    vb = lib().demo_payload_bytes(_mode(mode), n, CHUNK, k, step, diloco_period, ctypes.byref(ib))
+    return vb, ib.value
+
+
+def encode(g, m, vals, idx=None, *, k, beta, mode="demo", sign=True, diloco_period=8, seed=0, step=0, stream=None):
+    """One replica's encode (demo_encode): updates m in place, writes vals (and idx for DeMo)."""
+    import torch
+
+    init(m.device.index)
+    n = m.numel()
+    gp = _ptr(g, (torch.float32, torch.bfloat16), "g", n)
+    mp = _ptr(m, (torch.float32,), "m", n)
+    vp = _ptr(vals, (torch.float32,), "vals") if vals is not None else None
+    ip = _ptr(idx, (torch.uint8,), "idx") if idx is not None else None
+    _check(lib().demo_encode(gp, _grad_dtype(g), mp, n, CHUNK, k, beta, _mode(mode), int(bool(sign)), diloco_period,
+                             seed, step, vp, ip, _stream(stream)), "demo_encode")
+
+
+def decode_update(theta, vals, idx=None, *, k, lr, mode="demo", diloco_period=8, seed=0, step=0, stream=None):
+    """Scatter-mean of the R payloads in ``vals`` (and ``idx``) and theta -= lr Q (demo_decode_update)."""
+    import torch
+
+    init(theta.device.index)
+    n = theta.numel()
+    R = len(vals)
+    tp = _ptr(theta, (torch.float32,), "theta", n)
+    varr = (ctypes.c_void_p * R)(*[_ptr(v, (torch.float32,), f"vals[{r}]") for r, v in enumerate(vals)])
+    iarr = None
+    if idx is not None:
+        iarr = (ctypes.c_void_p * R)(*[_ptr(i, (torch.uint8,), f"idx[{r}]") for r, i in enumerate(idx)])
+    _check(lib().demo_decode_update(tp, n, CHUNK, k, lr, _mode(mode), R, varr, iarr, diloco_period, seed, step,
+                                    _stream(stream)), "demo_decode_update")
+
+
+def step(theta, gs, ms, *, k, beta, lr, mode="demo", sign=True, diloco_period=8, seed=0, step=0, stream=None):
+    """The fused shard step over R replicas (demo_step); theta and every m_r update in place."""
+    import torch
+
+    init(theta.device.index)
+    n = theta.numel()
+    R = len(ms)
+    if len(gs) != R:
+        raise ValueError("need one gradient per replica")
+    tp = _ptr(theta, (torch.float32,), "theta", n)
+    gd = _grad_dtype(gs[0])
+    garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n) for r, g in enumerate(gs)])
+    marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n) for r, m in enumerate(ms)])
+    _check(lib().demo_step(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr, gd, marr, diloco_period,
+                           seed, step, _stream(stream)), "demo_step")
+
+
+def device_fault():
+    """Read and clear the current device's fault word (0 = no kernel gave up on a wait)."""
+    code = ctypes.c_uint(0)
+    _check(lib().demo_device_fault(ctypes.byref(code)), "demo_device_fault")
+    return code.value

@@ -1,0 +1,215 @@
+// Split-path decode: scatter-mean of R replicas' payloads, inverse transform,
+// theta <- theta - lr Q.
+//
+// "DeToNATION: Decoupled Torch Network-Aware Training on Interlinked Online
+// Nodes" (Paper-Notes, AAAI 2026), method section, "1. FlexDeMo" Algorithm 1
+// steps 6-7 (the synchronised Q_t), "2. Replication Schemes" table.
+//
+// Per warp, theta tiles of 32 chunks stream through a two-slot TMA ring; lane
+// i combines the payload entries of its chunk (replicas in order 0..R-1) in
+// shared-memory accumulators, forms Q and updates its theta row, which leaves
+// through a TMA store.  The arithmetic matches the fused step operation by
+// operation, so split and fused results are bit-identical.
+#include "demo_common.cuh"
+#include "demo_params.h"
+
+namespace demo {
+
+struct alignas(1024) DecWarpSmem {
+  float tbuf[2][1024];  // theta tiles
+  float out[1024];      // TMA-store staging; before that, a [i][lane] scratch column per lane
+  float2 acc[32 * 32];  // DeMo accumulators [u][lane] = (sum, count)
+};
+
+constexpr size_t kDecSmem = 1024 + kWarps * sizeof(DecWarpSmem) + kWarps * 16 + 272;
+
+template <int MODE, int MAXR>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams<MAXR> p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  DecWarpSmem& ws = reinterpret_cast<DecWarpSmem*>(base)[warp];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kWarps * sizeof(DecWarpSmem)) + 2 * warp;
+  float* rcp = reinterpret_cast<float*>(base + kWarps * sizeof(DecWarpSmem) + kWarps * 16);
+  if (threadIdx.x <= kMaxReplicas) rcp[threadIdx.x] = p.rcp_tab[threadIdx.x];
+  __syncthreads();
+
+  const long long gw = static_cast<long long>(blockIdx.x) * kWarps + warp;
+  const long long TW = static_cast<long long>(gridDim.x) * kWarps;
+  if (gw >= p.ntiles) return;
+  const long long nitems = (p.ntiles - 1 - gw) / TW + 1;
+
+  if (lane == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  if constexpr (MODE == kModeDemo) {
+#pragma unroll
+    for (int u = 0; u < 32; ++u) ws.acc[u * 32 + lane] = make_float2(0.0f, 0.0f);
+  }
+  __syncwarp();
+
+  auto issue = [&](long long item) {
+    if (item >= nitems) return;
+    const int s = static_cast<int>(item & 1);
+    const int y = static_cast<int>((gw + item * TW) * 32);
+    mbar_expect_tx(&bars[s], kTileBytesF32);
+    tma_load_2d(ws.tbuf[s], &p.theta, &bars[s], 0, y);
+  };
+  if (lane == 0) {
+    issue(0);
+    issue(1);
+  }
+
+  for (long long item = 0; item < nitems; ++item) {
+    const int s = static_cast<int>(item & 1);
+    const uint32_t par = static_cast<uint32_t>((item >> 1) & 1);
+    const long long t = gw + item * TW;
+    const int y = static_cast<int>(t * 32);
+    const long long c = t * 32 + lane;
+    const bool valid = c < p.nc;
+
+    const bool ok = mbar_wait_bounded(&bars[s], par);
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) {
+        atomicOr(p.fault, kFaultLoadTimeout);
+        for (long long it = item; it < item + 2 && it < nitems; ++it)
+          mbar_wait_bounded(&bars[it & 1], static_cast<uint32_t>((it >> 1) & 1));
+        bulk_wait_all();
+      }
+      __syncwarp();
+      return;
+    }
+
+    float th[32];
+    load_row_f32(ws.tbuf[s], lane, th);
+    __syncwarp();
+    if (lane == 0) {
+      fence_proxy_async_smem();
+      issue(item + 2);
+      bulk_wait_read_all();
+    }
+    __syncwarp();
+
+    float Q[32];
+    if constexpr (MODE == kModeDemo) {
+      if (valid) {
+        for (int r = 0; r < p.R; ++r) {
+          const float* vrow = p.vals[r] + c * p.k;
+          const uint8_t* irow = p.idx[r] + c * p.k;
+          for (int j = 0; j < p.k; ++j) {
+            const int u = irow[j] & 31;
+            float2 a = ws.acc[u * 32 + lane];
+            a.x += vrow[j];
+            a.y += 1.0f;
+            ws.acc[u * 32 + lane] = a;
+          }
+        }
+      }
+      float Y[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u) {
+        const float2 a = ws.acc[u * 32 + lane];
+        Y[u] = a.x * rcp[static_cast<int>(a.y)];
+        ws.acc[u * 32 + lane] = make_float2(0.0f, 0.0f);
+      }
+      dct32_inverse(Y, Q);
+    } else if constexpr (MODE == kModeDiloco) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) Q[i] = 0.0f;
+      if (valid) {
+        for (int r = 0; r < p.R; ++r) {
+          const float4* vrow = reinterpret_cast<const float4*>(p.vals[r] + c * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 v = vrow[j];
+            Q[4 * j + 0] += v.x;
+            Q[4 * j + 1] += v.y;
+            Q[4 * j + 2] += v.z;
+            Q[4 * j + 3] += v.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) Q[i] *= p.rcpR;
+    } else {
+      // Random / Striding: every replica sent the same positions.
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ws.out[i * 32 + lane] = 0.0f;
+      auto take = [&](int j, int pos) {
+        float sum = 0.0f;
+        for (int r = 0; r < p.R; ++r) sum += p.vals[r][c * p.k + j];
+        ws.out[pos * 32 + lane] = sum * p.rcpR;
+      };
+      if (valid) {
+        if constexpr (MODE == kModeRandom) {
+          random_draws(p.hbase, static_cast<uint64_t>(c), p.k, take);
+        } else {
+          for (int j = 0; j < p.k; ++j) take(j, stride_position(p.stride_o, p.stride_ns, j));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) Q[i] = ws.out[i * 32 + lane];
+    }
+
+#pragma unroll
+    for (int i = 0; i < 32; ++i) th[i] = __fmaf_rn(-p.lr, Q[i], th[i]);
+    __syncwarp();
+    store_row_f32(ws.out, lane, th);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(&p.theta, ws.out, 0, y);
+      bulk_commit();
+    }
+  }
+  if (lane == 0) bulk_wait_all();
+}
+
+template <int MAXR>
+static cudaError_t launch_decode_t(const DecodeParams<MAXR>& p, int mode, int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kDecSmem;
+  cfg.stream = st;
+  switch (mode) {
+    case kModeDemo: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR>, p);
+    case kModeRandom: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeRandom, MAXR>, p);
+    case kModeStride: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeStride, MAXR>, p);
+    case kModeDiloco: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDiloco, MAXR>, p);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int grid, cudaStream_t st) {
+  return launch_decode_t(p, mode, grid, st);
+}
+
+cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int grid, cudaStream_t st) {
+  return launch_decode_t(p, mode, grid, st);
+}
+
+template <int MAXR>
+static cudaError_t prepare_t() {
+  const int bytes = static_cast<int>(kDecSmem);
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<kModeDemo, MAXR>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_kernel<kModeRandom, MAXR>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_kernel<kModeStride, MAXR>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_kernel<kModeDiloco, MAXR>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return e;
+}
+
+cudaError_t prepare_decode_kernels() {
+  cudaError_t e = prepare_t<kSmallReplicas>();
+  if (e == cudaSuccess) e = prepare_t<kMaxReplicas>();
+  return e;
+}
+
+}  // namespace demo

@@ -1,0 +1,72 @@
+// Kernel parameter blocks and launcher declarations of the DeMo shard step.
+// Tensor maps travel by value as __grid_constant__ kernel parameters.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace demo {
+
+constexpr int kMaxReplicas = 64;
+constexpr int kSmallReplicas = 4;  // parameter blocks for R <= 4 stay small
+
+template <int MAXR>
+struct StepParams {
+  CUtensorMap theta;
+  CUtensorMap g[MAXR];
+  CUtensorMap m[MAXR];
+  long long nc;      // chunks in the shard
+  long long ntiles;  // ceil(nc / 32)
+  int R, k, sign;
+  int sync;          // DiLoCo: this step sends the full momentum
+  int stride_o, stride_ns;
+  unsigned int stride_mask;
+  float beta, lr, rcpR;
+  unsigned long long hbase;  // sm(sm(seed) ^ step) for the Random scheme
+  float rcp_tab[kMaxReplicas + 1];  // float32(1/c), entry 0 = 0
+  unsigned int* fault;
+};
+
+struct EncodeParams {
+  CUtensorMap g;
+  CUtensorMap m;
+  float* vals;
+  uint8_t* idx;
+  long long nc, ntiles;
+  int k, sign, sync;
+  int stride_o, stride_ns;
+  unsigned int stride_mask;
+  float beta;
+  unsigned long long hbase;
+  unsigned int* fault;
+};
+
+template <int MAXR>
+struct DecodeParams {
+  CUtensorMap theta;
+  const float* vals[MAXR];
+  const uint8_t* idx[MAXR];
+  long long nc, ntiles;
+  int R, k;
+  int stride_o, stride_ns;
+  float lr, rcpR;
+  unsigned long long hbase;
+  float rcp_tab[kMaxReplicas + 1];
+  unsigned int* fault;
+};
+
+// Launchers (one per translation unit).  `grid` CTAs of 8 warps; each warp
+// walks the tiles gw, gw + 8*grid, ...
+cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, bool bf16, int grid, cudaStream_t st);
+cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int grid, cudaStream_t st);
+cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int grid, cudaStream_t st);
+cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int grid, cudaStream_t st);
+cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int grid, cudaStream_t st);
+
+// Set the dynamic shared-memory limit of every kernel instantiation.
+cudaError_t prepare_step_kernels();
+cudaError_t prepare_encode_kernels();
+cudaError_t prepare_decode_kernels();
+
+}  // namespace demo

@@ -1,0 +1,271 @@
+// Fused DeMo shard step: every replica's encode (momentum, selection, error
+// feedback, payload) and the decode (scatter-mean, inverse transform, theta
+// update) in one pass over HBM.  The payloads never leave the SM.
+//
+// "DeToNATION: Decoupled Torch Network-Aware Training on Interlinked Online
+// Nodes" (Paper-Notes, AAAI 2026), method section, "1. FlexDeMo", Algorithm 1
+// steps 3-7, with the replication group R simulated by R resident replicas.
+//
+// Per warp, a tile is 32 chunks (one per lane) and is visited as R + 1 items:
+// item r < R streams g_r and m_r through TMA into a two-slot ring, computes the
+// replica's encode in registers and writes m_r back through TMA; the last item
+// streams theta, turns the accumulated payloads into Q and writes theta back.
+// The load for item i + 2 is issued as soon as item i has been read, so two
+// tiles' worth of copies overlap the arithmetic of each warp.
+#include "demo_common.cuh"
+#include "demo_params.h"
+
+namespace demo {
+
+struct alignas(1024) StepWarpSmem {
+  float gbuf[2][1024];   // slot s: g_r tile (f32 or bf16) or the theta tile
+  float mbuf[2][1024];   // slot s: m_r tile
+  float out[1024];       // TMA-store staging; also a [u][lane] scratch column per lane
+  float2 acc[32 * 32];   // DeMo scatter-mean accumulators [u][lane] = (sum, count)
+};
+
+constexpr size_t kStepSmem = 1024 + kWarps * sizeof(StepWarpSmem) + kWarps * 16 + 272;
+
+template <int MODE, bool BF16, int MAXR>
+__global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepParams<MAXR> p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  StepWarpSmem& ws = reinterpret_cast<StepWarpSmem*>(base)[warp];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kWarps * sizeof(StepWarpSmem)) + 2 * warp;
+  float* rcp = reinterpret_cast<float*>(base + kWarps * sizeof(StepWarpSmem) + kWarps * 16);
+  if (threadIdx.x <= kMaxReplicas) rcp[threadIdx.x] = p.rcp_tab[threadIdx.x];
+  __syncthreads();
+
+  const long long gw = static_cast<long long>(blockIdx.x) * kWarps + warp;
+  const long long TW = static_cast<long long>(gridDim.x) * kWarps;
+  if (gw >= p.ntiles) return;
+  const long long ntw = (p.ntiles - 1 - gw) / TW + 1;
+  const bool theta_item = !(MODE == kModeDiloco && !p.sync);
+  const int ipt = theta_item ? p.R + 1 : p.R;
+  const long long nitems = ntw * ipt;
+
+  if (lane == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  if constexpr (MODE == kModeDemo) {
+#pragma unroll
+    for (int u = 0; u < 32; ++u) ws.acc[u * 32 + lane] = make_float2(0.0f, 0.0f);
+  }
+  __syncwarp();
+
+  auto issue = [&](long long item) {
+    if (item >= nitems) return;
+    const int s = static_cast<int>(item & 1);
+    const long long t = gw + (item / ipt) * TW;
+    const int kind = static_cast<int>(item % ipt);
+    const int y = static_cast<int>(t * 32);
+    if (kind < p.R) {
+      mbar_expect_tx(&bars[s], (BF16 ? kTileBytesBF16 : kTileBytesF32) + kTileBytesF32);
+      tma_load_2d(ws.gbuf[s], &p.g[kind], &bars[s], 0, y);
+      tma_load_2d(ws.mbuf[s], &p.m[kind], &bars[s], 0, y);
+    } else {
+      mbar_expect_tx(&bars[s], kTileBytesF32);
+      tma_load_2d(ws.gbuf[s], &p.theta, &bars[s], 0, y);
+    }
+  };
+  if (lane == 0) {
+    issue(0);
+    issue(1);
+  }
+
+  uint32_t P = 0;    // Random / Striding / DiLoCo: positions sent from this lane's chunk
+  float accr[32];    // Random / Striding / DiLoCo: per-position payload sums
+#pragma unroll
+  for (int i = 0; i < 32; ++i) accr[i] = 0.0f;
+
+  for (long long item = 0; item < nitems; ++item) {
+    const int s = static_cast<int>(item & 1);
+    const uint32_t par = static_cast<uint32_t>((item >> 1) & 1);
+    const long long t = gw + (item / ipt) * TW;
+    const int kind = static_cast<int>(item % ipt);
+    const int y = static_cast<int>(t * 32);
+    const long long c = t * 32 + lane;
+
+    const bool ok = mbar_wait_bounded(&bars[s], par);
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) {
+        atomicOr(p.fault, kFaultLoadTimeout);
+        for (long long it = item; it < item + 2 && it < nitems; ++it)
+          mbar_wait_bounded(&bars[it & 1], static_cast<uint32_t>((it >> 1) & 1));
+        bulk_wait_all();
+      }
+      __syncwarp();
+      return;
+    }
+
+    if (kind == 0) {
+      if constexpr (MODE == kModeRandom) P = random_mask(p.hbase, static_cast<uint64_t>(c), p.k);
+      if constexpr (MODE == kModeStride) P = p.stride_mask;
+      if constexpr (MODE == kModeDiloco) P = 0xffffffffu;
+      if constexpr (MODE != kModeDemo) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) accr[i] = 0.0f;
+      }
+    }
+
+    if (kind < p.R) {
+      // ---- one replica: m <- beta m + g; select q; m <- m - q; payload -> accumulators
+      float x[32], gv[32];
+      load_row_grad<BF16>(ws.gbuf[s], lane, gv);
+      load_row_f32(ws.mbuf[s], lane, x);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = __fmaf_rn(p.beta, x[i], gv[i]);
+      __syncwarp();
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        issue(item + 2);
+        bulk_wait_read_all();  // the previous store has left `out`
+      }
+      __syncwarp();
+
+      if constexpr (MODE == kModeDemo) {
+        float X[32], Xs[32];
+        dct32_forward(x, X);
+        const uint32_t M = topk_select(X, p.k, Xs);
+#pragma unroll
+        for (int u = 0; u < 32; ++u) ws.out[u * 32 + lane] = Xs[u];
+        uint32_t mm = M;
+        for (int j = 0; j < p.k; ++j) {  // payload in ascending u
+          const int u = __ffs(mm) - 1;
+          mm &= mm - 1;
+          float v = ws.out[u * 32 + lane];
+          if (p.sign) v = sign3(v);
+          float2 a = ws.acc[u * 32 + lane];
+          a.x += v;
+          a.y += 1.0f;
+          ws.acc[u * 32 + lane] = a;
+        }
+        float q[32];
+        dct32_inverse(Xs, q);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] -= q[i];
+      } else if constexpr (MODE == kModeDiloco) {
+        if (p.sync) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            accr[i] += p.sign ? sign3(x[i]) : x[i];
+            x[i] = 0.0f;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const bool in = (P >> i) & 1u;
+          const float v = p.sign ? sign3(x[i]) : x[i];
+          accr[i] += in ? v : 0.0f;
+          x[i] = in ? 0.0f : x[i];
+        }
+      }
+
+      __syncwarp();
+      store_row_f32(ws.out, lane, x);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&p.m[kind], ws.out, 0, y);
+        bulk_commit();
+      }
+    } else {
+      // ---- decode: Q from the accumulated payloads, theta <- theta - lr Q
+      float th[32];
+      load_row_f32(ws.gbuf[s], lane, th);
+      __syncwarp();
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        issue(item + 2);
+      }
+      float Q[32];
+      if constexpr (MODE == kModeDemo) {
+        float Y[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const float2 a = ws.acc[u * 32 + lane];
+          Y[u] = a.x * rcp[static_cast<int>(a.y)];
+          ws.acc[u * 32 + lane] = make_float2(0.0f, 0.0f);
+        }
+        dct32_inverse(Y, Q);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) Q[i] = accr[i] * p.rcpR;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) th[i] = __fmaf_rn(-p.lr, Q[i], th[i]);
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+      store_row_f32(ws.out, lane, th);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&p.theta, ws.out, 0, y);
+        bulk_commit();
+      }
+    }
+  }
+  if (lane == 0) bulk_wait_all();
+}
+
+template <int MAXR>
+static cudaError_t launch_step_t(const StepParams<MAXR>& p, int mode, bool bf16, int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kStepSmem;
+  cfg.stream = st;
+#define DEMO_LAUNCH(M, B) \
+  if (mode == M && bf16 == B) return cudaLaunchKernelEx(&cfg, step_kernel<M, B, MAXR>, p);
+  DEMO_LAUNCH(kModeDemo, false)
+  DEMO_LAUNCH(kModeDemo, true)
+  DEMO_LAUNCH(kModeRandom, false)
+  DEMO_LAUNCH(kModeRandom, true)
+  DEMO_LAUNCH(kModeStride, false)
+  DEMO_LAUNCH(kModeStride, true)
+  DEMO_LAUNCH(kModeDiloco, false)
+  DEMO_LAUNCH(kModeDiloco, true)
+#undef DEMO_LAUNCH
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, bool bf16, int grid, cudaStream_t st) {
+  return launch_step_t(p, mode, bf16, grid, st);
+}
+
+cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int grid, cudaStream_t st) {
+  return launch_step_t(p, mode, bf16, grid, st);
+}
+
+template <int MAXR>
+static cudaError_t prepare_t() {
+  cudaError_t e = cudaSuccess;
+#define DEMO_ATTR(M, B)                                                                           \
+  if (e == cudaSuccess)                                                                           \
+    e = cudaFuncSetAttribute(step_kernel<M, B, MAXR>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             static_cast<int>(kStepSmem));
+  DEMO_ATTR(kModeDemo, false)
+  DEMO_ATTR(kModeDemo, true)
+  DEMO_ATTR(kModeRandom, false)
+  DEMO_ATTR(kModeRandom, true)
+  DEMO_ATTR(kModeStride, false)
+  DEMO_ATTR(kModeStride, true)
+  DEMO_ATTR(kModeDiloco, false)
+  DEMO_ATTR(kModeDiloco, true)
+#undef DEMO_ATTR
+  return e;
+}
+
+cudaError_t prepare_step_kernels() {
+  cudaError_t e = prepare_t<kSmallReplicas>();
+  if (e == cudaSuccess) e = prepare_t<kMaxReplicas>();
+  return e;
+}
+
+}  // namespace demo

@@ -1,0 +1,165 @@
+/*
+ * demo.h -- C ABI of the GB300 decoupled-momentum (DeMo / FlexDeMo) shard step.
+ *
+ * The library runs, on one GPU, the data-parallel optimizer step of FlexDeMo
+ * for ONE flat float32 parameter shard and R replicas of it ("DeToNATION:
+ * Decoupled Torch Network-Aware Training on Interlinked Online Nodes",
+ * Paper-Notes AAAI 2026, section on the method, "1. FlexDeMo" Algorithm 1,
+ * steps 3-7; "DeMo: Decoupled Momentum Optimization", abstract):
+ *
+ *   per replica r:  m_r <- beta m_r + g_r                       (step 3)
+ *                   split m_r into 32-element chunks; select     (step 4)
+ *                   q_r = the selected component; m_r <- m_r - q_r (step 5)
+ *                   payload_r = q_r's values (ternary sign if asked)
+ *   all replicas:   Y = per-slot mean of the payloads (scatter-mean), (step 6)
+ *                   Q = inverse transform of Y,  theta <- theta - lr Q (step 7)
+ *
+ * Selection ("replication scheme", same page, "2. Replication Schemes" table):
+ *   DEMO_MODE_DEMO    orthonormal DCT-II of the chunk, keep the k coefficients
+ *                     of largest magnitude (exact ties: lowest index u); the
+ *                     payload carries k values and k uint8 indices per chunk,
+ *                     in ascending u order.  Q = inverse DCT (DCT-III) of Y.
+ *   DEMO_MODE_RANDOM  k positions per chunk drawn from the shared seed (no
+ *                     indices sent): draw j of chunk c at step t uses
+ *                     h = H(seed, t, c, j), H(s,t,c,j) = sm(sm(sm(sm(s)^t)^c)^j),
+ *                     sm = the splitmix64 output function, r_j = (h>>32)*(32-j)>>32,
+ *                     position = the r_j-th still-free position (partial
+ *                     Fisher-Yates).  Payload: k values in draw order.  Q = Y.
+ *   DEMO_MODE_STRIDE  positions o + (32/k) j, o = step mod (32/k); k must
+ *                     divide 32.  Payload: k values in j order.  Q = Y.
+ *   DEMO_MODE_DILOCO  on steps with (step+1) mod diloco_period == 0 the whole
+ *                     momentum is sent (32 values per chunk) and m is zeroed;
+ *                     on other steps only step 3 runs and theta is untouched.
+ * The sign flag replaces every sent value by sign(v) in {-1, 0, +1} (same page,
+ * "3. Sign function" subsection); m always subtracts the unsigned q.
+ * The mean of a slot divides by the number of replicas that sent that slot.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named as device pointers are caller-owned device memory of the
+ *     current device, 16-byte aligned, not aliasing one another.  Pointer
+ *     ARRAYS (g, m, vals, idx) are host arrays of R device pointers.
+ *   - n is the shard length, a positive multiple of 32; chunk must be 32.
+ *   - Calls enqueue on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *     and return without synchronising.  The library allocates no memory in
+ *     these calls and keeps no per-shard state.
+ *   - Argument errors are found on the host before anything is launched and
+ *     return a negative status; nothing is printed.  A launch failure returns
+ *     DEMO_ECUDA.  A device-side wait that gives up (a copy that never lands)
+ *     sets a device fault word read by demo_device_fault().
+ *   - Same inputs and (seed, step) give bit-identical outputs; replicas are
+ *     combined in the fixed order r = 0..R-1 (no floating-point atomics).
+ *   - Non-finite inputs produce unspecified values, never out-of-bounds
+ *     accesses.
+ */
+#ifndef DEMO_GB300_H
+#define DEMO_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DEMO_CHUNK 32
+#define DEMO_MAX_REPLICAS 64
+
+enum demo_mode {
+  DEMO_MODE_DEMO = 0,
+  DEMO_MODE_RANDOM = 1,
+  DEMO_MODE_STRIDE = 2,
+  DEMO_MODE_DILOCO = 3
+};
+
+enum demo_grad_dtype {
+  DEMO_GRAD_F32 = 0,  /* float32 gradients */
+  DEMO_GRAD_BF16 = 1  /* bfloat16 gradients, widened exactly to float32 */
+};
+
+enum demo_status {
+  DEMO_OK = 0,
+  DEMO_EINVAL = -1,   /* an argument is out of range or a pointer is NULL */
+  DEMO_EALIGN = -2,   /* a device pointer is not 16-byte aligned */
+  DEMO_ENODEV = -3,   /* no device, or the device is not an sm_103 GPU */
+  DEMO_ECUDA = -4,    /* a CUDA runtime call or a launch failed */
+  DEMO_ENOTINIT = -5  /* demo_init() was not called for the current device */
+};
+
+/*
+ * demo_init -- prepare the library for `device` and make it current.
+ * Checks that the device is compute capability 10.3 (GB300), resolves the
+ * tensor-map encoder from the driver and sets the kernels' shared-memory
+ * limits.  Idempotent; call it once per device before the other calls (and
+ * before any stream capture).  Returns DEMO_OK, DEMO_ENODEV or DEMO_ECUDA.
+ */
+int demo_init(int device);
+
+/*
+ * demo_payload_bytes -- bytes ONE replica sends for one step (host only).
+ * Returns the value bytes (float32); *idx_bytes (if not NULL) receives the
+ * index bytes (uint8, DeMo only).  DeMo: n/32*k*4 values + n/32*k indices;
+ * Random, Striding: n/32*k*4; DiLoCo: 4n on sync steps, else 0.  Returns 0 for
+ * invalid arguments.  Source: "2. Replication Schemes" table, whether a scheme
+ * transmits indices.
+ */
+size_t demo_payload_bytes(int mode, int64_t n, int chunk, int k, uint64_t step,
+                          int diloco_period, size_t* idx_bytes);
+
+/*
+ * demo_encode -- one replica's steps 3-5 plus its payload (the send buffer).
+ *   g       device, n elements of grad_dtype (read only)
+ *   m       device float32 [n], momentum, updated in place to beta m + g - q
+ *   vals    device float32: [n/32][k] (DeMo, Random, Striding) or [n] (DiLoCo
+ *           sync step); may be NULL on DiLoCo non-sync steps
+ *   idx     device uint8 [n/32][k] for DeMo (ascending u per chunk); NULL for
+ *           the other modes
+ *   k       1..32 (Striding: a divisor of 32; ignored by DiLoCo)
+ *   beta    finite float; sign: 0 or 1; diloco_period >= 1 (DiLoCo only)
+ *   seed, step: the shared index seed and the 0-based step counter
+ */
+int demo_encode(const void* g, int grad_dtype, float* m, int64_t n, int chunk, int k,
+                float beta, int mode, int sign, int diloco_period, uint64_t seed,
+                uint64_t step, float* vals, uint8_t* idx, void* stream);
+
+/*
+ * demo_decode_update -- step 6 (scatter-mean of R payloads) and step 7.
+ *   theta   device float32 [n], updated in place to theta - lr Q
+ *   R       1..64 payloads, vals[r] / idx[r] laid out as demo_encode writes
+ *           them (idx only for DeMo; pass NULL otherwise)
+ *   lr      finite float
+ * DiLoCo on a non-sync step leaves theta untouched and launches nothing.
+ * A DeMo index byte is used modulo 32 (it never addresses outside the chunk).
+ */
+int demo_decode_update(float* theta, int64_t n, int chunk, int k, float lr, int mode, int R,
+                       const float* const* vals, const uint8_t* const* idx,
+                       int diloco_period, uint64_t seed, uint64_t step, void* stream);
+
+/*
+ * demo_step -- the fused step: demo_encode for every replica followed by
+ * demo_decode_update, in one pass over memory; the payloads stay on chip.
+ *   theta   device float32 [n], updated in place
+ *   g[r]    device [n] of grad_dtype, r = 0..R-1 (read only)
+ *   m[r]    device float32 [n], updated in place
+ * Same arguments and limits as the split calls; results are bit-identical to
+ * demo_encode (r = 0..R-1) followed by demo_decode_update.
+ */
+int demo_step(float* theta, int64_t n, int chunk, int k, float beta, float lr, int mode,
+              int sign, int R, const void* const* g, int grad_dtype, float* const* m,
+              int diloco_period, uint64_t seed, uint64_t step, void* stream);
+
+/* demo_status_string -- a static, human-readable name for a status code. */
+const char* demo_status_string(int status);
+
+/*
+ * demo_device_fault -- read and clear the fault word of the current device.
+ * Synchronises the device.  *code receives 0 when no kernel gave up on a wait
+ * since the last call, else a bit set (1: a tile load never completed).
+ * Returns DEMO_OK, DEMO_ENOTINIT or DEMO_ECUDA.
+ */
+int demo_device_fault(unsigned int* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DEMO_GB300_H */

@@ -1,0 +1,175 @@
+"""Parity harness: the CUDA library against the float64 oracle, step by step.
+
+Every check is teacher-forced: the oracle takes one step from the GPU's own
+float32 state (promoted exactly to float64), so each step is judged on its own.
+For each step the harness
+
+* runs the split path (demo_encode per replica, demo_decode_update) and the
+  fused path (demo_step) on copies of the same state and requires them to be
+  bit-identical;
+* reads the GPU's Q exactly by decoding the payloads onto a zero theta with
+  lr = -1 (theta' = 0 + 1 * Q);
+* compares against the oracle on the chunks in ``rows`` (all chunks by default):
+  DeMo indices exactly (except chunks the oracle flags as near-ties), Random /
+  Striding positions exactly (the new momentum is exactly 0 there), payload
+  values, m and Q to TOL relative to the chunk's largest magnitude, and the
+  theta update to within one float32 rounding of theta - lr Q.
+"""
+
+import numpy as np
+import torch
+
+import decoupled_momentum_optimizer_gb300 as dm
+import oracle.demo_ref as ref
+
+C = 32
+TOL = 1e-5  # max |gpu - oracle| / max |oracle| per chunk (float32 vs float64)
+
+
+def f64(t):
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def chunk_close(gpu, orc, tol, excl=None):
+    """Per-chunk infinity-norm relative check; returns (bad chunk mask, worst ratio)."""
+    a = gpu.reshape(-1, C)
+    b = orc.reshape(-1, C)
+    num = np.abs(a - b).max(1)
+    den = np.abs(b).max(1)
+    zero = den == 0
+    bad = np.where(zero, num > 0, num > tol * den)
+    if excl is not None:
+        bad &= ~excl
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(zero, np.where(num > 0, np.inf, 0.0), num / np.where(zero, 1, den))
+    if excl is not None:
+        ratio = np.where(excl, 0.0, ratio)
+    return bad, float(ratio.max()) if ratio.size else 0.0
+
+
+def payload_buffers(mode, n, k, step, period, device="cuda"):
+    nc = n // C
+    if mode == "diloco":
+        sync = ref.diloco_is_sync(step, period)
+        vals = torch.zeros(n, device=device) if sync else None
+        return vals, None
+    vals = torch.full((nc * k,), float("nan"), device=device)
+    idx = torch.full((nc * k,), 255, dtype=torch.uint8, device=device) if mode == "demo" else None
+    return vals, idx
+
+
+def gpu_split(theta, ms, gs, *, k, beta, lr, mode, sign, seed, step, period):
+    n = theta.numel()
+    ms2 = [m.clone() for m in ms]
+    vals, idxs = [], []
+    for r in range(len(ms)):
+        v, i = payload_buffers(mode, n, k, step, period)
+        dm.encode(gs[r], ms2[r], v, i, k=k, beta=beta, mode=mode, sign=sign, diloco_period=period, seed=seed,
+                  step=step)
+        vals.append(v)
+        idxs.append(i)
+    th2 = theta.clone()
+    dvals = vals if vals[0] is not None else [torch.zeros(1, device=theta.device)] * len(ms)
+    dm.decode_update(th2, dvals, idxs if mode == "demo" else None, k=k, lr=lr, mode=mode, diloco_period=period,
+                     seed=seed, step=step)
+    Q = torch.zeros_like(theta)
+    dm.decode_update(Q, dvals, idxs if mode == "demo" else None, k=k, lr=-1.0, mode=mode, diloco_period=period,
+                     seed=seed, step=step)
+    return th2, ms2, vals, idxs, Q
+
+
+def gpu_fused(theta, ms, gs, *, k, beta, lr, mode, sign, seed, step, period):
+    th2 = theta.clone()
+    ms2 = [m.clone() for m in ms]
+    dm.step(th2, gs, ms2, k=k, beta=beta, lr=lr, mode=mode, sign=sign, diloco_period=period, seed=seed, step=step)
+    return th2, ms2
+
+
+def check_step(theta, ms, gs, *, k, beta, lr, mode, sign, seed=0, step=0, period=8, rows=None, tol=TOL,
+               stats=None):
+    """One teacher-forced step (see module docstring); returns the fused path's new (theta, ms)."""
+    n = theta.numel()
+    nc = n // C
+    R = len(ms)
+    th_s, ms_s, vals, idxs, Q = gpu_split(theta, ms, gs, k=k, beta=beta, lr=lr, mode=mode, sign=sign, seed=seed,
+                                          step=step, period=period)
+    th_f, ms_f = gpu_fused(theta, ms, gs, k=k, beta=beta, lr=lr, mode=mode, sign=sign, seed=seed, step=step,
+                           period=period)
+    torch.cuda.synchronize()
+    assert torch.equal(th_f, th_s), "fused and split theta differ"
+    for r in range(R):
+        assert torch.equal(ms_f[r], ms_s[r]), f"fused and split m[{r}] differ"
+
+    if rows is None:
+        rows = np.arange(nc)
+    rows = np.asarray(rows, dtype=np.int64)
+    el = (rows[:, None] * C + np.arange(C)[None, :]).reshape(-1)
+    el_t = torch.from_numpy(el).to(theta.device)
+
+    def pick(t):
+        return f64(t.index_select(0, el_t))
+
+    th0 = pick(theta)
+    m0 = [pick(m) for m in ms]
+    g0 = [pick(g) for g in gs]
+    th1, m1, info = ref.step(th0, m0, g0, beta=beta, lr=lr, k=k, mode=ref.__dict__["MODE_" + mode.upper()],
+                             sign=sign, seed=seed, step_idx=step, period=period, chunk_ids=rows)
+    excl = info["near_tie"].copy()
+    nrows = len(rows)
+
+    for r in range(R):
+        enc = info["encodes"][r]
+        mg = pick(ms_f[r]).reshape(nrows, C)
+        if mode == "demo":
+            gi = idxs[r].view(nc, k).index_select(0, torch.from_numpy(rows).to(theta.device)).cpu().numpy()
+            gv = f64(vals[r].view(nc, k).index_select(0, torch.from_numpy(rows).to(theta.device)))
+            oi = enc["idx"]
+            same = (gi == oi).all(1)
+            assert (same | excl).all(), f"DeMo indices differ in {(~same & ~excl).sum()} non-tied chunks"
+            X = enc["X"]
+            ov = np.take_along_axis(X, oi, axis=1)
+            if sign:
+                ov = np.sign(ov)
+                okv = (gv == ov).all(1)
+                assert (okv | excl).all(), "signed DeMo payload values differ"
+            else:
+                scale = np.abs(X).max(1, keepdims=True)
+                errv = np.abs(gv - ov) <= tol * np.where(scale == 0, 1, scale)
+                assert (errv.all(1) | excl).all(), "DeMo payload values differ"
+        elif mode in ("random", "stride"):
+            pos = enc["pos"]
+            at = np.take_along_axis(mg, pos, axis=1)
+            assert (at == 0.0).all(), "new momentum is not exactly 0 at the oracle's positions"
+            gv = f64(vals[r].view(nc, k).index_select(0, torch.from_numpy(rows).to(theta.device)))
+            ov = enc["vals"]
+            if sign:
+                assert np.array_equal(gv, ov), "signed payload values differ"
+            else:
+                bad, worst = chunk_close(gv, ov, tol)
+                assert not bad.any(), f"payload values differ (worst {worst:.3g})"
+        elif mode == "diloco" and enc["vals"] is not None:
+            gv = pick(vals[r]).reshape(nrows, C)
+            if sign:
+                assert np.array_equal(gv, enc["vals"]), "signed DiLoCo payload differs"
+            else:
+                bad, worst = chunk_close(gv, enc["vals"], tol)
+                assert not bad.any(), f"DiLoCo payload differs (worst {worst:.3g})"
+        bad, worst = chunk_close(mg, m1[r], tol, excl)
+        assert not bad.any(), f"m[{r}] differs in {bad.sum()} chunks (worst {worst:.3g})"
+
+    Qg = pick(Q)
+    bad, worst = chunk_close(Qg, info["Q"], tol, excl)
+    assert not bad.any(), f"Q differs in {bad.sum()} chunks (worst {worst:.3g})"
+
+    # theta' = theta - lr Q with one float32 rounding (checked to one ulp)
+    want = (th0 - ref.f32(lr) * Qg).astype(np.float32)
+    got = pick(th_f).astype(np.float32)
+    ulp = np.spacing(np.maximum(np.abs(want), np.abs(got)).astype(np.float32))
+    assert (np.abs(got.astype(np.float64) - want.astype(np.float64)) <= ulp).all(), "theta update is not theta - lr Q"
+
+    if stats is not None:
+        stats.setdefault("near_tie", 0)
+        stats["near_tie"] += int(excl.sum())
+        stats.setdefault("chunks", 0)
+        stats["chunks"] += nrows
+    return th_f, ms_f

@@ -1,0 +1,147 @@
+"""The C ABI without a GPU: the library builds, loads, exports every declared
+entry point, and its host-only logic (argument checks, payload sizes, status
+strings) behaves as include/demo.h states.  No call here reaches a kernel:
+argument checks run before any CUDA call, and valid arguments stop at
+DEMO_ENOTINIT / DEMO_ENODEV on a machine without a GPU.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle.demo_ref as ref
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "demo.h")
+
+OK, EINVAL, EALIGN, ENODEV, ECUDA, ENOTINIT = 0, -1, -2, -3, -4, -5
+
+
+@pytest.fixture(scope="module")
+def L():
+    from decoupled_momentum_optimizer_gb300 import build
+
+    build.build()
+    import decoupled_momentum_optimizer_gb300 as dm
+
+    return dm.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(demo_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert "demo_step" in names and "demo_encode" in names and "demo_decode_update" in names
+    for name in names:
+        assert hasattr(L, name), f"{name} declared in demo.h but not exported"
+
+
+def test_status_strings(L):
+    for code in (OK, EINVAL, EALIGN, ENODEV, ECUDA, ENOTINIT):
+        assert L.demo_status_string(code).decode().startswith("DEMO_")
+    assert b"UNKNOWN" in L.demo_status_string(12345)
+
+
+def test_payload_bytes_match_oracle(L):
+    import decoupled_momentum_optimizer_gb300 as dm
+
+    for mode in ("demo", "random", "stride", "diloco"):
+        for n in (32, 65536, 222903552):
+            for k in (1, 2, 4, 8, 32):
+                for step in (0, 6, 7):
+                    got = dm.payload_bytes(mode, n, k, step=step, diloco_period=8)
+                    want = ref.payload_bytes(dm.MODES[mode], n, k, step=step, period=8)
+                    assert got == want, (mode, n, k, step)
+    assert dm.payload_bytes("stride", 64, 3) == (0, 0)  # invalid: 3 does not divide 32
+    assert dm.payload_bytes("demo", 33, 4) == (0, 0)
+
+
+F = ctypes.c_void_p
+
+
+def p(a):
+    return ctypes.c_void_p(a)
+
+
+def encode_call(L, **kw):
+    a = dict(g=p(0x10000), gd=0, m=p(0x20000), n=64, chunk=32, k=4, beta=0.9, mode=0, sign=1, period=8, seed=0,
+             step=0, vals=p(0x30000), idx=p(0x40000), stream=None)
+    a.update(kw)
+    return L.demo_encode(a["g"], a["gd"], a["m"], a["n"], a["chunk"], a["k"], a["beta"], a["mode"], a["sign"],
+                         a["period"], a["seed"], a["step"], a["vals"], a["idx"], a["stream"])
+
+
+def step_call(L, R=2, **kw):
+    gs = kw.pop("gs", [0x100000 * (r + 1) for r in range(R)])
+    ms = kw.pop("ms", [0x1000000 * (r + 1) for r in range(R)])
+    a = dict(theta=p(0x500000000), n=64, chunk=32, k=4, beta=0.9, lr=0.1, mode=0, sign=1, R=R, gd=0, period=8,
+             seed=0, step=0, stream=None)
+    a.update(kw)
+    garr = (ctypes.c_void_p * max(1, len(gs)))(*gs)
+    marr = (ctypes.c_void_p * max(1, len(ms)))(*ms)
+    return L.demo_step(a["theta"], a["n"], a["chunk"], a["k"], a["beta"], a["lr"], a["mode"], a["sign"], a["R"],
+                       garr, a["gd"], marr, a["period"], a["seed"], a["step"], a["stream"])
+
+
+def test_encode_argument_checks(L):
+    assert encode_call(L, chunk=16) == EINVAL
+    assert encode_call(L, n=0) == EINVAL
+    assert encode_call(L, n=48) == EINVAL
+    assert encode_call(L, k=0) == EINVAL
+    assert encode_call(L, k=33) == EINVAL
+    assert encode_call(L, mode=2, k=3) == EINVAL
+    assert encode_call(L, mode=7) == EINVAL
+    assert encode_call(L, sign=2) == EINVAL
+    assert encode_call(L, gd=5) == EINVAL
+    assert encode_call(L, beta=float("nan")) == EINVAL
+    assert encode_call(L, g=None) == EINVAL
+    assert encode_call(L, idx=None) == EINVAL  # DeMo needs indices
+    assert encode_call(L, mode=3, period=0) == EINVAL
+    assert encode_call(L, g=p(0x10004)) == EALIGN
+    assert encode_call(L, vals=p(0x30008)) == EALIGN
+    assert encode_call(L, m=p(0x10000)) == EINVAL  # m overlaps g
+    # valid arguments reach the device check
+    assert encode_call(L) in (ENOTINIT, ENODEV)
+    assert encode_call(L, mode=1, idx=None) in (ENOTINIT, ENODEV)
+    assert encode_call(L, mode=3, vals=None, step=0, period=8) in (ENOTINIT, ENODEV)  # no payload off-sync
+    assert encode_call(L, mode=3, vals=None, step=7, period=8) == EINVAL  # sync step needs a payload buffer
+
+
+def test_step_argument_checks(L):
+    assert step_call(L, R=0, gs=[], ms=[]) == EINVAL
+    assert step_call(L, R=65, gs=[0x100000 * (r + 1) for r in range(65)],
+                     ms=[0x100000000 + 0x1000000 * r for r in range(65)]) == EINVAL
+    assert step_call(L, lr=float("inf")) == EINVAL
+    assert step_call(L, theta=None) == EINVAL
+    assert step_call(L, theta=p(0x500000004)) == EALIGN
+    assert step_call(L, ms=[0x1000000, 0x1000000]) == EINVAL  # two replicas share one momentum buffer
+    assert step_call(L, ms=[0x1000000, 0x500000000]) == EINVAL  # a momentum buffer is theta
+    assert step_call(L, gs=[0x100000, 0x100000]) in (ENOTINIT, ENODEV)  # shared read-only gradient is fine
+    assert step_call(L) in (ENOTINIT, ENODEV)
+
+
+def test_decode_argument_checks(L):
+    vals = (ctypes.c_void_p * 2)(0x30000, 0x40000)
+    idx = (ctypes.c_void_p * 2)(0x50000, 0x60000)
+    th = p(0x70000)
+    assert L.demo_decode_update(th, 64, 32, 4, 0.1, 0, 2, vals, None, 8, 0, 0, None) == EINVAL
+    assert L.demo_decode_update(th, 64, 32, 4, 0.1, 0, 0, vals, idx, 8, 0, 0, None) == EINVAL
+    bad = (ctypes.c_void_p * 2)(0x30000, 0x40001)
+    assert L.demo_decode_update(th, 64, 32, 4, 0.1, 1, 2, bad, None, 8, 0, 0, None) == EALIGN
+    assert L.demo_decode_update(th, 64, 32, 4, 0.1, 0, 2, vals, idx, 8, 0, 0, None) in (ENOTINIT, ENODEV)
+
+
+def test_init_without_device(L):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert L.demo_init(0) == ENODEV
+    code = ctypes.c_uint(0)
+    assert L.demo_device_fault(ctypes.byref(code)) == ENOTINIT
