@@ -274,6 +274,7 @@ def main():
 
     import decoupled_momentum_optimizer_gb300 as dm
     from decoupled_momentum_optimizer_gb300 import workloads as W
+    from decoupled_momentum_optimizer_gb300.sharding import shard_seed
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -302,8 +303,10 @@ def main():
     scratch = torch.empty(256 * 1024 * 1024 // 4, device=dev) if flush else None
     stream = torch.cuda.current_stream()
 
+    seed = shard_seed(0, rank)  # each GPU steps its own shard with its own index seed
+
     def one_step(t):
-        dm.step(theta, ring[t % 3], ms, k=k, beta=wl.beta, lr=wl.lr, mode=mode, sign=sign, seed=0, step=t,
+        dm.step(theta, ring[t % 3], ms, k=k, beta=wl.beta, lr=wl.lr, mode=mode, sign=sign, seed=seed, step=t,
                 stream=stream)
 
     for t in range(args.warmup):

@@ -30,12 +30,19 @@ def f64(t):
     return t.detach().to(torch.float64).cpu().numpy()
 
 
-def chunk_close(gpu, orc, tol, excl=None):
-    """Per-chunk infinity-norm relative check; returns (bad chunk mask, worst ratio)."""
+def chunk_close(gpu, orc, tol, excl=None, scale=None):
+    """Per-chunk infinity-norm relative check; returns (bad chunk mask, worst ratio).
+
+    The denominator is the chunk's largest oracle magnitude, or the largest
+    magnitude of ``scale`` when that is bigger (for results that cancel, such as
+    the momentum left after the subtraction, the error scale is the input's).
+    """
     a = gpu.reshape(-1, C)
     b = orc.reshape(-1, C)
     num = np.abs(a - b).max(1)
     den = np.abs(b).max(1)
+    if scale is not None:
+        den = np.maximum(den, np.abs(scale.reshape(-1, C)).max(1))
     zero = den == 0
     bad = np.where(zero, num > 0, num > tol * den)
     if excl is not None:
@@ -154,7 +161,8 @@ def check_step(theta, ms, gs, *, k, beta, lr, mode, sign, seed=0, step=0, period
             else:
                 bad, worst = chunk_close(gv, enc["vals"], tol)
                 assert not bad.any(), f"DiLoCo payload differs (worst {worst:.3g})"
-        bad, worst = chunk_close(mg, m1[r], tol, excl)
+        x = ref.f32(beta) * m0[r] + g0[r]  # the momentum before the subtraction of q
+        bad, worst = chunk_close(mg, m1[r], tol, excl, scale=x)
         assert not bad.any(), f"m[{r}] differs in {bad.sum()} chunks (worst {worst:.3g})"
 
     Qg = pick(Q)
