@@ -12,8 +12,9 @@ For each step the harness
 * compares against the oracle on the chunks in ``rows`` (all chunks by default):
   DeMo indices exactly (except chunks the oracle flags as near-ties), Random /
   Striding positions exactly (the new momentum is exactly 0 there), payload
-  values, m and Q to TOL relative to the chunk's largest magnitude, and the
-  theta update to within one float32 rounding of theta - lr Q.
+  values and Q to TOL relative to the chunk's largest magnitude, m to TOL
+  relative to the larger of that and the chunk's momentum before the
+  subtraction (k = 32 cancels it to rounding noise), and the theta update to within one float32 rounding of theta - lr Q.
 """
 
 import numpy as np
