@@ -85,8 +85,8 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t nc, bool bf16) {
   return r == CUDA_SUCCESS;
 }
 
-int grid_for(int64_t ntiles, const DeviceState* st) {
-  const int64_t want = (ntiles + kWarps - 1) / kWarps;
+int grid_for(int64_t ntiles, const DeviceState* st, int warps_per_cta = kWarps) {
+  const int64_t want = (ntiles + warps_per_cta - 1) / warps_per_cta;
   return static_cast<int>(want < st->sms ? want : st->sms);
 }
 
@@ -125,9 +125,11 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
   const int64_t nc = n / DEMO_CHUNK;
   const bool bf16 = grad_dtype == DEMO_GRAD_BF16;
   if (!make_map(&p.theta, theta, nc, false)) return DEMO_ECUDA;
+  p.theta_ptr = theta;
   for (int r = 0; r < R; ++r) {
     if (!make_map(&p.g[r], g[r], nc, bf16)) return DEMO_ECUDA;
     if (!make_map(&p.m[r], m[r], nc, false)) return DEMO_ECUDA;
+    p.m_ptr[r] = m[r];
   }
   p.nc = nc;
   p.ntiles = (nc + 31) / 32;
@@ -142,7 +144,7 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
   p.rcpR = 1.0f / static_cast<float>(R);
   fill_rcp(p);
   p.fault = st->fault;
-  const int grid = grid_for(p.ntiles, st);
+  const int grid = grid_for(p.ntiles, st, kStepWarps);
   cudaError_t e;
   if constexpr (MAXR == kSmallReplicas) {
     e = launch_step_small(p, mode, bf16, grid, stream);

@@ -130,6 +130,26 @@ __device__ __forceinline__ void store_row_f32(float* tile, int row, const float 
   }
 }
 
+// Write the warp's tile (row `lane` held by each lane in v) to rows [row0, row0 + 32)
+// of a row-major [nrows][32] float array.  The rows go through the swizzled
+// 4 KB shared tile `buf` and are read back transposed, so every 16-byte global
+// store instruction covers 512 contiguous bytes.  Rows at or past nrows are not
+// written.  `buf` may be reused as soon as the call returns and the warp has
+// synchronised.
+__device__ __forceinline__ void store_tile_coalesced(float* buf, int lane, const float (&v)[32], float* gbase,
+                                                     long long row0, long long nrows) {
+  store_row_f32(buf, lane, v);
+  __syncwarp();
+  const char* b = reinterpret_cast<const char*>(buf);
+  const int j = lane & 7;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int r = q * 4 + (lane >> 3);
+    const float4 val = *reinterpret_cast<const float4*>(b + r * 128 + ((j ^ (r & 7)) << 4));
+    if (row0 + r < nrows) reinterpret_cast<float4*>(gbase + (row0 + r) * 32)[j] = val;
+  }
+}
+
 __device__ __forceinline__ void load_row_bf16(const void* tile, int row, float (&v)[32]) {
   const char* base = reinterpret_cast<const char*>(tile) + row * 64;
 #pragma unroll

@@ -16,6 +16,8 @@ struct StepParams {
   CUtensorMap theta;
   CUtensorMap g[MAXR];
   CUtensorMap m[MAXR];
+  float* theta_ptr;  // the same buffers as raw pointers, for the coalesced stores
+  float* m_ptr[MAXR];
   long long nc;      // chunks in the shard
   long long ntiles;  // ceil(nc / 32)
   int R, k, sign;
@@ -56,8 +58,9 @@ struct DecodeParams {
   unsigned int* fault;
 };
 
-// Launchers (one per translation unit).  `grid` CTAs of 8 warps; each warp
-// walks the tiles gw, gw + 8*grid, ...
+// Launchers (one per translation unit).  `grid` CTAs of kStepWarps (fused
+// step) or kWarps (split path) warps; each warp walks the tiles gw, gw + W*grid, ...
+constexpr int kStepWarps = 11;
 cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, bool bf16, int grid, cudaStream_t st);
 cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int grid, cudaStream_t st);
 cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int grid, cudaStream_t st);

@@ -8,39 +8,43 @@
 //
 // Per warp, a tile is 32 chunks (one per lane) and is visited as R + 1 items:
 // item r < R streams g_r and m_r through TMA into a two-slot ring, computes the
-// replica's encode in registers and writes m_r back through TMA; the last item
-// streams theta, turns the accumulated payloads into Q and writes theta back.
-// The load for item i + 2 is issued as soon as item i has been read, so two
-// tiles' worth of copies overlap the arithmetic of each warp.
+// replica's encode in registers and writes m_r back; the last item streams
+// theta, turns the accumulated payloads into Q and writes theta back.  Results
+// leave through the item's own slot: each lane writes its row into the
+// swizzled tile, the warp reads it back transposed and issues 512-byte
+// coalesced stores, and the slot is immediately refilled with the load for
+// item i + 2.  Shared memory per warp is 20 KB (two 8 KB slots and a 4 KB
+// payload accumulator), so 11 warps fit on an SM.
 #include "demo_common.cuh"
 #include "demo_params.h"
 
 namespace demo {
 
 struct alignas(1024) StepWarpSmem {
-  float gbuf[2][1024];   // slot s: g_r tile (f32 or bf16) or the theta tile
-  float mbuf[2][1024];   // slot s: m_r tile
-  float out[1024];       // TMA-store staging; also a [u][lane] scratch column per lane
-  float2 acc[32 * 32];   // DeMo scatter-mean accumulators [u][lane] = (sum, count)
+  float gbuf[2][1024];  // slot s: g_r tile (f32 or bf16), later the stash of kept coefficients; or theta
+  float mbuf[2][1024];  // slot s: m_r tile, later the new m_r on its way out
+  float acc[32 * 32];   // DeMo: per-lane payload sums [u][lane]
 };
 
-constexpr size_t kStepSmem = 1024 + kWarps * sizeof(StepWarpSmem) + kWarps * 16 + 272;
+constexpr int kStepThreads = kStepWarps * 32;
+constexpr size_t kStepSmem = 1024 + kStepWarps * sizeof(StepWarpSmem) + kStepWarps * 16 + 272;
+static_assert(kStepSmem <= 232448, "shared memory per CTA");
 
 template <int MODE, bool BF16, int MAXR>
-__global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepParams<MAXR> p) {
+__global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_constant__ StepParams<MAXR> p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   StepWarpSmem& ws = reinterpret_cast<StepWarpSmem*>(base)[warp];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kWarps * sizeof(StepWarpSmem)) + 2 * warp;
-  float* rcp = reinterpret_cast<float*>(base + kWarps * sizeof(StepWarpSmem) + kWarps * 16);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kStepWarps * sizeof(StepWarpSmem)) + 2 * warp;
+  float* rcp = reinterpret_cast<float*>(base + kStepWarps * sizeof(StepWarpSmem) + kStepWarps * 16);
   if (threadIdx.x <= kMaxReplicas) rcp[threadIdx.x] = p.rcp_tab[threadIdx.x];
   __syncthreads();
 
-  const long long gw = static_cast<long long>(blockIdx.x) * kWarps + warp;
-  const long long TW = static_cast<long long>(gridDim.x) * kWarps;
+  const long long gw = static_cast<long long>(blockIdx.x) * kStepWarps + warp;
+  const long long TW = static_cast<long long>(gridDim.x) * kStepWarps;
   if (gw >= p.ntiles) return;
   const long long ntw = (p.ntiles - 1 - gw) / TW + 1;
   const bool theta_item = !(MODE == kModeDiloco && !p.sync);
@@ -54,7 +58,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   }
   if constexpr (MODE == kModeDemo) {
 #pragma unroll
-    for (int u = 0; u < 32; ++u) ws.acc[u * 32 + lane] = make_float2(0.0f, 0.0f);
+    for (int u = 0; u < 32; ++u) ws.acc[u * 32 + lane] = 0.0f;
   }
   __syncwarp();
 
@@ -78,18 +82,21 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     issue(1);
   }
 
-  uint32_t P = 0;    // Random / Striding / DiLoCo: positions sent from this lane's chunk
-  float accr[32];    // Random / Striding / DiLoCo: per-position payload sums
+  uint32_t P = 0;       // Random / Striding / DiLoCo: positions sent from this lane's chunk
+  float accr[32];       // Random / Striding / DiLoCo: per-position payload sums
+  uint32_t cnt8[8];     // DeMo: byte (u & 3) of cnt8[u >> 2] counts the replicas that sent slot u
 #pragma unroll
   for (int i = 0; i < 32; ++i) accr[i] = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) cnt8[i] = 0u;
 
   for (long long item = 0; item < nitems; ++item) {
     const int s = static_cast<int>(item & 1);
     const uint32_t par = static_cast<uint32_t>((item >> 1) & 1);
     const long long t = gw + (item / ipt) * TW;
     const int kind = static_cast<int>(item % ipt);
-    const int y = static_cast<int>(t * 32);
-    const long long c = t * 32 + lane;
+    const long long row0 = t * 32;
+    const long long c = row0 + lane;
 
     const bool ok = mbar_wait_bounded(&bars[s], par);
     if (!__all_sync(0xffffffffu, ok)) {
@@ -97,7 +104,6 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         atomicOr(p.fault, kFaultLoadTimeout);
         for (long long it = item; it < item + 2 && it < nitems; ++it)
           mbar_wait_bounded(&bars[it & 1], static_cast<uint32_t>((it >> 1) & 1));
-        bulk_wait_all();
       }
       __syncwarp();
       return;
@@ -107,7 +113,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       if constexpr (MODE == kModeRandom) P = random_mask(p.hbase, static_cast<uint64_t>(c), p.k);
       if constexpr (MODE == kModeStride) P = p.stride_mask;
       if constexpr (MODE == kModeDiloco) P = 0xffffffffu;
-      if constexpr (MODE != kModeDemo) {
+      if constexpr (MODE == kModeDemo) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cnt8[i] = 0u;
+      } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) accr[i] = 0.0f;
       }
@@ -120,31 +129,25 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       load_row_f32(ws.mbuf[s], lane, x);
 #pragma unroll
       for (int i = 0; i < 32; ++i) x[i] = __fmaf_rn(p.beta, x[i], gv[i]);
-      __syncwarp();
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        issue(item + 2);
-        bulk_wait_read_all();  // the previous store has left `out`
-      }
-      __syncwarp();
 
       if constexpr (MODE == kModeDemo) {
         float X[32], Xs[32];
         dct32_forward(x, X);
         const uint32_t M = topk_select(X, p.k, Xs);
+        __syncwarp();  // every lane has read its g row: the g tile becomes the stash
+        float* stash = ws.gbuf[s];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) ws.out[u * 32 + lane] = Xs[u];
+        for (int u = 0; u < 32; ++u) stash[u * 32 + lane] = Xs[u];
         uint32_t mm = M;
         for (int j = 0; j < p.k; ++j) {  // payload in ascending u
           const int u = __ffs(mm) - 1;
           mm &= mm - 1;
-          float v = ws.out[u * 32 + lane];
+          float v = stash[u * 32 + lane];
           if (p.sign) v = sign3(v);
-          float2 a = ws.acc[u * 32 + lane];
-          a.x += v;
-          a.y += 1.0f;
-          ws.acc[u * 32 + lane] = a;
+          ws.acc[u * 32 + lane] += v;
         }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cnt8[i] += (((M >> (4 * i)) & 0xfu) * 0x204081u) & 0x01010101u;
         float q[32];
         dct32_inverse(Xs, q);
 #pragma unroll
@@ -166,32 +169,19 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
           x[i] = in ? 0.0f : x[i];
         }
       }
-
-      __syncwarp();
-      store_row_f32(ws.out, lane, x);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(&p.m[kind], ws.out, 0, y);
-        bulk_commit();
-      }
+      store_tile_coalesced(ws.mbuf[s], lane, x, p.m_ptr[kind], row0, p.nc);
     } else {
       // ---- decode: Q from the accumulated payloads, theta <- theta - lr Q
       float th[32];
       load_row_f32(ws.gbuf[s], lane, th);
-      __syncwarp();
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        issue(item + 2);
-      }
       float Q[32];
       if constexpr (MODE == kModeDemo) {
         float Y[32];
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
-          const float2 a = ws.acc[u * 32 + lane];
-          Y[u] = a.x * rcp[static_cast<int>(a.y)];
-          ws.acc[u * 32 + lane] = make_float2(0.0f, 0.0f);
+          const uint32_t cnt = (cnt8[u >> 2] >> (8 * (u & 3))) & 0xffu;
+          Y[u] = ws.acc[u * 32 + lane] * rcp[cnt];
+          ws.acc[u * 32 + lane] = 0.0f;
         }
         dct32_inverse(Y, Q);
       } else {
@@ -200,25 +190,22 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       }
 #pragma unroll
       for (int i = 0; i < 32; ++i) th[i] = __fmaf_rn(-p.lr, Q[i], th[i]);
-      if (lane == 0) bulk_wait_read_all();
-      __syncwarp();
-      store_row_f32(ws.out, lane, th);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(&p.theta, ws.out, 0, y);
-        bulk_commit();
-      }
+      __syncwarp();  // every lane has read its theta row
+      store_tile_coalesced(ws.gbuf[s], lane, th, p.theta_ptr, row0, p.nc);
     }
+
+    // The slot has been read and written back: refill it with item + 2.
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) issue(item + 2);
   }
-  if (lane == 0) bulk_wait_all();
 }
 
 template <int MAXR>
 static cudaError_t launch_step_t(const StepParams<MAXR>& p, int mode, bool bf16, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kStepThreads);
   cfg.dynamicSmemBytes = kStepSmem;
   cfg.stream = st;
 #define DEMO_LAUNCH(M, B) \

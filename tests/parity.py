@@ -12,7 +12,10 @@ For each step the harness
 * compares against the oracle on the chunks in ``rows`` (all chunks by default):
   DeMo indices exactly (except chunks the oracle flags as near-ties), Random /
   Striding positions exactly (the new momentum is exactly 0 there), payload
-  values and Q to TOL relative to the chunk's largest magnitude, m to TOL
+  values to TOL relative to the chunk's largest magnitude; Q against the
+  oracle's decode of the GPU's own payloads to TOL, and against the oracle's
+  own Q to TOL relative to the mean of the summands' magnitudes (a mean of
+  nearly opposite values cancels float32 rounding up); m to TOL
   relative to the larger of that and the chunk's momentum before the
   subtraction (k = 32 cancels it to rounding noise), and the theta update to within one float32 rounding of theta - lr Q.
 """
@@ -38,12 +41,13 @@ def chunk_close(gpu, orc, tol, excl=None, scale=None):
     magnitude of ``scale`` when that is bigger (for results that cancel, such as
     the momentum left after the subtraction, the error scale is the input's).
     """
-    a = gpu.reshape(-1, C)
-    b = orc.reshape(-1, C)
+    a = gpu if gpu.ndim == 2 else gpu.reshape(-1, C)
+    b = orc if orc.ndim == 2 else orc.reshape(-1, C)
     num = np.abs(a - b).max(1)
     den = np.abs(b).max(1)
     if scale is not None:
-        den = np.maximum(den, np.abs(scale.reshape(-1, C)).max(1))
+        sc = scale if scale.ndim == 2 else scale.reshape(-1, C)
+        den = np.maximum(den, np.abs(sc).max(1))
     zero = den == 0
     bad = np.where(zero, num > 0, num > tol * den)
     if excl is not None:
@@ -167,7 +171,28 @@ def check_step(theta, ms, gs, *, k, beta, lr, mode, sign, seed=0, step=0, period
         assert not bad.any(), f"m[{r}] differs in {bad.sum()} chunks (worst {worst:.3g})"
 
     Qg = pick(Q)
-    bad, worst = chunk_close(Qg, info["Q"], tol, excl)
+    # decode alone: the oracle's scatter-mean and inverse transform of the GPU's own payloads
+    gpu_vals, gpu_pos = [], []
+    for r in range(R):
+        enc = info["encodes"][r]
+        if enc["vals"] is None:
+            continue
+        if mode == "diloco":
+            gpu_vals.append(pick(vals[r]).reshape(nrows, C))
+            gpu_pos.append(enc["pos"])
+        else:
+            rt = torch.from_numpy(rows).to(theta.device)
+            gpu_vals.append(f64(vals[r].view(nc, k).index_select(0, rt)))
+            gpu_pos.append(idxs[r].view(nc, k).index_select(0, rt).cpu().numpy().astype(np.int64)
+                           if mode == "demo" else enc["pos"])
+    _, Qd, _, _ = ref.decode_update(np.zeros(nrows * C), gpu_vals, gpu_pos, 0.0,
+                                    ref.__dict__["MODE_" + mode.upper()])
+    bad, worst = chunk_close(Qg, Qd, tol)
+    assert not bad.any(), f"decode of the GPU payloads: Q differs in {bad.sum()} chunks (worst {worst:.3g})"
+    # end to end: the mean of R replicas can cancel, so the error scale is the mean of |values|
+    Yabs, _ = ref.scatter_mean([None if e["vals"] is None else np.abs(e["vals"]) for e in info["encodes"]],
+                               [e["pos"] for e in info["encodes"]], nrows)
+    bad, worst = chunk_close(Qg, info["Q"], tol, excl, scale=Yabs)
     assert not bad.any(), f"Q differs in {bad.sum()} chunks (worst {worst:.3g})"
 
     # theta' = theta - lr Q with one float32 rounding (checked to one ulp)
