@@ -46,6 +46,7 @@ def parse_args():
     p.add_argument("--R", type=int, default=None)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--sweep", default=None, help="measure every configuration of the results table into this JSONL file")
     return p.parse_args()
 
 
@@ -264,16 +265,181 @@ def run_reference(args):
 # Our arm
 # ----------------------------------------------------------------------------
 
+class Case:
+    """Device state for one (workload, R) measurement: theta, m_r and gradient sets."""
+
+    def __init__(self, wl, R, dev, n_sets):
+        import torch
+
+        from decoupled_momentum_optimizer_gb300 import workloads as W
+
+        self.wl, self.R, self.n = wl, R, wl.n
+        self.theta = W.make_theta0(wl, dev)
+        self.ms = [torch.zeros(wl.n, device=dev) for _ in range(R)]
+        streams = [W.GradStream(wl, r, dev) for r in range(R)]
+        self.ring = [[s.next() for s in streams] for _ in range(n_sets)]
+        self.grad_bytes = self.ring[0][0].element_size()
+
+
+def time_fused(dm, case, mode, k, sign, seed, steps, warmup, stream, per_launch=True, sampler=None,
+               step0=0, diloco_period=8):
+    """Mean step and mean launch time (ms) of demo_step over ``steps`` timed steps."""
+    import torch
+
+    wl = case.wl
+    flush = algorithmic_bytes(case.n, case.R, case.grad_bytes, mode) < 2 * L2_BYTES
+    scratch = torch.empty(256 * 1024 * 1024 // 4, device=case.theta.device) if flush else None
+
+    def one(t):
+        dm.step(case.theta, case.ring[t % len(case.ring)], case.ms, k=k, beta=wl.beta, lr=wl.lr, mode=mode,
+                sign=sign, seed=seed, step=t, diloco_period=diloco_period, stream=stream)
+
+    for t in range(warmup):
+        one(step0 + t)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    ctx = sampler if sampler is not None else _Null()
+    with ctx:
+        a.record(stream)
+        for i in range(steps):
+            if flush:
+                scratch.fill_(float(i))
+            ev[i][0].record(stream)
+            one(step0 + warmup + i)
+            ev[i][1].record(stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+    launch = sum(x.elapsed_time(y) for x, y in ev) / steps
+    step = launch if flush else a.elapsed_time(b) / steps
+    return step, launch, flush
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def time_split(dm, case, mode, k, sign, seed, steps, warmup, stream, diloco_period=8, step0=0):
+    """Mean time (ms) of R demo_encode calls + one demo_decode_update (the wire-format path)."""
+    import torch
+
+    wl, n, R = case.wl, case.n, case.R
+    nc = n // 32
+    dev = case.theta.device
+    if mode == "diloco":
+        vals = [torch.empty(n, device=dev) for _ in range(R)]
+        idx = None
+    else:
+        vals = [torch.empty(nc * k, device=dev) for _ in range(R)]
+        idx = [torch.empty(nc * k, dtype=torch.uint8, device=dev) for _ in range(R)] if mode == "demo" else None
+
+    def one(t):
+        g = case.ring[t % len(case.ring)]
+        for r in range(R):
+            dm.encode(g[r], case.ms[r], vals[r], idx[r] if idx else None, k=k, beta=wl.beta, mode=mode, sign=sign,
+                      diloco_period=diloco_period, seed=seed, step=t, stream=stream)
+        dm.decode_update(case.theta, vals, idx, k=k, lr=wl.lr, mode=mode, diloco_period=diloco_period, seed=seed,
+                         step=t, stream=stream)
+
+    for t in range(warmup):
+        one(step0 + t)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(steps):
+        one(step0 + warmup + i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def split_bytes(n, R, grad_bytes, mode, k, sync=True):
+    """Algorithmic bytes of the split path: R encodes (g, m, payload out) + decode (R payloads in, theta)."""
+    nc = n // 32
+    if mode == "demo":
+        P = nc * k * 5
+    elif mode in ("random", "stride"):
+        P = nc * k * 4
+    else:
+        P = 4 * n if sync else 0
+    theta = 8 * n if (mode != "diloco" or sync) else 0
+    return R * (n * (grad_bytes + 8) + P) + (R * P + theta if theta else 0)
+
+
+def time_e2e(dm, case, mode, k, sign, seed, steps, dev):
+    """End to end through the public API: every step copies its R gradients from pinned host memory
+    and reads theta back to pinned host memory.  The copies of step t+1's gradients overlap step t."""
+    import torch
+
+    wl, n, R = case.wl, case.n, case.R
+    host_g = [[g.cpu().pin_memory() for g in case.ring[i % len(case.ring)]] for i in range(2)]
+    host_theta = torch.empty(n, dtype=torch.float32).pin_memory()
+    dev_g = [[torch.empty_like(g) for g in case.ring[0]] for _ in range(2)]
+    main = torch.cuda.current_stream()
+    h2d = torch.cuda.Stream(device=dev)
+    d2h = torch.cuda.Stream(device=dev)
+
+    def run(K, t0):
+        e_in = [torch.cuda.Event() for _ in range(K)]
+        e_step = [torch.cuda.Event() for _ in range(K)]
+        e_out = [torch.cuda.Event() for _ in range(K)]
+
+        def load(t):
+            with torch.cuda.stream(h2d):
+                if t >= 2:
+                    h2d.wait_event(e_step[t - 2])  # step t-2 has finished reading this buffer
+                for r in range(R):
+                    dev_g[t % 2][r].copy_(host_g[t % 2][r], non_blocking=True)
+                e_in[t].record(h2d)
+
+        load(0)
+        if K > 1:
+            load(1)
+        for t in range(K):
+            main.wait_event(e_in[t])
+            if t >= 1:
+                main.wait_event(e_out[t - 1])  # theta of step t-1 has been read back
+            dm.step(case.theta, dev_g[t % 2], case.ms, k=k, beta=wl.beta, lr=wl.lr, mode=mode, sign=sign,
+                    seed=seed, step=t0 + t, stream=main)
+            e_step[t].record(main)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(e_step[t])
+                host_theta.copy_(case.theta, non_blocking=True)
+                e_out[t].record(d2h)
+            if t + 2 < K:
+                load(t + 2)
+        return e_out[K - 1]
+
+    run(2, 1000)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(main)
+    last = run(steps, 2000)
+    main.wait_event(last)
+    b.record(main)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return ms, sum(g.numel() * g.element_size() for g in host_g[0]), n * 4
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
 
     import torch
     import torch.distributed as dist
 
     import decoupled_momentum_optimizer_gb300 as dm
-    from decoupled_momentum_optimizer_gb300 import workloads as W
     from decoupled_momentum_optimizer_gb300.sharding import shard_seed
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -291,86 +457,34 @@ def main():
     n = wl.n
     dm.init(local)
     dev = torch.device("cuda", local)
-
-    # state and a ring of three pre-drawn gradient sets per replica (inputs >> L2)
-    theta = W.make_theta0(wl, dev)
-    ms = [torch.zeros(n, device=dev) for _ in range(R)]
-    streams = [W.GradStream(wl, r, dev) for r in range(R)]
-    ring = [[s.next() for s in streams] for _ in range(3)]
-    grad_bytes = ring[0][0].element_size()
-    step_bytes = algorithmic_bytes(n, R, grad_bytes, mode)
-    flush = step_bytes < 2 * L2_BYTES
-    scratch = torch.empty(256 * 1024 * 1024 // 4, device=dev) if flush else None
+    case = Case(wl, R, dev, n_sets=3)  # three pre-drawn gradient sets per replica, cycled
+    step_bytes = algorithmic_bytes(n, R, case.grad_bytes, mode)
     stream = torch.cuda.current_stream()
-
     seed = shard_seed(0, rank)  # each GPU steps its own shard with its own index seed
 
-    def one_step(t):
-        dm.step(theta, ring[t % 3], ms, k=k, beta=wl.beta, lr=wl.lr, mode=mode, sign=sign, seed=seed, step=t,
-                stream=stream)
-
-    for t in range(args.warmup):
-        one_step(t)
-    torch.cuda.synchronize()
-
-    K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     sampler = ClockSampler(local)
     barrier()
-    torch.cuda.synchronize()
-    with sampler:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for i in range(K):
-            if flush:
-                scratch.fill_(float(i))
-            ev[i][0].record(stream)
-            one_step(args.warmup + i)
-            ev[i][1].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
+    step_ms, kernel_ms, flush = time_fused(dm, case, mode, k, sign, seed, args.steps, args.warmup, stream,
+                                           sampler=sampler)
     barrier()
-    launch_ms = [a.elapsed_time(b) for a, b in ev]
-    step_ms = sum(launch_ms) / K if flush else t_start.elapsed_time(t_end) / K
-    kernel_ms = sum(launch_ms) / K
     if world > 1:
         tt = torch.tensor([step_ms, kernel_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         step_ms, kernel_ms = tt.tolist()
 
-    # end to end through the public API from pinned host memory
     e2e = None
     if not args.no_e2e:
-        host_g = [g.cpu().pin_memory() for g in ring[0]]
-        host_theta = torch.empty(n, dtype=torch.float32).pin_memory()
-        dev_g = [torch.empty_like(g) for g in ring[0]]
-        Ke = max(3, min(K, 10))
-        for t in range(2):
-            for r in range(R):
-                dev_g[r].copy_(host_g[r], non_blocking=True)
-            dm.step(theta, dev_g, ms, k=k, beta=wl.beta, lr=wl.lr, mode=mode, sign=sign, step=1000 + t)
-            host_theta.copy_(theta, non_blocking=True)
+        Ke = max(3, min(args.steps, 10))
         barrier()
-        torch.cuda.synchronize()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for t in range(Ke):
-            for r in range(R):
-                dev_g[r].copy_(host_g[r], non_blocking=True)
-            dm.step(theta, dev_g, ms, k=k, beta=wl.beta, lr=wl.lr, mode=mode, sign=sign, step=2000 + t)
-            host_theta.copy_(theta, non_blocking=True)
-        b.record(stream)
-        torch.cuda.synchronize()
-        e_ms = a.elapsed_time(b) / Ke
+        e_ms, hb, db = time_e2e(dm, case, mode, k, sign, seed, Ke, dev)
         if world > 1:
             tt = torch.tensor([e_ms], device=dev)
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
             e_ms = tt.item()
-        e2e = {"value": world * n / (e_ms * 1e-3), "unit": "params/s",
-               "h2d_bytes_per_step": sum(g.numel() * g.element_size() for g in host_g),
-               "d2h_bytes_per_step": n * 4, "ms_per_step": e_ms, "steps": Ke}
+        e2e = {"value": world * n / (e_ms * 1e-3), "unit": "params/s", "h2d_bytes_per_step": hb,
+               "d2h_bytes_per_step": db, "ms_per_step": e_ms, "steps": Ke,
+               "note": "gradients copied from pinned host memory and theta read back every step; "
+                       "the next step's gradient copies overlap the current step"}
 
     fault = dm.device_fault()
     if rank != 0:
@@ -382,14 +496,15 @@ def main():
     achieved = step_bytes / (kernel_ms * 1e-3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": ncu_traffic(args.workload, mode, k, R), "kernel": "demo::step_kernel",
-            "algorithmic_bytes_per_launch": step_bytes, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-            if peak_kind == "measured" else "fallback 6.8 TB/s"}
+            "algorithmic_bytes_per_launch": step_bytes,
+            "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s"}
     line = {
         "metric": METRIC,
         "value": world * n / (step_ms * 1e-3),
         "unit": "params/s",
         "n_gpus": world,
-        "steps": K,
+        "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": step_ms,
         "higher_is_better": True,
@@ -406,7 +521,7 @@ def main():
         "achieved_gbs": achieved,
         "hbm_frac_of_peak": achieved / peak,
         "roofline": roof,
-        "gpu_launches": K,
+        "gpu_launches": args.steps,
         "clocks": sampler.summary(),
         "e2e": e2e,
         "device_fault": fault,
@@ -416,6 +531,94 @@ def main():
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# Sweep: every configuration of the results table, one JSON line each
+# ----------------------------------------------------------------------------
+
+def sweep_cases():
+    """(workload, mode, k, sign, R, paths) for the results table."""
+    out = []
+    for name in ("t5_base", "vit_b16", "olmo2_1b_half"):
+        from decoupled_momentum_optimizer_gb300 import workloads as W
+
+        wl = W.workload(name)
+        for mode, k, sign in wl.runs:
+            out.append((name, mode, k, sign, wl.R, ("fused", "split")))
+    for e in (20, 22, 24, 26, 28, 30):
+        for k in (1, 2, 4, 8):
+            out.append((f"flat{1 << e}", "demo", k, True, 2, ("fused",) if e != 26 else ("fused", "split")))
+    for R in (1, 8, 64):
+        out.append((f"flat{1 << 26}", "demo", 4, True, R, ("fused", "split")))
+    out.append((f"flat{1 << 30}", "demo", 4, True, 8, ("fused",)))
+    for e in (24, 26, 28):
+        for mode, k in (("random", 1), ("random", 8), ("stride", 4), ("diloco", 1), ("diloco-sync", 1)):
+            out.append((f"flat{1 << e}", mode, k, True, 2, ("fused", "split") if e == 26 else ("fused",)))
+    return out
+
+
+def run_sweep(args):
+    import torch
+
+    import decoupled_momentum_optimizer_gb300 as dm
+    from decoupled_momentum_optimizer_gb300 import workloads as W
+
+    dm.init(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    peak, _ = measured_peaks()
+    cache = {}
+    f = open(args.sweep, "w")
+    for name, mode, k, sign, R, paths in sweep_cases():
+        key = (name, R)
+        if key not in cache:
+            cache.clear()
+            torch.cuda.empty_cache()
+            wl = W.workload(name)
+            cache[key] = Case(wl, R, dev, n_sets=1 if wl.n >= (1 << 24) else 3)
+        case = cache[key]
+        n = case.n
+        # DiLoCo: period 8; "diloco" times the off-sync steps, "diloco-sync" the sync step
+        real_mode = "diloco" if mode.startswith("diloco") else mode
+        sync = mode == "diloco-sync"
+        period = 8
+        step0 = 7 if sync else 0
+        rec = {"workload": name, "n": n, "mode": mode, "k": k, "sign": sign, "R": R, "grad_dtype": case.wl.g_dtype}
+        steps, warmup = (args.steps, args.warmup) if not real_mode == "diloco" else (1, 0)
+        if real_mode == "diloco":
+            # one step at a time so that every timed step is (or is not) a sync step
+            ms_list, l_list = [], []
+            for rep in range(6):
+                t0 = step0 + 8 * rep
+                s_ms, l_ms, _ = time_fused(dm, case, real_mode, k, sign, 0, 1, 0, stream, step0=t0,
+                                           diloco_period=period)
+                ms_list.append(s_ms)
+                l_list.append(l_ms)
+            step_ms, launch_ms = statistics.median(ms_list[1:]), statistics.median(l_list[1:])
+        else:
+            step_ms, launch_ms, _ = time_fused(dm, case, real_mode, k, sign, 0, steps, warmup, stream)
+        fb = algorithmic_bytes(n, R, case.grad_bytes, real_mode, sync=sync or real_mode != "diloco")
+        rec.update(fused_ms=step_ms, fused_params_per_s=n / (step_ms * 1e-3), fused_bytes=fb,
+                   fused_gbs=fb / (launch_ms * 1e-3) / 1e9, fused_frac=fb / (launch_ms * 1e-3) / 1e9 / peak)
+        if "split" in paths:
+            if real_mode == "diloco":
+                sm = statistics.median([time_split(dm, case, real_mode, k, sign, 0, 1, 0, stream,
+                                                   diloco_period=period, step0=step0 + 8 * rep) for rep in range(4)])
+            else:
+                sm = time_split(dm, case, real_mode, k, sign, 0, steps, warmup, stream)
+            sb = split_bytes(n, R, case.grad_bytes, real_mode, k, sync=sync or real_mode != "diloco")
+            rec.update(split_ms=sm, split_params_per_s=n / (sm * 1e-3), split_bytes=sb,
+                       split_gbs=sb / (sm * 1e-3) / 1e9, split_frac=sb / (sm * 1e-3) / 1e9 / peak)
+        f.write(json.dumps(rec) + "\n")
+        f.flush()
+        print(f"{name:16s} {mode:11s} k={k:2d} sign={int(sign)} R={R:2d}  fused {step_ms:8.3f} ms "
+              f"{rec['fused_gbs']:7.0f} GB/s {100 * rec['fused_frac']:5.1f}%"
+              + (f"  split {rec['split_ms']:8.3f} ms {rec['split_gbs']:7.0f} GB/s" if "split_ms" in rec else ""),
+              flush=True)
+    f.close()
+    print(json.dumps({"sweep": args.sweep, "device_fault": dm.device_fault()}))
     return 0
 
 
