@@ -85,7 +85,7 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t nc, bool bf16) {
   return r == CUDA_SUCCESS;
 }
 
-int grid_for(int64_t ntiles, const DeviceState* st, int warps_per_cta = kWarps) {
+int grid_for(int64_t ntiles, const DeviceState* st, int warps_per_cta = kStepWarps) {
   const int64_t want = (ntiles + warps_per_cta - 1) / warps_per_cta;
   return static_cast<int>(want < st->sms ? want : st->sms);
 }
@@ -144,7 +144,7 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
   p.rcpR = 1.0f / static_cast<float>(R);
   fill_rcp(p);
   p.fault = st->fault;
-  const int grid = grid_for(p.ntiles, st, kStepWarps);
+  const int grid = grid_for(p.ntiles, st);
   cudaError_t e;
   if constexpr (MAXR == kSmallReplicas) {
     e = launch_step_small(p, mode, bf16, grid, stream);
@@ -162,6 +162,7 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
   std::memset(&p, 0, sizeof(p));
   const int64_t nc = n / DEMO_CHUNK;
   if (!make_map(&p.theta, theta, nc, false)) return DEMO_ECUDA;
+  p.theta_ptr = theta;
   for (int r = 0; r < R; ++r) {
     p.vals[r] = vals[r];
     p.idx[r] = (mode == DEMO_MODE_DEMO) ? idx[r] : nullptr;
@@ -285,6 +286,7 @@ int demo_encode(const void* g, int grad_dtype, float* m, int64_t n, int chunk, i
   const int64_t nc = n / DEMO_CHUNK;
   const bool bf16 = grad_dtype == DEMO_GRAD_BF16;
   if (!make_map(&p.g, g, nc, bf16) || !make_map(&p.m, m, nc, false)) return DEMO_ECUDA;
+  p.m_ptr = m;
   p.vals = vals;
   p.idx = idx;
   p.nc = nc;

@@ -18,8 +18,6 @@
 namespace demo {
 
 constexpr int kChunk = 32;
-constexpr int kWarps = 8;               // warps per CTA (one tile each at a time)
-constexpr int kThreads = kWarps * 32;
 constexpr int kTileBytesF32 = 32 * 128;  // 32 rows x 32 float32
 constexpr int kTileBytesBF16 = 32 * 64;  // 32 rows x 32 bfloat16
 constexpr unsigned kFaultLoadTimeout = 1u;
@@ -286,16 +284,35 @@ __device__ __forceinline__ void dct32_inverse(const float (&Y)[32], float (&q)[3
 
 __device__ __forceinline__ uint32_t umax32(uint32_t a, uint32_t b) { return a > b ? a : b; }
 
+// Largest of 32 unsigned keys: a tree of 3-input maxima.
 __device__ __forceinline__ uint32_t max_tree(const uint32_t (&v)[32]) {
-  uint32_t a[16];
+  uint32_t a[11];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) a[i] = umax32(v[i], v[i + 16]);
+  for (int i = 0; i < 10; ++i) a[i] = __vimax3_u32(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+  a[10] = umax32(v[30], v[31]);
+  const uint32_t b0 = __vimax3_u32(a[0], a[1], a[2]);
+  const uint32_t b1 = __vimax3_u32(a[3], a[4], a[5]);
+  const uint32_t b2 = __vimax3_u32(a[6], a[7], a[8]);
+  const uint32_t b3 = umax32(a[9], a[10]);
+  return __vimax3_u32(b0, b1, umax32(b2, b3));
+}
+
+// Largest key strictly below T, as T + max_u (key_u - T) over the wrapped
+// differences: keys below T map to [2^32 - T, 2^32), all others to [0, 2^31),
+// so one add-and-max per key filters and maximises at once.  Returns T itself
+// when no key is below T.
+__device__ __forceinline__ uint32_t next_below(const uint32_t (&key)[32], uint32_t T) {
+  const uint32_t negT = 0u - T;
+  uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
 #pragma unroll
-  for (int w = 8; w >= 1; w >>= 1) {
-#pragma unroll
-    for (int i = 0; i < w; ++i) a[i] = umax32(a[i], a[i + w]);
+  for (int u = 0; u < 32; u += 4) {
+    m0 = __viaddmax_u32(key[u + 0], negT, m0);
+    m1 = __viaddmax_u32(key[u + 1], negT, m1);
+    m2 = __viaddmax_u32(key[u + 2], negT, m2);
+    m3 = __viaddmax_u32(key[u + 3], negT, m3);
   }
-  return a[0];
+  const uint32_t best = __vimax3_u32(m0, m1, umax32(m2, m3));
+  return best >= 0x80000000u ? best + T : T;
 }
 
 __device__ __forceinline__ uint32_t topk_select(const float (&X)[32], int k, float (&Xs)[32]) {
@@ -309,13 +326,7 @@ __device__ __forceinline__ uint32_t topk_select(const float (&X)[32], int k, flo
   for (int u = 0; u < 32; ++u) key[u] = __float_as_uint(X[u]) & 0x7fffffffu;
 
   uint32_t T = max_tree(key);
-  for (int r = 1; r < k; ++r) {
-    uint32_t d[32];
-#pragma unroll
-    for (int u = 0; u < 32; ++u) d[u] = key[u] - T;
-    const uint32_t best = max_tree(d);
-    T = (best >= 0x80000000u) ? best + T : T;
-  }
+  for (int r = 1; r < k; ++r) T = next_below(key, T);
   uint32_t M = 0;
 #pragma unroll
   for (int u = 0; u < 32; ++u) M |= static_cast<uint32_t>(key[u] >= T) << u;

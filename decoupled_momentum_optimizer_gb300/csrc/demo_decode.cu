@@ -8,36 +8,86 @@
 // Per warp, theta tiles of 32 chunks stream through a two-slot TMA ring; lane
 // i combines the payload entries of its chunk (replicas in order 0..R-1) in
 // shared-memory accumulators, forms Q and updates its theta row, which leaves
-// through a TMA store.  The arithmetic matches the fused step operation by
-// operation, so split and fused results are bit-identical.
+// through the tile's own slot with coalesced stores.  The arithmetic matches
+// the fused step operation by operation, so split and fused results are
+// bit-identical.
 #include "demo_common.cuh"
 #include "demo_params.h"
 
 namespace demo {
 
 struct alignas(1024) DecWarpSmem {
-  float tbuf[2][1024];  // theta tiles
-  float out[1024];      // TMA-store staging; before that, a [i][lane] scratch column per lane
-  float2 acc[32 * 32];  // DeMo accumulators [u][lane] = (sum, count)
+  float tbuf[2][1024];  // theta tiles (and the theta rows on their way out)
+  float2 acc[32 * 32];  // DeMo: [u][lane] = (sum, count); others: [i][lane].x = Q scratch
 };
 
-constexpr size_t kDecSmem = 1024 + kWarps * sizeof(DecWarpSmem) + kWarps * 16 + 272;
+constexpr int kDecWarps = kStepWarps;
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr size_t kDecSmem = 1024 + kDecWarps * sizeof(DecWarpSmem) + kDecWarps * 16 + 272;
+
+// Load k payload values (and index bytes) of one chunk; k in {1, 2, 4, 8} uses one vector load each.
+__device__ __forceinline__ void load_payload(const float* vrow, const uint8_t* irow, float (&pv)[8], uint32_t& ilo,
+                                             uint32_t& ihi, int k) {
+  ilo = ihi = 0;
+  switch (k) {
+    case 1:
+      pv[0] = vrow[0];
+      if (irow) ilo = irow[0];
+      break;
+    case 2: {
+      const float2 v = *reinterpret_cast<const float2*>(vrow);
+      pv[0] = v.x;
+      pv[1] = v.y;
+      if (irow) ilo = *reinterpret_cast<const uint16_t*>(irow);
+      break;
+    }
+    case 4: {
+      const float4 v = *reinterpret_cast<const float4*>(vrow);
+      pv[0] = v.x;
+      pv[1] = v.y;
+      pv[2] = v.z;
+      pv[3] = v.w;
+      if (irow) ilo = *reinterpret_cast<const uint32_t*>(irow);
+      break;
+    }
+    default: {  // 8
+      const float4 a = reinterpret_cast<const float4*>(vrow)[0];
+      const float4 b = reinterpret_cast<const float4*>(vrow)[1];
+      pv[0] = a.x;
+      pv[1] = a.y;
+      pv[2] = a.z;
+      pv[3] = a.w;
+      pv[4] = b.x;
+      pv[5] = b.y;
+      pv[6] = b.z;
+      pv[7] = b.w;
+      if (irow) {
+        const uint2 w = *reinterpret_cast<const uint2*>(irow);
+        ilo = w.x;
+        ihi = w.y;
+      }
+      break;
+    }
+  }
+}
+
+__device__ __forceinline__ bool vector_kd(int k) { return k == 1 || k == 2 || k == 4 || k == 8; }
 
 template <int MODE, int MAXR>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams<MAXR> p) {
+__global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_constant__ DecodeParams<MAXR> p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   DecWarpSmem& ws = reinterpret_cast<DecWarpSmem*>(base)[warp];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kWarps * sizeof(DecWarpSmem)) + 2 * warp;
-  float* rcp = reinterpret_cast<float*>(base + kWarps * sizeof(DecWarpSmem) + kWarps * 16);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kDecWarps * sizeof(DecWarpSmem)) + 2 * warp;
+  float* rcp = reinterpret_cast<float*>(base + kDecWarps * sizeof(DecWarpSmem) + kDecWarps * 16);
   if (threadIdx.x <= kMaxReplicas) rcp[threadIdx.x] = p.rcp_tab[threadIdx.x];
   __syncthreads();
 
-  const long long gw = static_cast<long long>(blockIdx.x) * kWarps + warp;
-  const long long TW = static_cast<long long>(gridDim.x) * kWarps;
+  const long long gw = static_cast<long long>(blockIdx.x) * kDecWarps + warp;
+  const long long TW = static_cast<long long>(gridDim.x) * kDecWarps;
   if (gw >= p.ntiles) return;
   const long long nitems = (p.ntiles - 1 - gw) / TW + 1;
 
@@ -46,10 +96,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     mbar_init(&bars[1], 1);
     fence_mbar_init();
   }
-  if constexpr (MODE == kModeDemo) {
 #pragma unroll
-    for (int u = 0; u < 32; ++u) ws.acc[u * 32 + lane] = make_float2(0.0f, 0.0f);
-  }
+  for (int u = 0; u < 32; ++u) ws.acc[u * 32 + lane] = make_float2(0.0f, 0.0f);
   __syncwarp();
 
   auto issue = [&](long long item) {
@@ -67,9 +115,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   for (long long item = 0; item < nitems; ++item) {
     const int s = static_cast<int>(item & 1);
     const uint32_t par = static_cast<uint32_t>((item >> 1) & 1);
-    const long long t = gw + item * TW;
-    const int y = static_cast<int>(t * 32);
-    const long long c = t * 32 + lane;
+    const long long row0 = (gw + item * TW) * 32;
+    const long long c = row0 + lane;
     const bool valid = c < p.nc;
 
     const bool ok = mbar_wait_bounded(&bars[s], par);
@@ -78,7 +125,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         atomicOr(p.fault, kFaultLoadTimeout);
         for (long long it = item; it < item + 2 && it < nitems; ++it)
           mbar_wait_bounded(&bars[it & 1], static_cast<uint32_t>((it >> 1) & 1));
-        bulk_wait_all();
       }
       __syncwarp();
       return;
@@ -86,13 +132,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
     float th[32];
     load_row_f32(ws.tbuf[s], lane, th);
-    __syncwarp();
-    if (lane == 0) {
-      fence_proxy_async_smem();
-      issue(item + 2);
-      bulk_wait_read_all();
-    }
-    __syncwarp();
 
     float Q[32];
     if constexpr (MODE == kModeDemo) {
@@ -100,12 +139,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         for (int r = 0; r < p.R; ++r) {
           const float* vrow = p.vals[r] + c * p.k;
           const uint8_t* irow = p.idx[r] + c * p.k;
-          for (int j = 0; j < p.k; ++j) {
-            const int u = irow[j] & 31;
-            float2 a = ws.acc[u * 32 + lane];
-            a.x += vrow[j];
-            a.y += 1.0f;
-            ws.acc[u * 32 + lane] = a;
+          if (vector_kd(p.k)) {
+            float pv[8];
+            uint32_t ilo, ihi;
+            load_payload(vrow, irow, pv, ilo, ihi, p.k);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (j < p.k) {
+                const int u = ((j < 4 ? ilo >> (8 * j) : ihi >> (8 * (j - 4)))) & 31;
+                float2 a = ws.acc[u * 32 + lane];
+                a.x += pv[j];
+                a.y += 1.0f;
+                ws.acc[u * 32 + lane] = a;
+              }
+            }
+          } else {
+            for (int j = 0; j < p.k; ++j) {
+              const int u = irow[j] & 31;
+              float2 a = ws.acc[u * 32 + lane];
+              a.x += vrow[j];
+              a.y += 1.0f;
+              ws.acc[u * 32 + lane] = a;
+            }
           }
         }
       }
@@ -136,13 +191,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 #pragma unroll
       for (int i = 0; i < 32; ++i) Q[i] *= p.rcpR;
     } else {
-      // Random / Striding: every replica sent the same positions.
+      // Random / Striding: every replica sent the same positions; Q = mean at those positions.
+      float* qs = reinterpret_cast<float*>(ws.acc);  // [i][lane] scratch (first 4 KB)
 #pragma unroll
-      for (int i = 0; i < 32; ++i) ws.out[i * 32 + lane] = 0.0f;
+      for (int i = 0; i < 32; ++i) qs[i * 32 + lane] = 0.0f;
       auto take = [&](int j, int pos) {
         float sum = 0.0f;
         for (int r = 0; r < p.R; ++r) sum += p.vals[r][c * p.k + j];
-        ws.out[pos * 32 + lane] = sum * p.rcpR;
+        qs[pos * 32 + lane] = sum * p.rcpR;
       };
       if (valid) {
         if constexpr (MODE == kModeRandom) {
@@ -152,28 +208,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         }
       }
 #pragma unroll
-      for (int i = 0; i < 32; ++i) Q[i] = ws.out[i * 32 + lane];
+      for (int i = 0; i < 32; ++i) Q[i] = qs[i * 32 + lane];
     }
 
 #pragma unroll
     for (int i = 0; i < 32; ++i) th[i] = __fmaf_rn(-p.lr, Q[i], th[i]);
-    __syncwarp();
-    store_row_f32(ws.out, lane, th);
+    __syncwarp();  // every lane has read its theta row
+    store_tile_coalesced(ws.tbuf[s], lane, th, p.theta_ptr, row0, p.nc);
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) {
-      tma_store_2d(&p.theta, ws.out, 0, y);
-      bulk_commit();
-    }
+    if (lane == 0) issue(item + 2);
   }
-  if (lane == 0) bulk_wait_all();
 }
 
 template <int MAXR>
 static cudaError_t launch_decode_t(const DecodeParams<MAXR>& p, int mode, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kDecThreads);
   cfg.dynamicSmemBytes = kDecSmem;
   cfg.stream = st;
   switch (mode) {

@@ -33,6 +33,7 @@ struct StepParams {
 struct EncodeParams {
   CUtensorMap g;
   CUtensorMap m;
+  float* m_ptr;
   float* vals;
   uint8_t* idx;
   long long nc, ntiles;
@@ -47,6 +48,7 @@ struct EncodeParams {
 template <int MAXR>
 struct DecodeParams {
   CUtensorMap theta;
+  float* theta_ptr;
   const float* vals[MAXR];
   const uint8_t* idx[MAXR];
   long long nc, ntiles;
@@ -58,8 +60,8 @@ struct DecodeParams {
   unsigned int* fault;
 };
 
-// Launchers (one per translation unit).  `grid` CTAs of kStepWarps (fused
-// step) or kWarps (split path) warps; each warp walks the tiles gw, gw + W*grid, ...
+// Launchers (one per translation unit).  `grid` CTAs of kStepWarps warps; each
+// warp walks the tiles gw, gw + kStepWarps * grid, ...
 constexpr int kStepWarps = 11;
 cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, bool bf16, int grid, cudaStream_t st);
 cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int grid, cudaStream_t st);
