@@ -324,27 +324,24 @@ class _Null:
         return False
 
 
-def time_split(dm, case, mode, k, sign, seed, steps, warmup, stream, diloco_period=8, step0=0):
+def time_split(dm, case, mode, k, sign, seed, steps, warmup, stream, diloco_period=8, step0=0, wire="f32"):
     """Mean time (ms) of R demo_encode calls + one demo_decode_update (the wire-format path)."""
     import torch
 
     wl, n, R = case.wl, case.n, case.R
-    nc = n // 32
     dev = case.theta.device
-    if mode == "diloco":
-        vals = [torch.empty(n, device=dev) for _ in range(R)]
-        idx = None
-    else:
-        vals = [torch.empty(nc * k, device=dev) for _ in range(R)]
-        idx = [torch.empty(nc * k, dtype=torch.uint8, device=dev) for _ in range(R)] if mode == "demo" else None
+    bufs = [dm.payload_buffers(mode, n, k, step=diloco_period - 1, diloco_period=diloco_period, wire=wire,
+                               device=dev) for _ in range(R)]
+    vals = [b[0] for b in bufs]
+    idx = [b[1] for b in bufs] if mode == "demo" else None
 
     def one(t):
         g = case.ring[t % len(case.ring)]
         for r in range(R):
             dm.encode(g[r], case.ms[r], vals[r], idx[r] if idx else None, k=k, beta=wl.beta, mode=mode, sign=sign,
-                      diloco_period=diloco_period, seed=seed, step=t, stream=stream)
+                      diloco_period=diloco_period, seed=seed, step=t, wire=wire, stream=stream)
         dm.decode_update(case.theta, vals, idx, k=k, lr=wl.lr, mode=mode, diloco_period=diloco_period, seed=seed,
-                         step=t, stream=stream)
+                         step=t, wire=wire, stream=stream)
 
     for t in range(warmup):
         one(step0 + t)
@@ -359,15 +356,12 @@ def time_split(dm, case, mode, k, sign, seed, steps, warmup, stream, diloco_peri
     return a.elapsed_time(b) / steps
 
 
-def split_bytes(n, R, grad_bytes, mode, k, sync=True):
+def split_bytes(n, R, grad_bytes, mode, k, sync=True, wire="f32"):
     """Algorithmic bytes of the split path: R encodes (g, m, payload out) + decode (R payloads in, theta)."""
-    nc = n // 32
-    if mode == "demo":
-        P = nc * k * 5
-    elif mode in ("random", "stride"):
-        P = nc * k * 4
-    else:
-        P = 4 * n if sync else 0
+    import decoupled_momentum_optimizer_gb300 as dm
+
+    vb, ib = dm.payload_bytes(mode, n, k, step=7 if sync else 0, diloco_period=8, wire=wire)
+    P = vb + ib
     theta = 8 * n if (mode != "diloco" or sync) else 0
     return R * (n * (grad_bytes + 8) + P) + (R * P + theta if theta else 0)
 
@@ -547,6 +541,10 @@ def sweep_cases():
         wl = W.workload(name)
         for mode, k, sign in wl.runs:
             out.append((name, mode, k, sign, wl.R, ("fused", "split")))
+    # compact wire formats of the split path (T5-base shard)
+    out.append(("t5_base", "demo", 4, True, 2, ("split:ternary", "split:bf16")))
+    out.append(("t5_base", "random", 8, True, 2, ("split:ternary",)))
+    out.append(("t5_base", "demo", 4, False, 2, ("split:bf16", "split:f16")))
     for e in (20, 22, 24, 26, 28, 30):
         for k in (1, 2, 4, 8):
             out.append((f"flat{1 << e}", "demo", k, True, 2, ("fused",) if e != 26 else ("fused", "split")))
@@ -586,6 +584,21 @@ def run_sweep(args):
         period = 8
         step0 = 7 if sync else 0
         rec = {"workload": name, "n": n, "mode": mode, "k": k, "sign": sign, "R": R, "grad_dtype": case.wl.g_dtype}
+        wires = [x.split(":")[1] for x in paths if x.startswith("split:")]
+        if wires:
+            # wire-format runs of the split path only
+            for wire in wires:
+                sm = time_split(dm, case, real_mode, k, sign, 0, steps, warmup, stream, wire=wire)
+                sb = split_bytes(n, R, case.grad_bytes, real_mode, k, wire=wire)
+                r2 = dict(rec, mode=f"{mode}/{wire}", split_ms=sm, split_params_per_s=n / (sm * 1e-3), split_bytes=sb,
+                          split_gbs=sb / (sm * 1e-3) / 1e9, split_frac=sb / (sm * 1e-3) / 1e9 / peak,
+                          payload_bytes_per_replica=sum(dm.payload_bytes(real_mode, n, k, wire=wire)))
+                f.write(json.dumps(r2) + "\n")
+                f.flush()
+                print(f"{name:16s} {mode + '/' + wire:16s} k={k:2d} sign={int(sign)} R={R:2d}  split {sm:8.3f} ms "
+                      f"{r2['split_gbs']:7.0f} GB/s  payload {r2['payload_bytes_per_replica'] / 1e6:8.2f} MB/replica",
+                      flush=True)
+            continue
         steps, warmup = (args.steps, args.warmup) if not real_mode == "diloco" else (1, 0)
         if real_mode == "diloco":
             # one step at a time so that every timed step is (or is not) a sync step

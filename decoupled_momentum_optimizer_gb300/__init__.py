@@ -12,6 +12,7 @@ import ctypes
 import os
 
 MODES = {"demo": 0, "random": 1, "stride": 2, "diloco": 3}
+WIRES = {"f32": 0, "ternary": 1, "bf16": 2, "f16": 3}
 GRAD_F32, GRAD_BF16 = 0, 1
 CHUNK = 32
 MAX_REPLICAS = 64
@@ -31,6 +32,19 @@ _SIGS = {
     "demo_step": (ctypes.c_int, [_c_vp, _c_i64, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_float,
                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_vp, ctypes.c_int, _c_vp, ctypes.c_int,
                                  _c_u64, _c_u64, _c_vp]),
+    "demo_payload_bytes_wire": (ctypes.c_size_t, [ctypes.c_int, _c_i64, ctypes.c_int, ctypes.c_int, _c_u64,
+                                                  ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "demo_encode_wire": (ctypes.c_int, [_c_vp, ctypes.c_int, _c_vp, _c_i64, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_u64, _c_u64,
+                                        ctypes.c_int, _c_vp, _c_vp, _c_vp]),
+    "demo_decode_update_wire": (ctypes.c_int, [_c_vp, _c_i64, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                               ctypes.c_int, ctypes.c_int, _c_vp, _c_vp, ctypes.c_int, _c_u64, _c_u64,
+                                               ctypes.c_int, _c_vp]),
+    "demo_step_wire": (ctypes.c_int, [_c_vp, _c_i64, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_vp, ctypes.c_int, _c_vp,
+                                      ctypes.c_int, _c_u64, _c_u64, ctypes.c_int, _c_vp]),
+    "demo_validate_payload": (ctypes.c_int, [_c_i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_vp,
+                                             ctypes.POINTER(_c_i64)]),
     "demo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "demo_device_fault": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint)]),
 }
@@ -118,45 +132,82 @@ def _mode(mode):
     return MODES[mode] if isinstance(mode, str) else int(mode)
 
 
-def payload_bytes(mode, n, k, step=0, diloco_period=8):
-    """(value bytes, index bytes) one replica sends for a step."""
+def _wire(wire):
+    return WIRES[wire] if isinstance(wire, str) else int(wire)
+
+
+def payload_bytes(mode, n, k, step=0, diloco_period=8, wire="f32"):
+    """(value bytes, index bytes) one replica sends for a step in the given wire format."""
     ib = ctypes.c_size_t(0)
-    vb = lib().demo_payload_bytes(_mode(mode), n, CHUNK, k, step, diloco_period, ctypes.byref(ib))
+    vb = lib().demo_payload_bytes_wire(_mode(mode), n, CHUNK, k, step, diloco_period, _wire(wire), ctypes.byref(ib))
     return vb, ib.value
 
 
-def encode(g, m, vals, idx=None, *, k, beta, mode="demo", sign=True, diloco_period=8, seed=0, step=0, stream=None):
-    """One replica's encode (demo_encode): updates m in place, writes vals (and idx for DeMo)."""
+def payload_buffers(mode, n, k, step=0, diloco_period=8, wire="f32", device="cuda"):
+    """Empty device buffers (vals, idx) sized for one replica's payload; None where nothing is sent."""
+    import torch
+
+    vb, ib = payload_bytes(mode, n, k, step=step, diloco_period=diloco_period, wire=wire)
+    w = _wire(wire)
+    vdt = {0: torch.float32, 1: torch.int32, 2: torch.bfloat16, 3: torch.float16}[w]
+    vals = torch.empty(vb // torch.empty(0, dtype=vdt).element_size(), dtype=vdt, device=device) if vb else None
+    idx = None
+    if ib:
+        idx = torch.empty(ib // 4, dtype=torch.int32, device=device) if w == 1 else \
+            torch.empty(ib, dtype=torch.uint8, device=device)
+    return vals, idx
+
+
+def _val_dtypes(wire):
+    import torch
+
+    return {0: (torch.float32,), 1: (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,),
+            2: (torch.bfloat16, torch.int16), 3: (torch.float16, torch.int16)}[wire]
+
+
+def _idx_dtypes(wire):
+    import torch
+
+    return (torch.int32,) if wire == 1 else (torch.uint8,)
+
+
+def encode(g, m, vals, idx=None, *, k, beta, mode="demo", sign=True, diloco_period=8, seed=0, step=0, wire="f32",
+           stream=None):
+    """One replica's encode (demo_encode_wire): updates m in place, writes vals (and idx for DeMo)."""
     import torch
 
     init(m.device.index)
     n = m.numel()
+    w = _wire(wire)
     gp = _ptr(g, (torch.float32, torch.bfloat16), "g", n)
     mp = _ptr(m, (torch.float32,), "m", n)
-    vp = _ptr(vals, (torch.float32,), "vals") if vals is not None else None
-    ip = _ptr(idx, (torch.uint8,), "idx") if idx is not None else None
-    _check(lib().demo_encode(gp, _grad_dtype(g), mp, n, CHUNK, k, beta, _mode(mode), int(bool(sign)), diloco_period,
-                             seed, step, vp, ip, _stream(stream)), "demo_encode")
+    vp = _ptr(vals, _val_dtypes(w), "vals") if vals is not None else None
+    ip = _ptr(idx, _idx_dtypes(w), "idx") if idx is not None else None
+    _check(lib().demo_encode_wire(gp, _grad_dtype(g), mp, n, CHUNK, k, beta, _mode(mode), int(bool(sign)),
+                                  diloco_period, seed, step, w, vp, ip, _stream(stream)), "demo_encode")
 
 
-def decode_update(theta, vals, idx=None, *, k, lr, mode="demo", diloco_period=8, seed=0, step=0, stream=None):
-    """Scatter-mean of the R payloads in ``vals`` (and ``idx``) and theta -= lr Q (demo_decode_update)."""
+def decode_update(theta, vals, idx=None, *, k, lr, mode="demo", diloco_period=8, seed=0, step=0, wire="f32",
+                  stream=None):
+    """Scatter-mean of the R payloads in ``vals`` (and ``idx``) and theta -= lr Q (demo_decode_update_wire)."""
     import torch
 
     init(theta.device.index)
     n = theta.numel()
     R = len(vals)
+    w = _wire(wire)
     tp = _ptr(theta, (torch.float32,), "theta", n)
-    varr = (ctypes.c_void_p * R)(*[_ptr(v, (torch.float32,), f"vals[{r}]") for r, v in enumerate(vals)])
+    varr = (ctypes.c_void_p * R)(*[_ptr(v, _val_dtypes(w), f"vals[{r}]") for r, v in enumerate(vals)])
     iarr = None
     if idx is not None:
-        iarr = (ctypes.c_void_p * R)(*[_ptr(i, (torch.uint8,), f"idx[{r}]") for r, i in enumerate(idx)])
-    _check(lib().demo_decode_update(tp, n, CHUNK, k, lr, _mode(mode), R, varr, iarr, diloco_period, seed, step,
-                                    _stream(stream)), "demo_decode_update")
+        iarr = (ctypes.c_void_p * R)(*[_ptr(i, _idx_dtypes(w), f"idx[{r}]") for r, i in enumerate(idx)])
+    _check(lib().demo_decode_update_wire(tp, n, CHUNK, k, lr, _mode(mode), R, varr, iarr, diloco_period, seed, step,
+                                         w, _stream(stream)), "demo_decode_update")
 
 
-def step(theta, gs, ms, *, k, beta, lr, mode="demo", sign=True, diloco_period=8, seed=0, step=0, stream=None):
-    """The fused shard step over R replicas (demo_step); theta and every m_r update in place."""
+def step(theta, gs, ms, *, k, beta, lr, mode="demo", sign=True, diloco_period=8, seed=0, step=0, wire="f32",
+         stream=None):
+    """The fused shard step over R replicas (demo_step_wire); theta and every m_r update in place."""
     import torch
 
     init(theta.device.index)
@@ -168,8 +219,16 @@ def step(theta, gs, ms, *, k, beta, lr, mode="demo", sign=True, diloco_period=8,
     gd = _grad_dtype(gs[0])
     garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n) for r, g in enumerate(gs)])
     marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n) for r, m in enumerate(ms)])
-    _check(lib().demo_step(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr, gd, marr, diloco_period,
-                           seed, step, _stream(stream)), "demo_step")
+    _check(lib().demo_step_wire(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr, gd, marr,
+                                diloco_period, seed, step, _wire(wire), _stream(stream)), "demo_step")
+
+
+def validate_payload(idx_host, n, k, wire="f32"):
+    """Host check of a DeMo index payload (a CPU tensor): returns (ok, first bad chunk or -1)."""
+    bad = ctypes.c_int64(-1)
+    status = lib().demo_validate_payload(n, CHUNK, k, _wire(wire), ctypes.c_void_p(idx_host.data_ptr()),
+                                         ctypes.byref(bad))
+    return status == 0, bad.value
 
 
 def device_fault():

@@ -59,6 +59,8 @@ int check_shape(int64_t n, int chunk, int k, int mode, int diloco_period) {
   return DEMO_OK;
 }
 
+bool valid_wire(int wire) { return wire >= DEMO_WIRE_F32 && wire <= DEMO_WIRE_F16; }
+
 int current_state(DeviceState** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -118,7 +120,7 @@ int to_status(cudaError_t e) { return e == cudaSuccess ? DEMO_OK : DEMO_ECUDA; }
 template <int MAXR>
 int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float lr, int mode, int sign, int R,
              const void* const* g, int grad_dtype, float* const* m, int diloco_period, uint64_t seed, uint64_t step,
-             cudaStream_t stream) {
+             int wire, cudaStream_t stream) {
   static_assert(sizeof(StepParams<MAXR>) < 32000, "kernel parameter block too large");
   StepParams<MAXR> p;
   std::memset(&p, 0, sizeof(p));
@@ -143,6 +145,7 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
   p.lr = lr;
   p.rcpR = 1.0f / static_cast<float>(R);
   fill_rcp(p);
+  p.wire = wire;
   p.fault = st->fault;
   const int grid = grid_for(p.ntiles, st);
   cudaError_t e;
@@ -156,7 +159,7 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
 
 template <int MAXR>
 int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mode, int R,
-               const float* const* vals, const uint8_t* const* idx, uint64_t seed, uint64_t step,
+               const void* const* vals, const void* const* idx, uint64_t seed, uint64_t step, int wire,
                cudaStream_t stream) {
   DecodeParams<MAXR> p;
   std::memset(&p, 0, sizeof(p));
@@ -175,6 +178,7 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
   p.lr = lr;
   p.rcpR = 1.0f / static_cast<float>(R);
   fill_rcp(p);
+  p.wire = wire;
   p.fault = st->fault;
   const int grid = grid_for(p.ntiles, st);
   cudaError_t e;
@@ -243,30 +247,40 @@ int demo_init(int device) {
   return DEMO_OK;
 }
 
-size_t demo_payload_bytes(int mode, int64_t n, int chunk, int k, uint64_t step, int diloco_period,
-                          size_t* idx_bytes) {
+size_t demo_payload_bytes_wire(int mode, int64_t n, int chunk, int k, uint64_t step, int diloco_period, int wire,
+                               size_t* idx_bytes) {
   if (idx_bytes) *idx_bytes = 0;
-  if (check_shape(n, chunk, k, mode, diloco_period) != DEMO_OK) return 0;
+  if (check_shape(n, chunk, k, mode, diloco_period) != DEMO_OK || !valid_wire(wire)) return 0;
   const size_t nc = static_cast<size_t>(n / DEMO_CHUNK);
-  switch (mode) {
-    case DEMO_MODE_DEMO:
-      if (idx_bytes) *idx_bytes = nc * static_cast<size_t>(k);
-      return nc * static_cast<size_t>(k) * 4;
-    case DEMO_MODE_RANDOM:
-    case DEMO_MODE_STRIDE:
-      return nc * static_cast<size_t>(k) * 4;
-    default:
-      return diloco_sync(step, diloco_period) ? static_cast<size_t>(n) * 4 : 0;
+  const size_t T = (nc + 31) / 32;
+  size_t kv;
+  if (mode == DEMO_MODE_DILOCO) {
+    if (!diloco_sync(step, diloco_period)) return 0;
+    kv = DEMO_CHUNK;
+  } else {
+    kv = static_cast<size_t>(k);
   }
+  if (wire == DEMO_WIRE_TERNARY) {
+    if (idx_bytes && mode == DEMO_MODE_DEMO) *idx_bytes = T * static_cast<size_t>(k) * 20;
+    return T * kv * 8;
+  }
+  if (idx_bytes && mode == DEMO_MODE_DEMO) *idx_bytes = nc * static_cast<size_t>(k);
+  return nc * kv * (wire == DEMO_WIRE_F32 ? 4 : 2);
 }
 
-int demo_encode(const void* g, int grad_dtype, float* m, int64_t n, int chunk, int k, float beta, int mode,
-                int sign, int diloco_period, uint64_t seed, uint64_t step, float* vals, uint8_t* idx,
-                void* stream) {
+size_t demo_payload_bytes(int mode, int64_t n, int chunk, int k, uint64_t step, int diloco_period,
+                          size_t* idx_bytes) {
+  return demo_payload_bytes_wire(mode, n, chunk, k, step, diloco_period, DEMO_WIRE_F32, idx_bytes);
+}
+
+int demo_encode_wire(const void* g, int grad_dtype, float* m, int64_t n, int chunk, int k, float beta, int mode,
+                     int sign, int diloco_period, uint64_t seed, uint64_t step, int wire, void* vals, void* idx,
+                     void* stream) {
   int s = check_shape(n, chunk, k, mode, diloco_period);
   if (s != DEMO_OK) return s;
   if (grad_dtype != DEMO_GRAD_F32 && grad_dtype != DEMO_GRAD_BF16) return DEMO_EINVAL;
   if (sign != 0 && sign != 1) return DEMO_EINVAL;
+  if (!valid_wire(wire) || (wire == DEMO_WIRE_TERNARY && !sign)) return DEMO_EINVAL;
   if (!std::isfinite(beta)) return DEMO_EINVAL;
   const bool sends = mode != DEMO_MODE_DILOCO || diloco_sync(step, diloco_period);
   if (g == nullptr || m == nullptr) return DEMO_EINVAL;
@@ -294,6 +308,7 @@ int demo_encode(const void* g, int grad_dtype, float* m, int64_t n, int chunk, i
   p.k = (mode == DEMO_MODE_DILOCO) ? DEMO_CHUNK : k;
   p.sign = sign;
   p.sync = (mode == DEMO_MODE_DILOCO) ? (sends ? 1 : 0) : 1;
+  p.wire = wire;
   fill_selection(p, mode, p.k, seed, step);
   p.stride_mask = (mode == DEMO_MODE_STRIDE) ? stride_mask(p.stride_o, p.stride_ns, k) : 0u;
   p.beta = beta;
@@ -301,12 +316,20 @@ int demo_encode(const void* g, int grad_dtype, float* m, int64_t n, int chunk, i
   return to_status(launch_encode(p, mode, bf16, grid_for(p.ntiles, st), static_cast<cudaStream_t>(stream)));
 }
 
-int demo_decode_update(float* theta, int64_t n, int chunk, int k, float lr, int mode, int R,
-                       const float* const* vals, const uint8_t* const* idx, int diloco_period, uint64_t seed,
-                       uint64_t step, void* stream) {
+int demo_encode(const void* g, int grad_dtype, float* m, int64_t n, int chunk, int k, float beta, int mode,
+                int sign, int diloco_period, uint64_t seed, uint64_t step, float* vals, uint8_t* idx,
+                void* stream) {
+  return demo_encode_wire(g, grad_dtype, m, n, chunk, k, beta, mode, sign, diloco_period, seed, step,
+                          DEMO_WIRE_F32, vals, idx, stream);
+}
+
+int demo_decode_update_wire(float* theta, int64_t n, int chunk, int k, float lr, int mode, int R,
+                            const void* const* vals, const void* const* idx, int diloco_period, uint64_t seed,
+                            uint64_t step, int wire, void* stream) {
   int s = check_shape(n, chunk, k, mode, diloco_period);
   if (s != DEMO_OK) return s;
   if (R < 1 || R > DEMO_MAX_REPLICAS) return DEMO_EINVAL;
+  if (!valid_wire(wire)) return DEMO_EINVAL;
   if (!std::isfinite(lr)) return DEMO_EINVAL;
   if (theta == nullptr || vals == nullptr) return DEMO_EINVAL;
   if (mode == DEMO_MODE_DEMO && idx == nullptr) return DEMO_EINVAL;
@@ -325,18 +348,28 @@ int demo_decode_update(float* theta, int64_t n, int chunk, int k, float lr, int 
   if (s != DEMO_OK) return s;
   if (!sends) return DEMO_OK;  // DiLoCo between syncs: theta does not move
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  return R <= kSmallReplicas ? run_decode<kSmallReplicas>(st, theta, n, k, lr, mode, R, vals, idx, seed, step, cs)
-                             : run_decode<kMaxReplicas>(st, theta, n, k, lr, mode, R, vals, idx, seed, step, cs);
+  return R <= kSmallReplicas
+             ? run_decode<kSmallReplicas>(st, theta, n, k, lr, mode, R, vals, idx, seed, step, wire, cs)
+             : run_decode<kMaxReplicas>(st, theta, n, k, lr, mode, R, vals, idx, seed, step, wire, cs);
 }
 
-int demo_step(float* theta, int64_t n, int chunk, int k, float beta, float lr, int mode, int sign, int R,
-              const void* const* g, int grad_dtype, float* const* m, int diloco_period, uint64_t seed,
-              uint64_t step, void* stream) {
+int demo_decode_update(float* theta, int64_t n, int chunk, int k, float lr, int mode, int R,
+                       const float* const* vals, const uint8_t* const* idx, int diloco_period, uint64_t seed,
+                       uint64_t step, void* stream) {
+  return demo_decode_update_wire(theta, n, chunk, k, lr, mode, R, reinterpret_cast<const void* const*>(vals),
+                                 reinterpret_cast<const void* const*>(idx), diloco_period, seed, step, DEMO_WIRE_F32,
+                                 stream);
+}
+
+int demo_step_wire(float* theta, int64_t n, int chunk, int k, float beta, float lr, int mode, int sign, int R,
+                   const void* const* g, int grad_dtype, float* const* m, int diloco_period, uint64_t seed,
+                   uint64_t step, int wire, void* stream) {
   int s = check_shape(n, chunk, k, mode, diloco_period);
   if (s != DEMO_OK) return s;
   if (R < 1 || R > DEMO_MAX_REPLICAS) return DEMO_EINVAL;
   if (grad_dtype != DEMO_GRAD_F32 && grad_dtype != DEMO_GRAD_BF16) return DEMO_EINVAL;
   if (sign != 0 && sign != 1) return DEMO_EINVAL;
+  if (!valid_wire(wire) || (wire == DEMO_WIRE_TERNARY && !sign)) return DEMO_EINVAL;
   if (!std::isfinite(beta) || !std::isfinite(lr)) return DEMO_EINVAL;
   if (theta == nullptr || g == nullptr || m == nullptr) return DEMO_EINVAL;
   for (int r = 0; r < R; ++r)
@@ -362,9 +395,44 @@ int demo_step(float* theta, int64_t n, int chunk, int k, float beta, float lr, i
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   return R <= kSmallReplicas
              ? run_step<kSmallReplicas>(st, theta, n, k, beta, lr, mode, sign, R, g, grad_dtype, m, diloco_period,
-                                        seed, step, cs)
+                                        seed, step, wire, cs)
              : run_step<kMaxReplicas>(st, theta, n, k, beta, lr, mode, sign, R, g, grad_dtype, m, diloco_period,
-                                      seed, step, cs);
+                                      seed, step, wire, cs);
+}
+
+int demo_step(float* theta, int64_t n, int chunk, int k, float beta, float lr, int mode, int sign, int R,
+              const void* const* g, int grad_dtype, float* const* m, int diloco_period, uint64_t seed,
+              uint64_t step, void* stream) {
+  return demo_step_wire(theta, n, chunk, k, beta, lr, mode, sign, R, g, grad_dtype, m, diloco_period, seed, step,
+                        DEMO_WIRE_F32, stream);
+}
+
+int demo_validate_payload(int64_t n, int chunk, int k, int wire, const void* idx_host, int64_t* first_bad) {
+  if (first_bad) *first_bad = -1;
+  if (check_shape(n, chunk, k, DEMO_MODE_DEMO, 1) != DEMO_OK || !valid_wire(wire) || idx_host == nullptr)
+    return DEMO_EINVAL;
+  const int64_t nc = n / DEMO_CHUNK;
+  for (int64_t c = 0; c < nc; ++c) {
+    int prev = -1;
+    bool ok = true;
+    for (int j = 0; j < k && ok; ++j) {
+      int u;
+      if (wire == DEMO_WIRE_TERNARY) {
+        const uint32_t* w = static_cast<const uint32_t*>(idx_host) + ((c / 32) * k + j) * 5;
+        u = 0;
+        for (int b = 0; b < 5; ++b) u |= static_cast<int>((w[b] >> (c % 32)) & 1u) << b;
+      } else {
+        u = static_cast<const uint8_t*>(idx_host)[c * k + j];
+      }
+      ok = u < DEMO_CHUNK && u > prev;
+      prev = u;
+    }
+    if (!ok) {
+      if (first_bad) *first_bad = c;
+      return DEMO_EINVAL;
+    }
+  }
+  return DEMO_OK;
 }
 
 int demo_device_fault(unsigned int* code) {

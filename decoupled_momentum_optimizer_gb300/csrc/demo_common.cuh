@@ -10,6 +10,8 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -24,6 +26,24 @@ constexpr unsigned kFaultLoadTimeout = 1u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 enum { kModeDemo = 0, kModeRandom = 1, kModeStride = 2, kModeDiloco = 3 };
+enum { kWireF32 = 0, kWireTernary = 1, kWireBF16 = 2, kWireF16 = 3 };
+
+// The value a receiver decodes from v sent in `wire` (nearest-even 16-bit rounding).
+__device__ __forceinline__ float wire_round(float v, int wire) {
+  if (wire == kWireBF16) return __bfloat162float(__float2bfloat16_rn(v));
+  if (wire == kWireF16) return __half2float(__float2half_rn(v));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t wire_bits16(float v, int wire) {
+  if (wire == kWireBF16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  return __half_as_ushort(__float2half_rn(v));
+}
+
+__device__ __forceinline__ float wire_from_bits16(uint32_t b, int wire) {
+  if (wire == kWireBF16) return __bfloat162float(__ushort_as_bfloat16(static_cast<unsigned short>(b)));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(b)));
+}
 
 // ----------------------------------------------------------------------------
 // PTX wrappers: shared-memory addresses, mbarriers, TMA, proxy fences

@@ -6,8 +6,9 @@
 // steps 6-7 (the synchronised Q_t), "2. Replication Schemes" table.
 //
 // Per warp, theta tiles of 32 chunks stream through a two-slot TMA ring; lane
-// i combines the payload entries of its chunk (replicas in order 0..R-1) in
-// shared-memory accumulators, forms Q and updates its theta row, which leaves
+// i combines the payload entries of its chunk (replicas in order 0..R-1, read in
+// the payload's wire format) in shared-memory accumulators, forms Q and updates
+// its theta row, which leaves
 // through the tile's own slot with coalesced stores.  The arithmetic matches
 // the fused step operation by operation, so split and fused results are
 // bit-identical.
@@ -25,53 +26,82 @@ constexpr int kDecWarps = kStepWarps;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr size_t kDecSmem = 1024 + kDecWarps * sizeof(DecWarpSmem) + kDecWarps * 16 + 272;
 
-// Load k payload values (and index bytes) of one chunk; k in {1, 2, 4, 8} uses one vector load each.
-__device__ __forceinline__ void load_payload(const float* vrow, const uint8_t* irow, float (&pv)[8], uint32_t& ilo,
-                                             uint32_t& ihi, int k) {
+__device__ __forceinline__ bool vector_kd(int k) { return k == 1 || k == 2 || k == 4 || k == 8; }
+
+// Value j of chunk c (tile `tile`, lane `lane`) of a payload with kv values per chunk.
+__device__ __forceinline__ float payload_value(const void* vals, int wire, long long c, long long tile, int lane,
+                                               int kv, int j) {
+  if (wire == kWireF32) return static_cast<const float*>(vals)[c * kv + j];
+  if (wire == kWireTernary) {
+    const uint2 w = reinterpret_cast<const uint2*>(vals)[tile * kv + j];
+    const uint32_t nz = (w.x >> lane) & 1u, ng = (w.y >> lane) & 1u;
+    return nz ? (ng ? -1.0f : 1.0f) : 0.0f;
+  }
+  return wire_from_bits16(static_cast<const uint16_t*>(vals)[c * kv + j], wire);
+}
+
+// Index j of chunk c in a DeMo payload (uint8, or 5 ternary bit-planes); used modulo 32.
+__device__ __forceinline__ int payload_index(const void* idx, int wire, long long c, long long tile, int lane, int k,
+                                             int j) {
+  if (wire == kWireTernary) {
+    const uint32_t* w = static_cast<const uint32_t*>(idx) + (tile * k + j) * 5;
+    int u = 0;
+#pragma unroll
+    for (int b = 0; b < 5; ++b) u |= static_cast<int>((w[b] >> lane) & 1u) << b;
+    return u;
+  }
+  return static_cast<const uint8_t*>(idx)[c * k + j] & 31;
+}
+
+// Vector load of one chunk's k values (k in {1, 2, 4, 8}; float32 or 16-bit wire) and its index bytes.
+__device__ __forceinline__ void load_payload(const void* vals, const void* idx, int wire, long long c, int k,
+                                             float (&pv)[8], uint32_t& ilo, uint32_t& ihi) {
   ilo = ihi = 0;
-  switch (k) {
-    case 1:
-      pv[0] = vrow[0];
-      if (irow) ilo = irow[0];
-      break;
-    case 2: {
-      const float2 v = *reinterpret_cast<const float2*>(vrow);
-      pv[0] = v.x;
-      pv[1] = v.y;
-      if (irow) ilo = *reinterpret_cast<const uint16_t*>(irow);
-      break;
-    }
-    case 4: {
-      const float4 v = *reinterpret_cast<const float4*>(vrow);
-      pv[0] = v.x;
-      pv[1] = v.y;
-      pv[2] = v.z;
-      pv[3] = v.w;
-      if (irow) ilo = *reinterpret_cast<const uint32_t*>(irow);
-      break;
-    }
-    default: {  // 8
-      const float4 a = reinterpret_cast<const float4*>(vrow)[0];
-      const float4 b = reinterpret_cast<const float4*>(vrow)[1];
-      pv[0] = a.x;
-      pv[1] = a.y;
-      pv[2] = a.z;
-      pv[3] = a.w;
-      pv[4] = b.x;
-      pv[5] = b.y;
-      pv[6] = b.z;
-      pv[7] = b.w;
-      if (irow) {
-        const uint2 w = *reinterpret_cast<const uint2*>(irow);
-        ilo = w.x;
-        ihi = w.y;
+  if (wire == kWireF32) {
+    const float* vrow = static_cast<const float*>(vals) + c * k;
+    switch (k) {
+      case 1: pv[0] = vrow[0]; break;
+      case 2: { const float2 v = *reinterpret_cast<const float2*>(vrow); pv[0] = v.x; pv[1] = v.y; break; }
+      case 4: {
+        const float4 v = *reinterpret_cast<const float4*>(vrow);
+        pv[0] = v.x; pv[1] = v.y; pv[2] = v.z; pv[3] = v.w;
+        break;
       }
-      break;
+      default: {
+        const float4 a = reinterpret_cast<const float4*>(vrow)[0];
+        const float4 b = reinterpret_cast<const float4*>(vrow)[1];
+        pv[0] = a.x; pv[1] = a.y; pv[2] = a.z; pv[3] = a.w;
+        pv[4] = b.x; pv[5] = b.y; pv[6] = b.z; pv[7] = b.w;
+      }
+    }
+  } else {
+    const uint16_t* vrow = static_cast<const uint16_t*>(vals) + c * k;
+    uint32_t h[4] = {0, 0, 0, 0};
+    switch (k) {
+      case 1: h[0] = vrow[0]; break;
+      case 2: h[0] = *reinterpret_cast<const uint32_t*>(vrow); break;
+      case 4: { const uint2 v = *reinterpret_cast<const uint2*>(vrow); h[0] = v.x; h[1] = v.y; break; }
+      default: {
+        const uint4 v = *reinterpret_cast<const uint4*>(vrow);
+        h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      pv[2 * i] = wire_from_bits16(h[i] & 0xffffu, wire);
+      pv[2 * i + 1] = wire_from_bits16(h[i] >> 16, wire);
+    }
+  }
+  if (idx) {
+    const uint8_t* irow = static_cast<const uint8_t*>(idx) + c * k;
+    switch (k) {
+      case 1: ilo = irow[0]; break;
+      case 2: ilo = *reinterpret_cast<const uint16_t*>(irow); break;
+      case 4: ilo = *reinterpret_cast<const uint32_t*>(irow); break;
+      default: { const uint2 w = *reinterpret_cast<const uint2*>(irow); ilo = w.x; ihi = w.y; }
     }
   }
 }
-
-__device__ __forceinline__ bool vector_kd(int k) { return k == 1 || k == 2 || k == 4 || k == 8; }
 
 template <int MODE, int MAXR>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_constant__ DecodeParams<MAXR> p) {
@@ -135,14 +165,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
 
     float Q[32];
     if constexpr (MODE == kModeDemo) {
-      if (valid) {
-        for (int r = 0; r < p.R; ++r) {
-          const float* vrow = p.vals[r] + c * p.k;
-          const uint8_t* irow = p.idx[r] + c * p.k;
-          if (vector_kd(p.k)) {
+      const long long tile = row0 >> 5;
+      for (int r = 0; r < p.R; ++r) {
+        if (p.wire != kWireTernary && vector_kd(p.k)) {
+          if (valid) {
             float pv[8];
             uint32_t ilo, ihi;
-            load_payload(vrow, irow, pv, ilo, ihi, p.k);
+            load_payload(p.vals[r], p.idx[r], p.wire, c, p.k, pv, ilo, ihi);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               if (j < p.k) {
@@ -153,11 +182,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
                 ws.acc[u * 32 + lane] = a;
               }
             }
-          } else {
-            for (int j = 0; j < p.k; ++j) {
-              const int u = irow[j] & 31;
+          }
+        } else {
+          // Per-chunk formats are read only for chunks that exist; the ternary words
+          // belong to the whole tile and are read by every lane.
+          const bool reads = valid || p.wire == kWireTernary;
+          for (int j = 0; j < p.k; ++j) {
+            const int u = reads ? payload_index(p.idx[r], p.wire, c, tile, lane, p.k, j) : 0;
+            const float v = reads ? payload_value(p.vals[r], p.wire, c, tile, lane, p.k, j) : 0.0f;
+            if (valid) {
               float2 a = ws.acc[u * 32 + lane];
-              a.x += vrow[j];
+              a.x += v;
               a.y += 1.0f;
               ws.acc[u * 32 + lane] = a;
             }
@@ -175,16 +210,38 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     } else if constexpr (MODE == kModeDiloco) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) Q[i] = 0.0f;
-      if (valid) {
-        for (int r = 0; r < p.R; ++r) {
-          const float4* vrow = reinterpret_cast<const float4*>(p.vals[r] + c * 32);
+      for (int r = 0; r < p.R; ++r) {
+        if (p.wire == kWireTernary) {
+          const uint2* w = reinterpret_cast<const uint2*>(p.vals[r]) + (row0 >> 5) * 32;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 v = vrow[j];
-            Q[4 * j + 0] += v.x;
-            Q[4 * j + 1] += v.y;
-            Q[4 * j + 2] += v.z;
-            Q[4 * j + 3] += v.w;
+          for (int j = 0; j < 32; ++j) {
+            const uint2 b = w[j];
+            const float v = ((b.x >> lane) & 1u) ? (((b.y >> lane) & 1u) ? -1.0f : 1.0f) : 0.0f;
+            Q[j] += valid ? v : 0.0f;
+          }
+        } else if (valid) {
+          if (p.wire == kWireF32) {
+            const float4* vrow = reinterpret_cast<const float4*>(static_cast<const float*>(p.vals[r]) + c * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 v = vrow[j];
+              Q[4 * j + 0] += v.x;
+              Q[4 * j + 1] += v.y;
+              Q[4 * j + 2] += v.z;
+              Q[4 * j + 3] += v.w;
+            }
+          } else {
+            const uint4* vrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.vals[r]) + c * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 v = vrow[j];
+              const uint32_t h[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                Q[8 * j + 2 * i] += wire_from_bits16(h[i] & 0xffffu, p.wire);
+                Q[8 * j + 2 * i + 1] += wire_from_bits16(h[i] >> 16, p.wire);
+              }
+            }
           }
         }
       }
@@ -195,17 +252,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
       float* qs = reinterpret_cast<float*>(ws.acc);  // [i][lane] scratch (first 4 KB)
 #pragma unroll
       for (int i = 0; i < 32; ++i) qs[i * 32 + lane] = 0.0f;
+      const long long tile = row0 >> 5;
+      const bool reads = valid || p.wire == kWireTernary;  // as in the DeMo branch
       auto take = [&](int j, int pos) {
         float sum = 0.0f;
-        for (int r = 0; r < p.R; ++r) sum += p.vals[r][c * p.k + j];
-        qs[pos * 32 + lane] = sum * p.rcpR;
+        for (int r = 0; r < p.R; ++r) sum += reads ? payload_value(p.vals[r], p.wire, c, tile, lane, p.k, j) : 0.0f;
+        if (valid) qs[pos * 32 + lane] = sum * p.rcpR;
       };
-      if (valid) {
-        if constexpr (MODE == kModeRandom) {
-          random_draws(p.hbase, static_cast<uint64_t>(c), p.k, take);
-        } else {
-          for (int j = 0; j < p.k; ++j) take(j, stride_position(p.stride_o, p.stride_ns, j));
-        }
+      if constexpr (MODE == kModeRandom) {
+        random_draws(p.hbase, static_cast<uint64_t>(c), p.k, take);
+      } else {
+        for (int j = 0; j < p.k; ++j) take(j, stride_position(p.stride_o, p.stride_ns, j));
       }
 #pragma unroll
       for (int i = 0; i < 32; ++i) Q[i] = qs[i * 32 + lane];

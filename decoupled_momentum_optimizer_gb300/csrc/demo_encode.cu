@@ -8,9 +8,11 @@
 // Same warp/tile organisation as the fused step: per warp, tiles of 32 chunks
 // stream through a two-slot TMA ring; each lane encodes its chunk in registers;
 // the new momentum leaves through the tile's own slot with coalesced stores and
-// the slot is refilled at once.  The payload of chunk c is written to
-// vals[c*k .. c*k+k) (and idx for DeMo) by the lane that owns c, as one vector
-// store when k is 1, 2, 4 or 8.
+// the slot is refilled at once.  The payload is written in the requested wire
+// format: float32 / 16-bit values of chunk c at vals[c*k .. c*k+k) (and uint8
+// indices for DeMo) by the lane that owns c, as one vector store when k is 1, 2,
+// 4 or 8; or ternary bit-planes, one 32-bit word per warp tile and value slot
+// built with warp ballots.
 #include "demo_common.cuh"
 #include "demo_params.h"
 
@@ -25,31 +27,122 @@ constexpr int kEncWarps = kStepWarps;
 constexpr int kEncThreads = kEncWarps * 32;
 constexpr size_t kEncSmem = 1024 + kEncWarps * sizeof(EncWarpSmem) + kEncWarps * 16;
 
-// Store k payload values (and index bytes) of one chunk; k in {1, 2, 4, 8} uses one vector store each.
-__device__ __forceinline__ void store_payload(float* vrow, uint8_t* irow, const float (&pv)[8], uint32_t ilo,
-                                              uint32_t ihi, int k) {
-  switch (k) {
-    case 1:
-      vrow[0] = pv[0];
-      if (irow) irow[0] = static_cast<uint8_t>(ilo);
-      break;
-    case 2:
-      *reinterpret_cast<float2*>(vrow) = make_float2(pv[0], pv[1]);
-      if (irow) *reinterpret_cast<uint16_t*>(irow) = static_cast<uint16_t>(ilo);
-      break;
-    case 4:
-      *reinterpret_cast<float4*>(vrow) = make_float4(pv[0], pv[1], pv[2], pv[3]);
-      if (irow) *reinterpret_cast<uint32_t*>(irow) = ilo;
-      break;
-    default:  // 8
-      reinterpret_cast<float4*>(vrow)[0] = make_float4(pv[0], pv[1], pv[2], pv[3]);
-      reinterpret_cast<float4*>(vrow)[1] = make_float4(pv[4], pv[5], pv[6], pv[7]);
-      if (irow) *reinterpret_cast<uint2*>(irow) = make_uint2(ilo, ihi);
-      break;
+__device__ __forceinline__ bool vector_k(int k) { return k == 1 || k == 2 || k == 4 || k == 8; }
+
+// Collects one chunk's payload entries (slot j: value v, index u) and writes
+// them in the wire format.  put() must be called by all 32 lanes of the warp
+// for the same j (the ternary format packs the warp's chunks with ballots).
+struct PayloadOut {
+  void* vals;
+  void* idx;       // nullptr unless DeMo
+  long long c;     // this lane's chunk
+  long long tile;  // the warp's tile (chunks 32 tile .. 32 tile + 31)
+  int lane, k, wire;
+  bool valid, vec;
+  float pv[8];
+  uint32_t ilo, ihi;
+
+  __device__ __forceinline__ void put(int j, int u, float v) {
+    if (wire == kWireTernary) {
+      const uint32_t nz = __ballot_sync(0xffffffffu, valid && v != 0.0f);
+      const uint32_t ng = __ballot_sync(0xffffffffu, valid && v < 0.0f);
+      uint32_t* vw = static_cast<uint32_t*>(vals) + (tile * k + j) * 2;
+      if (lane == 0) {
+        vw[0] = nz;
+        vw[1] = ng;
+      }
+      if (idx) {
+        uint32_t* iw = static_cast<uint32_t*>(idx) + (tile * k + j) * 5;
+#pragma unroll
+        for (int b = 0; b < 5; ++b) {
+          const uint32_t w = __ballot_sync(0xffffffffu, valid && ((u >> b) & 1));
+          if (lane == 0) iw[b] = w;
+        }
+      }
+      return;
+    }
+    if (vec) {
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) pv[jj] = (jj == j) ? v : pv[jj];
+      if (j < 4) ilo |= static_cast<uint32_t>(u) << (8 * j);
+      else ihi |= static_cast<uint32_t>(u) << (8 * (j - 4));
+      return;
+    }
+    if (!valid) return;
+    if (wire == kWireF32) static_cast<float*>(vals)[c * k + j] = v;
+    else static_cast<uint16_t*>(vals)[c * k + j] = static_cast<uint16_t>(wire_bits16(v, wire));
+    if (idx) static_cast<uint8_t*>(idx)[c * k + j] = static_cast<uint8_t>(u);
+  }
+
+  // Vector store of the collected entries (k in {1, 2, 4, 8}, value formats other than ternary).
+  __device__ __forceinline__ void finish() {
+    if (wire == kWireTernary || !vec || !valid) return;
+    uint8_t* irow = idx ? static_cast<uint8_t*>(idx) + c * k : nullptr;
+    if (wire == kWireF32) {
+      float* vrow = static_cast<float*>(vals) + c * k;
+      switch (k) {
+        case 1: vrow[0] = pv[0]; break;
+        case 2: *reinterpret_cast<float2*>(vrow) = make_float2(pv[0], pv[1]); break;
+        case 4: *reinterpret_cast<float4*>(vrow) = make_float4(pv[0], pv[1], pv[2], pv[3]); break;
+        default:
+          reinterpret_cast<float4*>(vrow)[0] = make_float4(pv[0], pv[1], pv[2], pv[3]);
+          reinterpret_cast<float4*>(vrow)[1] = make_float4(pv[4], pv[5], pv[6], pv[7]);
+      }
+    } else {
+      uint32_t h[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h[i] = wire_bits16(pv[2 * i], wire) | (wire_bits16(pv[2 * i + 1], wire) << 16);
+      uint16_t* vrow = static_cast<uint16_t*>(vals) + c * k;
+      switch (k) {
+        case 1: vrow[0] = static_cast<uint16_t>(h[0]); break;
+        case 2: *reinterpret_cast<uint32_t*>(vrow) = h[0]; break;
+        case 4: *reinterpret_cast<uint2*>(vrow) = make_uint2(h[0], h[1]); break;
+        default: *reinterpret_cast<uint4*>(vrow) = make_uint4(h[0], h[1], h[2], h[3]);
+      }
+    }
+    if (irow) {
+      switch (k) {
+        case 1: irow[0] = static_cast<uint8_t>(ilo); break;
+        case 2: *reinterpret_cast<uint16_t*>(irow) = static_cast<uint16_t>(ilo); break;
+        case 4: *reinterpret_cast<uint32_t*>(irow) = ilo; break;
+        default: *reinterpret_cast<uint2*>(irow) = make_uint2(ilo, ihi);
+      }
+    }
+  }
+};
+
+// DiLoCo sync step: the whole row of 32 values of this lane's chunk, in the wire format.
+__device__ __forceinline__ void put_row(void* vals, int wire, long long c, long long tile, int lane, bool valid,
+                                        const float (&v)[32]) {
+  if (wire == kWireTernary) {
+    uint32_t my_nz = 0, my_ng = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t nz = __ballot_sync(0xffffffffu, valid && v[j] != 0.0f);
+      const uint32_t ng = __ballot_sync(0xffffffffu, valid && v[j] < 0.0f);
+      my_nz = (lane == j) ? nz : my_nz;
+      my_ng = (lane == j) ? ng : my_ng;
+    }
+    reinterpret_cast<uint2*>(static_cast<uint32_t*>(vals) + tile * 64)[lane] = make_uint2(my_nz, my_ng);
+    return;
+  }
+  if (!valid) return;
+  if (wire == kWireF32) {
+    float4* row = reinterpret_cast<float4*>(static_cast<float*>(vals) + c * 32);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) row[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  } else {
+    uint4* row = reinterpret_cast<uint4*>(static_cast<uint16_t*>(vals) + c * 32);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t h[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        h[i] = wire_bits16(v[8 * j + 2 * i], wire) | (wire_bits16(v[8 * j + 2 * i + 1], wire) << 16);
+      row[j] = make_uint4(h[0], h[1], h[2], h[3]);
+    }
   }
 }
-
-__device__ __forceinline__ bool vector_k(int k) { return k == 1 || k == 2 || k == 4 || k == 8; }
 
 template <int MODE, bool BF16>
 __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_constant__ EncodeParams p) {
@@ -118,52 +211,26 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
       const uint32_t M = topk_select(X, p.k, Xs);
 #pragma unroll
       for (int u = 0; u < 32; ++u) scratch[u * 32 + lane] = Xs[u];
-      float* vrow = p.vals + c * p.k;
-      uint8_t* irow = p.idx + c * p.k;
+      PayloadOut out{p.vals, p.idx, c, row0 >> 5, lane, p.k, p.wire, valid, vector_k(p.k) && p.wire != kWireTernary,
+                     {0, 0, 0, 0, 0, 0, 0, 0}, 0u, 0u};
       uint32_t mm = M;
-      if (vector_k(p.k)) {
-        float pv[8];
-        uint32_t ilo = 0, ihi = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          pv[j] = 0.0f;
-          if (j < p.k) {
-            const int u = __ffs(mm) - 1;
-            mm &= mm - 1;
-            const float v = scratch[u * 32 + lane];
-            pv[j] = p.sign ? sign3(v) : v;
-            if (j < 4) ilo |= static_cast<uint32_t>(u) << (8 * j);
-            else ihi |= static_cast<uint32_t>(u) << (8 * (j - 4));
-          }
-        }
-        if (valid) store_payload(vrow, irow, pv, ilo, ihi, p.k);
-      } else {
-        for (int j = 0; j < p.k; ++j) {
-          const int u = __ffs(mm) - 1;
-          mm &= mm - 1;
-          float v = scratch[u * 32 + lane];
-          if (p.sign) v = sign3(v);
-          if (valid) {
-            vrow[j] = v;
-            irow[j] = static_cast<uint8_t>(u);
-          }
-        }
+      for (int j = 0; j < p.k; ++j) {  // payload in ascending u
+        const int u = __ffs(mm) - 1;
+        mm &= mm - 1;
+        const float v = scratch[u * 32 + lane];
+        out.put(j, u, p.sign ? sign3(v) : v);
       }
+      out.finish();
       float q[32];
       dct32_inverse(Xs, q);
 #pragma unroll
       for (int i = 0; i < 32; ++i) x[i] -= q[i];
     } else if constexpr (MODE == kModeDiloco) {
       if (p.sync) {
-        if (valid) {
-          float4* vrow = reinterpret_cast<float4*>(p.vals + c * 32);
+        float sv[32];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            float4 v = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-            if (p.sign) v = make_float4(sign3(v.x), sign3(v.y), sign3(v.z), sign3(v.w));
-            vrow[j] = v;
-          }
-        }
+        for (int i = 0; i < 32; ++i) sv[i] = p.sign ? sign3(x[i]) : x[i];
+        put_row(p.vals, p.wire, c, row0 >> 5, lane, valid, sv);
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = 0.0f;
       }
@@ -171,38 +238,20 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
       // Random / Striding: values at the selected positions, in draw order.
 #pragma unroll
       for (int i = 0; i < 32; ++i) scratch[i * 32 + lane] = x[i];
-      float* vrow = p.vals + c * p.k;
+      PayloadOut out{p.vals, nullptr, c, row0 >> 5, lane, p.k, p.wire, valid,
+                     vector_k(p.k) && p.wire != kWireTernary, {0, 0, 0, 0, 0, 0, 0, 0}, 0u, 0u};
+      auto emit = [&](int j, int pos) {
+        const float v = scratch[pos * 32 + lane];
+        out.put(j, pos, p.sign ? sign3(v) : v);
+      };
       uint32_t P;
-      if (vector_k(p.k)) {
-        float pv[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) pv[j] = 0.0f;
-        auto emit = [&](int j, int pos) {
-          const float v = scratch[pos * 32 + lane];
-          const float w = p.sign ? sign3(v) : v;
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) pv[jj] = (jj == j) ? w : pv[jj];
-        };
-        if constexpr (MODE == kModeRandom) {
-          P = random_draws(p.hbase, static_cast<uint64_t>(c), p.k, emit);
-        } else {
-          for (int j = 0; j < p.k; ++j) emit(j, stride_position(p.stride_o, p.stride_ns, j));
-          P = p.stride_mask;
-        }
-        if (valid) store_payload(vrow, nullptr, pv, 0, 0, p.k);
+      if constexpr (MODE == kModeRandom) {
+        P = random_draws(p.hbase, static_cast<uint64_t>(c), p.k, emit);
       } else {
-        auto emit = [&](int j, int pos) {
-          float v = scratch[pos * 32 + lane];
-          if (p.sign) v = sign3(v);
-          if (valid) vrow[j] = v;
-        };
-        if constexpr (MODE == kModeRandom) {
-          P = random_draws(p.hbase, static_cast<uint64_t>(c), p.k, emit);
-        } else {
-          for (int j = 0; j < p.k; ++j) emit(j, stride_position(p.stride_o, p.stride_ns, j));
-          P = p.stride_mask;
-        }
+        for (int j = 0; j < p.k; ++j) emit(j, stride_position(p.stride_o, p.stride_ns, j));
+        P = p.stride_mask;
       }
+      out.finish();
 #pragma unroll
       for (int i = 0; i < 32; ++i) x[i] = ((P >> i) & 1u) ? 0.0f : x[i];
     }

@@ -27,6 +27,7 @@ struct StepParams {
   float beta, lr, rcpR;
   unsigned long long hbase;  // sm(sm(seed) ^ step) for the Random scheme
   float rcp_tab[kMaxReplicas + 1];  // float32(1/c), entry 0 = 0
+  int wire;                         // payload wire format the on-chip values are rounded to
   unsigned int* fault;
 };
 
@@ -34,10 +35,10 @@ struct EncodeParams {
   CUtensorMap g;
   CUtensorMap m;
   float* m_ptr;
-  float* vals;
-  uint8_t* idx;
+  void* vals;  // wire-format payload values
+  void* idx;   // DeMo indices (uint8 [nc][k], or uint32 bit-planes for the ternary format)
   long long nc, ntiles;
-  int k, sign, sync;
+  int k, sign, sync, wire;
   int stride_o, stride_ns;
   unsigned int stride_mask;
   float beta;
@@ -49,10 +50,10 @@ template <int MAXR>
 struct DecodeParams {
   CUtensorMap theta;
   float* theta_ptr;
-  const float* vals[MAXR];
-  const uint8_t* idx[MAXR];
+  const void* vals[MAXR];
+  const void* idx[MAXR];
   long long nc, ntiles;
-  int R, k;
+  int R, k, wire;
   int stride_o, stride_ns;
   float lr, rcpR;
   unsigned long long hbase;

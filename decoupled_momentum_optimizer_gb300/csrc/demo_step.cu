@@ -14,7 +14,9 @@
 // swizzled tile, the warp reads it back transposed and issues 512-byte
 // coalesced stores, and the slot is immediately refilled with the load for
 // item i + 2.  Shared memory per warp is 20 KB (two 8 KB slots and a 4 KB
-// payload accumulator), so 11 warps fit on an SM.
+// payload accumulator), so 11 warps fit on an SM.  With a 16-bit wire format
+// the accumulated values are rounded exactly as the split path's receiver
+// rounds them, so fused and split results stay bit-identical.
 #include "demo_common.cuh"
 #include "demo_params.h"
 
@@ -144,7 +146,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
           mm &= mm - 1;
           float v = stash[u * 32 + lane];
           if (p.sign) v = sign3(v);
-          ws.acc[u * 32 + lane] += v;
+          ws.acc[u * 32 + lane] += wire_round(v, p.wire);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) cnt8[i] += (((M >> (4 * i)) & 0xfu) * 0x204081u) & 0x01010101u;
@@ -154,20 +156,32 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         for (int i = 0; i < 32; ++i) x[i] -= q[i];
       } else if constexpr (MODE == kModeDiloco) {
         if (p.sync) {
+          if (p.wire >= kWireBF16) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            accr[i] += p.sign ? sign3(x[i]) : x[i];
-            x[i] = 0.0f;
+            for (int i = 0; i < 32; ++i) accr[i] += wire_round(p.sign ? sign3(x[i]) : x[i], p.wire);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) accr[i] += p.sign ? sign3(x[i]) : x[i];
           }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = 0.0f;
         }
       } else {
+        if (p.wire >= kWireBF16) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const bool in = (P >> i) & 1u;
-          const float v = p.sign ? sign3(x[i]) : x[i];
-          accr[i] += in ? v : 0.0f;
-          x[i] = in ? 0.0f : x[i];
+          for (int i = 0; i < 32; ++i) {
+            const bool in = (P >> i) & 1u;
+            accr[i] += in ? wire_round(p.sign ? sign3(x[i]) : x[i], p.wire) : 0.0f;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const bool in = (P >> i) & 1u;
+            accr[i] += in ? (p.sign ? sign3(x[i]) : x[i]) : 0.0f;
+          }
         }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = ((P >> i) & 1u) ? 0.0f : x[i];
       }
       store_tile_coalesced(ws.mbuf[s], lane, x, p.m_ptr[kind], row0, p.nc);
     } else {

@@ -144,7 +144,13 @@ def _cmul_const(P, z, ang):
     k = round(ang / (math.pi / 2))
     if abs(ang - k * math.pi / 2) < 1e-15:
         k %= 4
-        return [(re, im), (P.neg(im), re), (P.neg(re), P.neg(im)), (im, P.neg(re))][k]
+        if k == 0:
+            return (re, im)
+        if k == 1:
+            return (P.neg(im), re)
+        if k == 2:
+            return (P.neg(re), P.neg(im))
+        return (im, P.neg(re))
     r = P.fma(re, c, P.mul(im, -s))  # re c - im s
     i = P.fma(re, s, P.mul(im, c))   # re s + im c
     return (r, i)

@@ -76,6 +76,31 @@ enum demo_grad_dtype {
   DEMO_GRAD_BF16 = 1  /* bfloat16 gradients, widened exactly to float32 */
 };
 
+/*
+ * Wire formats of the payload (what the split path writes and reads):
+ *   DEMO_WIRE_F32      values float32 [n/32][kv]; DeMo indices uint8 [n/32][k].
+ *   DEMO_WIRE_TERNARY  sign must be 1.  Chunks are grouped in tiles of 32 (chunk c
+ *                      is bit c mod 32 of tile c / 32; T = ceil(n/32 / 32) tiles).
+ *                      Values: uint32 [T][kv][2]; word 0 has bit l set when value j
+ *                      of chunk 32t+l is nonzero, word 1 when it is negative.  DeMo
+ *                      indices: uint32 [T][k][5]; word b holds bit b of index j of
+ *                      every chunk of the tile.  Bits of chunks past the end are 0.
+ *                      2 bits per value and 5 per index instead of 32 and 8.
+ *   DEMO_WIRE_BF16     values rounded to nearest-even bfloat16, [n/32][kv] 16-bit
+ *                      words; indices as DEMO_WIRE_F32.
+ *   DEMO_WIRE_F16      values rounded to nearest-even float16, likewise.
+ * kv = k for DeMo, Random and Striding and 32 for DiLoCo.  The receiver decodes
+ * the rounded values; the ternary format is lossless for signed payloads.  The
+ * ternary values come from the sign subsection of the DeToNATION notes ("3. Sign
+ * function and hyper-parameters"), which also compares fp32 with fp16 payloads.
+ */
+enum demo_wire {
+  DEMO_WIRE_F32 = 0,
+  DEMO_WIRE_TERNARY = 1,
+  DEMO_WIRE_BF16 = 2,
+  DEMO_WIRE_F16 = 3
+};
+
 enum demo_status {
   DEMO_OK = 0,
   DEMO_EINVAL = -1,   /* an argument is out of range or a pointer is NULL */
@@ -146,6 +171,36 @@ int demo_decode_update(float* theta, int64_t n, int chunk, int k, float lr, int 
 int demo_step(float* theta, int64_t n, int chunk, int k, float beta, float lr, int mode,
               int sign, int R, const void* const* g, int grad_dtype, float* const* m,
               int diloco_period, uint64_t seed, uint64_t step, void* stream);
+
+/*
+ * Wire-format variants of the calls above.  `vals` / `idx` point to buffers laid
+ * out as the wire format states (device memory, 16-byte aligned); the other
+ * arguments are those of the plain calls, which equal these with DEMO_WIRE_F32.
+ * demo_step_wire rounds the values it accumulates on chip exactly as the split
+ * path's receiver would, so fused and split results stay bit-identical for
+ * every format.  DEMO_WIRE_TERNARY with sign == 0 returns DEMO_EINVAL.
+ */
+size_t demo_payload_bytes_wire(int mode, int64_t n, int chunk, int k, uint64_t step, int diloco_period,
+                               int wire, size_t* idx_bytes);
+int demo_encode_wire(const void* g, int grad_dtype, float* m, int64_t n, int chunk, int k, float beta,
+                     int mode, int sign, int diloco_period, uint64_t seed, uint64_t step, int wire,
+                     void* vals, void* idx, void* stream);
+int demo_decode_update_wire(float* theta, int64_t n, int chunk, int k, float lr, int mode, int R,
+                            const void* const* vals, const void* const* idx, int diloco_period,
+                            uint64_t seed, uint64_t step, int wire, void* stream);
+int demo_step_wire(float* theta, int64_t n, int chunk, int k, float beta, float lr, int mode, int sign,
+                   int R, const void* const* g, int grad_dtype, float* const* m, int diloco_period,
+                   uint64_t seed, uint64_t step, int wire, void* stream);
+
+/*
+ * demo_validate_payload -- host-side check of one replica's DeMo indices
+ * (host memory, wire layout as above): every chunk must list k distinct indices
+ * in [0, 32) in ascending order.  Returns DEMO_OK, or DEMO_EINVAL with
+ * *first_bad (if not NULL) set to the first offending chunk.  A receiver can run
+ * it on a payload from an untrusted link; the decode kernels themselves only
+ * use an index modulo 32, so a corrupt index never addresses outside its chunk.
+ */
+int demo_validate_payload(int64_t n, int chunk, int k, int wire, const void* idx_host, int64_t* first_bad);
 
 /* demo_status_string -- a static, human-readable name for a status code. */
 const char* demo_status_string(int status);

@@ -299,34 +299,39 @@ def scatter_mean(vals_list, pos_list, nc):
     return Y, cnt
 
 
-def decode_update(theta, vals_list, pos_list, lr, mode):
+def decode_update(theta, vals_list, pos_list, lr, mode, wire=0):
     """Algorithm 1 step 6 (combine) and step 7 (theta <- theta - lr Q).
 
     DeMo: Q = D^T Y (inverse DCT of the scatter-mean); the other schemes send
-    values in the parameter domain, so Q = Y.
+    values in the parameter domain, so Q = Y.  ``wire`` rounds the received
+    values as the wire format does (see the wire-format section below).
     """
     theta = np.asarray(theta, dtype=np.float64)
     n = theta.shape[0]
     nc = n // CHUNK
+    vals_list = [wire_round(v, wire) for v in vals_list]
     Y, cnt = scatter_mean(vals_list, pos_list, nc)
     Q = Y @ _D if mode == MODE_DEMO else Y
     new_theta = theta - f32(lr) * Q.reshape(n)
     return new_theta, Q, Y, cnt
 
 
-def step(theta, ms, gs, *, beta, lr, k, mode, sign, seed=0, step_idx=0, period=8, chunk_ids=None):
+def step(theta, ms, gs, *, beta, lr, k, mode, sign, seed=0, step_idx=0, period=8, chunk_ids=None, wire=0):
     """One full step over R replicas: encode every replica, combine, update.
 
     Returns (theta_new, [m_r new], info) where info holds the payloads, Q and
-    the per-replica near-tie flags.
+    the per-replica near-tie flags.  ``wire`` is the payload encoding (the
+    ternary format needs the sign flag).
     """
+    if wire == WIRE_TERNARY and not sign:
+        raise ValueError("the ternary wire format carries signed values only")
     encs = [
         encode(m, g, beta, k, mode, sign, seed=seed, step=step_idx, period=period, chunk_ids=chunk_ids)
         for m, g in zip(ms, gs)
     ]
     vals_list = [e["vals"] for e in encs]
     pos_list = [e["pos"] for e in encs]
-    new_theta, Q, Y, cnt = decode_update(theta, vals_list, pos_list, lr, mode)
+    new_theta, Q, Y, cnt = decode_update(theta, vals_list, pos_list, lr, mode, wire=wire)
     info = {
         "encodes": encs,
         "Q": Q,
@@ -358,3 +363,113 @@ def payload_bytes(mode, n, k, step=0, period=8, idx_bytes_per_entry=1):
     if mode == MODE_DILOCO:
         return (n * 4 if diloco_is_sync(step, period) else 0), 0
     raise ValueError("unknown mode")
+
+
+# ----------------------------------------------------------------------------
+# Wire formats of the payload (the compact encodings of the sent values)
+# ----------------------------------------------------------------------------
+#
+# WIRE_F32:     values float32 [nc][kv], DeMo indices uint8 [nc][k].
+# WIRE_TERNARY: sign must be on.  Chunks are grouped in tiles of 32 (chunk c is
+#               bit c mod 32 of tile c // 32).  Values: uint32 [T][kv][2], word 0
+#               has bit l set when value j of chunk 32t+l is nonzero, word 1 when it
+#               is negative.  DeMo indices: uint32 [T][k][5], word b holds bit b of
+#               index j of each chunk of the tile.  T = ceil(nc / 32); bits of
+#               chunks past nc are 0.
+# WIRE_BF16 / WIRE_F16: values rounded to nearest-even bfloat16 / float16,
+#               [nc][kv] 16-bit words; indices as WIRE_F32.
+# kv = k for DeMo, Random and Striding, 32 for DiLoCo.  The sign subsection of
+# the DeToNATION notes gives the three values; the fp32-versus-fp16 comparison
+# of the same subsection is what the 16-bit formats measure.
+
+WIRE_F32 = 0
+WIRE_TERNARY = 1
+WIRE_BF16 = 2
+WIRE_F16 = 3
+
+
+def round_bf16(x):
+    """float64 -> nearest bfloat16 (ties to even), returned as float64."""
+    x = np.asarray(x, dtype=np.float64)
+    f = x.astype(np.float32)  # exact for the values this is used on (float32 payloads)
+    b = f.view(np.uint32).astype(np.uint64)
+    lsb = (b >> 16) & 1
+    r = ((b + 0x7FFF + lsb) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def round_f16(x):
+    """float64 -> nearest float16 (ties to even), returned as float64."""
+    return np.asarray(x, dtype=np.float64).astype(np.float16).astype(np.float64)
+
+
+def wire_round(vals, wire):
+    """The value a receiver decodes from ``vals`` sent in ``wire``."""
+    if vals is None or wire in (WIRE_F32, WIRE_TERNARY):
+        return vals
+    if wire == WIRE_BF16:
+        return round_bf16(vals)
+    if wire == WIRE_F16:
+        return round_f16(vals)
+    raise ValueError("unknown wire format")
+
+
+def ternary_pack(vals, idx=None):
+    """Pack ternary values [nc][kv] (and DeMo indices [nc][k]) into tile bit-planes."""
+    vals = np.asarray(vals)
+    nc, kv = vals.shape
+    T = (nc + 31) // 32
+    vw = np.zeros((T, kv, 2), dtype=np.uint64)
+    iw = None if idx is None else np.zeros((T, idx.shape[1], 5), dtype=np.uint64)
+    for c in range(nc):
+        t, lane = divmod(c, 32)
+        for j in range(kv):
+            v = vals[c, j]
+            if v not in (-1.0, 0.0, 1.0):
+                raise ValueError("ternary wire format needs values in {-1, 0, 1}")
+            if v != 0:
+                vw[t, j, 0] |= 1 << lane
+            if v < 0:
+                vw[t, j, 1] |= 1 << lane
+        if idx is not None:
+            for j in range(idx.shape[1]):
+                for b in range(5):
+                    if (int(idx[c, j]) >> b) & 1:
+                        iw[t, j, b] |= 1 << lane
+    return vw.astype(np.uint32), (None if iw is None else iw.astype(np.uint32))
+
+
+def ternary_unpack(vw, iw, nc):
+    """Inverse of ternary_pack: values [nc][kv] as float64 and indices [nc][k] (or None)."""
+    T, kv, _ = vw.shape
+    vals = np.zeros((nc, kv))
+    idx = None if iw is None else np.zeros((nc, iw.shape[1]), dtype=np.int64)
+    for c in range(nc):
+        t, lane = divmod(c, 32)
+        for j in range(kv):
+            nz = (int(vw[t, j, 0]) >> lane) & 1
+            neg = (int(vw[t, j, 1]) >> lane) & 1
+            vals[c, j] = 0.0 if not nz else (-1.0 if neg else 1.0)
+        if iw is not None:
+            for j in range(iw.shape[1]):
+                idx[c, j] = sum(((int(iw[t, j, b]) >> lane) & 1) << b for b in range(5))
+    return vals, idx
+
+
+def payload_bytes_wire(mode, n, k, step=0, period=8, wire=WIRE_F32):
+    """(value bytes, index bytes) one replica sends in ``wire`` for one step."""
+    nc = n // CHUNK
+    T = (nc + 31) // 32
+    if mode == MODE_DILOCO:
+        if not diloco_is_sync(step, period):
+            return 0, 0
+        kv = CHUNK
+    else:
+        kv = k
+    if wire == WIRE_TERNARY:
+        vb = T * kv * 8
+        ib = T * k * 20 if mode == MODE_DEMO else 0
+    else:
+        vb = nc * kv * (4 if wire == WIRE_F32 else 2)
+        ib = nc * k if mode == MODE_DEMO else 0
+    return vb, ib

@@ -58,6 +58,13 @@ def test_payload_bytes_match_oracle(L):
                     got = dm.payload_bytes(mode, n, k, step=step, diloco_period=8)
                     want = ref.payload_bytes(dm.MODES[mode], n, k, step=step, period=8)
                     assert got == want, (mode, n, k, step)
+    for wire in ("f32", "ternary", "bf16", "f16"):
+        for mode in ("demo", "random", "diloco"):
+            for n in (32, 32 * 33, 222903552):
+                for step in (6, 7):
+                    got = dm.payload_bytes(mode, n, 4, step=step, diloco_period=8, wire=wire)
+                    want = ref.payload_bytes_wire(dm.MODES[mode], n, 4, step=step, period=8, wire=dm.WIRES[wire])
+                    assert got == want, (wire, mode, n, step)
     assert dm.payload_bytes("stride", 64, 3) == (0, 0)  # invalid: 3 does not divide 32
     assert dm.payload_bytes("demo", 33, 4) == (0, 0)
 
@@ -135,6 +142,32 @@ def test_decode_argument_checks(L):
     bad = (ctypes.c_void_p * 2)(0x30000, 0x40001)
     assert L.demo_decode_update(th, 64, 32, 4, 0.1, 1, 2, bad, None, 8, 0, 0, None) == EALIGN
     assert L.demo_decode_update(th, 64, 32, 4, 0.1, 0, 2, vals, idx, 8, 0, 0, None) in (ENOTINIT, ENODEV)
+
+
+def test_validate_payload_host(L):
+    import torch
+
+    import decoupled_momentum_optimizer_gb300 as dm
+
+    good = torch.tensor([[0, 3, 7, 31], [1, 2, 3, 4], [5, 9, 10, 11]], dtype=torch.uint8).reshape(-1)
+    assert dm.validate_payload(good, 96, 4) == (True, -1)
+    bad = good.clone()
+    bad[4 * 2 + 2] = 9  # duplicate in chunk 2
+    assert dm.validate_payload(bad, 96, 4) == (False, 2)
+    bad = good.clone()
+    bad[3] = 32  # out of range in chunk 0
+    assert dm.validate_payload(bad, 96, 4) == (False, 0)
+    assert L.demo_validate_payload(96, 32, 4, 0, None, None) == EINVAL
+
+
+def test_wire_argument_checks(L):
+    # ternary needs the sign flag
+    a = dict(g=p(0x10000), gd=0, m=p(0x20000), n=64, chunk=32, k=4, beta=0.9, mode=0, sign=0, period=8, seed=0,
+             step=0, vals=p(0x30000), idx=p(0x40000), stream=None)
+    assert L.demo_encode_wire(a["g"], 0, a["m"], 64, 32, 4, 0.9, 0, 0, 8, 0, 0, 1, a["vals"], a["idx"], None) == EINVAL
+    assert L.demo_encode_wire(a["g"], 0, a["m"], 64, 32, 4, 0.9, 0, 1, 8, 0, 0, 7, a["vals"], a["idx"], None) == EINVAL
+    assert L.demo_encode_wire(a["g"], 0, a["m"], 64, 32, 4, 0.9, 0, 1, 8, 0, 0, 1, a["vals"], a["idx"],
+                              None) in (ENOTINIT, ENODEV)
 
 
 def test_init_without_device(L):

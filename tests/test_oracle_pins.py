@@ -402,3 +402,64 @@ def test_golden_demo_step_unchanged():
     for (r, c), want in idx.items():
         assert list(info["encodes"][r]["idx"][c]) == want
     assert np.array_equal(np.array(th), th1)
+
+
+# ----------------------------------------------------------------------------
+# Wire formats
+# ----------------------------------------------------------------------------
+
+def test_ternary_pack_hand_example():
+    # three chunks (one partial tile), k = 4
+    vals = np.array([[1, 0, -1, 1], [0, 0, 0, 0], [-1, -1, 1, 0]], dtype=float)
+    idx = np.array([[0, 3, 17, 31], [1, 2, 3, 4], [5, 6, 7, 8]])
+    vw, iw = ref.ternary_pack(vals, idx)
+    assert vw.shape == (1, 4, 2) and iw.shape == (1, 4, 5)
+    # value 0: nonzero in chunks 0 and 2, negative in chunk 2
+    assert vw[0, 0].tolist() == [0b101, 0b100]
+    # value 1: nonzero only in chunk 2, negative there
+    assert vw[0, 1].tolist() == [0b100, 0b100]
+    # value 2: chunk 0 negative, chunk 2 positive
+    assert vw[0, 2].tolist() == [0b101, 0b001]
+    # index 3 of the chunks is 31, 4, 8: bit planes b0..b4
+    assert iw[0, 3].tolist() == [0b001, 0b001, 0b011, 0b101, 0b001]
+
+
+def test_ternary_round_trip_and_sizes():
+    r = rng(20)
+    for nc in (1, 31, 32, 33, 70):
+        vals = r.integers(-1, 2, size=(nc, 8)).astype(float)
+        idx = np.sort(np.stack([r.choice(32, 8, replace=False) for _ in range(nc)]), axis=1)
+        vw, iw = ref.ternary_pack(vals, idx)
+        v2, i2 = ref.ternary_unpack(vw, iw, nc)
+        assert np.array_equal(v2, vals) and np.array_equal(i2, idx)
+    n = 32 * 32 * 100  # 100 full tiles
+    for k in (1, 2, 4, 8):
+        vb, ib = ref.payload_bytes_wire(ref.MODE_DEMO, n, k, wire=ref.WIRE_TERNARY)
+        assert (vb + ib) * 8 == (n // 32) * k * 7  # 2 bits per value + 5 per index
+        vb, ib = ref.payload_bytes_wire(ref.MODE_RANDOM, n, k, wire=ref.WIRE_TERNARY)
+        assert vb * 8 == (n // 32) * k * 2 and ib == 0
+        assert ref.payload_bytes_wire(ref.MODE_DEMO, n, k, wire=ref.WIRE_F32) == ref.payload_bytes(ref.MODE_DEMO, n, k)
+        assert ref.payload_bytes_wire(ref.MODE_DEMO, n, k, wire=ref.WIRE_BF16) == ((n // 32) * k * 2, (n // 32) * k)
+
+
+def test_16bit_rounding_matches_torch():
+    import torch
+
+    x = np.concatenate([rng(21).standard_normal(20000) * s for s in (1e-3, 1.0, 1e3)]).astype(np.float32)
+    x = np.concatenate([x, np.float32([1.00390625, 1.005859375, -0.0, 0.0, 65504.0])]).astype(np.float64)
+    tb = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    th = torch.tensor(x, dtype=torch.float32).to(torch.float16).to(torch.float64).numpy()
+    assert np.array_equal(ref.round_bf16(x), tb)
+    assert np.array_equal(ref.round_f16(x), th)
+
+
+def test_ternary_wire_step_equals_signed_f32_step():
+    r = rng(22)
+    n = 40 * C
+    th, ms, gs = r.standard_normal(n), [r.standard_normal(n)] * 2, [r.standard_normal(n), r.standard_normal(n)]
+    for mode, k in ((ref.MODE_DEMO, 4), (ref.MODE_RANDOM, 8), (ref.MODE_DILOCO, 1)):
+        a, _, _ = ref.step(th, ms, gs, beta=0.9, lr=0.1, k=k, mode=mode, sign=True, step_idx=7)
+        b, _, _ = ref.step(th, ms, gs, beta=0.9, lr=0.1, k=k, mode=mode, sign=True, step_idx=7, wire=ref.WIRE_TERNARY)
+        assert np.array_equal(a, b)
+    with pytest.raises(ValueError):
+        ref.step(th, ms, gs, beta=0.9, lr=0.1, k=4, mode=ref.MODE_DEMO, sign=False, wire=ref.WIRE_TERNARY)

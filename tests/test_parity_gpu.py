@@ -36,7 +36,7 @@ def cuda_normal(n, std, seed, dtype=torch.float32):
 
 
 def run_steps(n, R, k, mode, sign, steps, *, beta=0.999, lr=1e-3, g_std=1e-2, seed=0, period=8, bf16=False,
-              rows=None, zero_chunks=(), stats=None):
+              rows=None, zero_chunks=(), stats=None, wire="f32"):
     theta = cuda_normal(n, 2e-2, 12345)
     ms = [torch.zeros(n, device="cuda") for _ in range(R)]
     for c in zero_chunks:
@@ -47,7 +47,7 @@ def run_steps(n, R, k, mode, sign, steps, *, beta=0.999, lr=1e-3, g_std=1e-2, se
             for g in gs:
                 g[c * C:(c + 1) * C] = 0
         theta, ms = check_step(theta, ms, gs, k=k, beta=beta, lr=lr, mode=mode, sign=sign, seed=seed, step=t,
-                               period=period, rows=rows, stats=stats)
+                               period=period, rows=rows, stats=stats, wire=wire)
     return theta, ms
 
 
