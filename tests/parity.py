@@ -60,6 +60,7 @@ def chunk_close(gpu, orc, tol, excl=None, scale=None):
 
 
 WIRE_REL = {"f32": 0.0, "ternary": 0.0, "bf16": 2.0 ** -8, "f16": 2.0 ** -11}  # one unit of the format's mantissa
+WIRE_ABS = {"f32": 0.0, "ternary": 0.0, "bf16": 0.0, "f16": 2.0 ** -24}  # fp16 subnormal spacing below 2^-14
 
 
 def gpu_split(theta, ms, gs, *, k, beta, lr, mode, sign, seed, step, period, wire="f32"):
@@ -143,7 +144,7 @@ def check_step(theta, ms, gs, *, k, beta, lr, mode, sign, seed=0, step=0, period
     th1, m1, info = ref.step(th0, m0, g0, beta=beta, lr=lr, k=k, mode=ref.__dict__["MODE_" + mode.upper()],
                              sign=sign, seed=seed, step_idx=step, period=period, chunk_ids=rows,
                              wire=dm.WIRES[wire])
-    wrel = WIRE_REL[wire]
+    wrel, wabs = WIRE_REL[wire], WIRE_ABS[wire]
     excl = info["near_tie"].copy()
     nrows = len(rows)
 
@@ -164,7 +165,7 @@ def check_step(theta, ms, gs, *, k, beta, lr, mode, sign, seed=0, step=0, period
                 assert (okv | excl).all(), "signed DeMo payload values differ"
             else:
                 scale = np.abs(X).max(1, keepdims=True)
-                errv = np.abs(gv - ov) <= wrel * np.abs(ov) + tol * np.where(scale == 0, 1, scale)
+                errv = np.abs(gv - ov) <= wrel * np.abs(ov) + wabs + tol * np.where(scale == 0, 1, scale)
                 assert (errv.all(1) | excl).all(), "DeMo payload values differ"
         elif mode in ("random", "stride"):
             pos = enc["pos"]
@@ -174,14 +175,14 @@ def check_step(theta, ms, gs, *, k, beta, lr, mode, sign, seed=0, step=0, period
             if sign:
                 assert np.array_equal(gv, ov), "signed payload values differ"
             else:
-                err = np.abs(gv - ov) <= wrel * np.abs(ov) + tol * np.abs(ov).max(1, keepdims=True)
+                err = np.abs(gv - ov) <= wrel * np.abs(ov) + wabs + tol * np.abs(ov).max(1, keepdims=True)
                 assert err.all(), "payload values differ"
         elif mode == "diloco" and enc["vals"] is not None:
             if sign:
                 assert np.array_equal(gv, enc["vals"]), "signed DiLoCo payload differs"
             else:
                 ov = enc["vals"]
-                err = np.abs(gv - ov) <= wrel * np.abs(ov) + tol * np.abs(ov).max(1, keepdims=True)
+                err = np.abs(gv - ov) <= wrel * np.abs(ov) + wabs + tol * np.abs(ov).max(1, keepdims=True)
                 assert err.all(), "DiLoCo payload differs"
         x = ref.f32(beta) * m0[r] + g0[r]  # the momentum before the subtraction of q
         bad, worst = chunk_close(mg, m1[r], tol, excl, scale=x)
@@ -203,6 +204,8 @@ def check_step(theta, ms, gs, *, k, beta, lr, mode, sign, seed=0, step=0, period
     # end to end: the mean of R replicas can cancel, so the error scale is the mean of |values|
     Yabs, _ = ref.scatter_mean([None if e["vals"] is None else np.abs(e["vals"]) for e in info["encodes"]],
                                [e["pos"] for e in info["encodes"]], nrows)
+    if wabs and not sign:  # the fp16 floor is absolute: compare it against the summand scale
+        Yabs = np.maximum(Yabs, wabs / max(tol + wrel, 1e-30))
     bad, worst = chunk_close(Qg, info["Q"], tol + (0.0 if sign else wrel), excl, scale=Yabs)
     assert not bad.any(), f"Q differs in {bad.sum()} chunks (worst {worst:.3g})"
 
