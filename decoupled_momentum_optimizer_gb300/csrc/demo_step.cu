@@ -141,12 +141,22 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
 #pragma unroll
         for (int u = 0; u < 32; ++u) stash[u * 32 + lane] = Xs[u];
         uint32_t mm = M;
-        for (int j = 0; j < p.k; ++j) {  // payload in ascending u
-          const int u = __ffs(mm) - 1;
-          mm &= mm - 1;
-          float v = stash[u * 32 + lane];
-          if (p.sign) v = sign3(v);
-          ws.acc[u * 32 + lane] += wire_round(v, p.wire);
+        if (p.wire >= kWireBF16) {
+          for (int j = 0; j < p.k; ++j) {  // payload in ascending u, rounded as the wire format rounds it
+            const int u = __ffs(mm) - 1;
+            mm &= mm - 1;
+            float v = stash[u * 32 + lane];
+            if (p.sign) v = sign3(v);
+            ws.acc[u * 32 + lane] += wire_round(v, p.wire);
+          }
+        } else {
+          for (int j = 0; j < p.k; ++j) {  // payload in ascending u
+            const int u = __ffs(mm) - 1;
+            mm &= mm - 1;
+            float v = stash[u * 32 + lane];
+            if (p.sign) v = sign3(v);
+            ws.acc[u * 32 + lane] += v;
+          }
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) cnt8[i] += (((M >> (4 * i)) & 0xfu) * 0x204081u) & 0x01010101u;
