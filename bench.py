@@ -356,6 +356,29 @@ def time_split(dm, case, mode, k, sign, seed, steps, warmup, stream, diloco_peri
     return a.elapsed_time(b) / steps
 
 
+def time_adamw(dm, case, steps, warmup, stream):
+    """Mean time (ms) of one Decoupled AdamW step (demo_adamw_step) over the case's replicas."""
+    import torch
+
+    vs = [torch.zeros_like(m) for m in case.ms]
+
+    def one(t):
+        dm.adamw_step(case.theta, case.ring[t % len(case.ring)], case.ms, vs, lr=1e-3, weight_decay=0.01, step=t,
+                      stream=stream)
+
+    for t in range(warmup):
+        one(t)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(steps):
+        one(warmup + i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
 def split_bytes(n, R, grad_bytes, mode, k, sync=True, wire="f32"):
     """Algorithmic bytes of the split path: R encodes (g, m, payload out) + decode (R payloads in, theta)."""
     import decoupled_momentum_optimizer_gb300 as dm
@@ -545,6 +568,9 @@ def sweep_cases():
     out.append(("t5_base", "demo", 4, True, 2, ("split:ternary", "split:bf16")))
     out.append(("t5_base", "random", 8, True, 2, ("split:ternary",)))
     out.append(("t5_base", "demo", 4, False, 2, ("split:bf16", "split:f16")))
+    # Decoupled AdamW (moments local, directions averaged densely)
+    for name in ("t5_base", "olmo2_1b_half", f"flat{1 << 28}"):
+        out.append((name, "adamw", 0, False, 2, ("adamw",)))
     for e in (20, 22, 24, 26, 28, 30):
         for k in (1, 2, 4, 8):
             out.append((f"flat{1 << e}", "demo", k, True, 2, ("fused",) if e != 26 else ("fused", "split")))
@@ -584,6 +610,16 @@ def run_sweep(args):
         period = 8
         step0 = 7 if sync else 0
         rec = {"workload": name, "n": n, "mode": mode, "k": k, "sign": sign, "R": R, "grad_dtype": case.wl.g_dtype}
+        if mode == "adamw":
+            am = time_adamw(dm, case, args.steps, args.warmup, stream)
+            ab = n * (R * (case.grad_bytes + 16) + 8)
+            r2 = dict(rec, fused_ms=am, fused_params_per_s=n / (am * 1e-3), fused_bytes=ab,
+                      fused_gbs=ab / (am * 1e-3) / 1e9, fused_frac=ab / (am * 1e-3) / 1e9 / peak)
+            f.write(json.dumps(r2) + "\n")
+            f.flush()
+            print(f"{name:16s} {'adamw':16s} R={R:2d}  step {am:8.3f} ms {r2['fused_gbs']:7.0f} GB/s "
+                  f"{100 * r2['fused_frac']:5.1f}%", flush=True)
+            continue
         wires = [x.split(":")[1] for x in paths if x.startswith("split:")]
         if wires:
             # wire-format runs of the split path only

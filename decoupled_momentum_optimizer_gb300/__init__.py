@@ -45,6 +45,9 @@ _SIGS = {
                                       ctypes.c_int, _c_u64, _c_u64, ctypes.c_int, _c_vp]),
     "demo_validate_payload": (ctypes.c_int, [_c_i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_vp,
                                              ctypes.POINTER(_c_i64)]),
+    "demo_adamw_step": (ctypes.c_int, [_c_vp, _c_i64, ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                       ctypes.c_float, ctypes.c_int, _c_vp, ctypes.c_int, _c_vp, _c_vp, _c_u64,
+                                       _c_vp]),
     "demo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "demo_device_fault": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint)]),
 }
@@ -221,6 +224,23 @@ def step(theta, gs, ms, *, k, beta, lr, mode="demo", sign=True, diloco_period=8,
     marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n) for r, m in enumerate(ms)])
     _check(lib().demo_step_wire(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr, gd, marr,
                                 diloco_period, seed, step, _wire(wire), _stream(stream)), "demo_step")
+
+
+def adamw_step(theta, gs, ms, vs, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, step=0, stream=None):
+    """One Decoupled AdamW step (demo_adamw_step): theta, every m_r and v_r update in place."""
+    import torch
+
+    init(theta.device.index)
+    n = theta.numel()
+    R = len(ms)
+    if len(gs) != R or len(vs) != R:
+        raise ValueError("need one gradient, first and second moment per replica")
+    tp = _ptr(theta, (torch.float32,), "theta", n)
+    garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n) for r, g in enumerate(gs)])
+    marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n) for r, m in enumerate(ms)])
+    varr = (ctypes.c_void_p * R)(*[_ptr(v, (torch.float32,), f"v[{r}]", n) for r, v in enumerate(vs)])
+    _check(lib().demo_adamw_step(tp, n, beta1, beta2, eps, lr, weight_decay, R, garr, _grad_dtype(gs[0]), marr, varr,
+                                 step, _stream(stream)), "demo_adamw_step")
 
 
 def validate_payload(idx_host, n, k, wire="f32"):

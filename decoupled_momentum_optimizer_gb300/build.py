@@ -1,7 +1,7 @@
 """Build libdemo_gb300.so in-tree for sm_103a (GB300) with nvcc.
 
 Usage: ``python -m decoupled_momentum_optimizer_gb300.build`` (or ``build()``).
-The four translation units compile in parallel, then link into one shared
+The translation units compile in parallel, then link into one shared
 library next to this file.  The DCT factor header is regenerated from its
 generator first, so the constants always come from gen_dct_factors.py.
 """
@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB_NAME = "libdemo_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = ["demo_api.cu", "demo_step.cu", "demo_encode.cu", "demo_decode.cu"]
+SOURCES = ["demo_api.cu", "demo_step.cu", "demo_encode.cu", "demo_decode.cu", "demo_adamw.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -1,0 +1,77 @@
+// Decoupled AdamW shard step: each replica keeps its own first and second
+// moments (never synchronised); the replicas' AdamW directions are averaged
+// densely (full synchronisation) and applied with decoupled weight decay.
+//
+// "DeToNATION: Decoupled Torch Network-Aware Training on Interlinked Online
+// Nodes" (Paper-Notes, AAAI 2026), method section, "4. Decoupled AdamW"; the
+// ViT-B bandwidth table runs it with full synchronisation.  AdamW itself is
+// Loshchilov & Hutter's (bias-corrected moments, decoupled weight decay).
+//
+// The step is elementwise, so it is a plain grid-stride loop over groups of
+// four parameters: per group every replica's g, m, v are read with one
+// 16-byte load each (8 bytes for bf16 g), m and v are written back, and theta
+// is read and written once.  All accesses are fully coalesced.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "demo_params.h"
+
+namespace demo {
+
+constexpr int kAdamThreads = 256;
+
+__device__ __forceinline__ float4 load_grad4(const void* g, long long i, bool bf16) {
+  if (!bf16) return reinterpret_cast<const float4*>(g)[i];
+  const uint2 w = reinterpret_cast<const uint2*>(g)[i];
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u), __uint_as_float(w.y << 16),
+                     __uint_as_float(w.y & 0xffff0000u));
+}
+
+struct AdamLane {
+  float b1, b2, omb1, omb2, rbc1, rbc2, eps;
+
+  // One replica's moments for one parameter; returns its AdamW direction.
+  __device__ __forceinline__ float update(float g, float& m, float& v) const {
+    m = __fmaf_rn(b1, m, omb1 * g);
+    v = __fmaf_rn(b2, v, omb2 * (g * g));
+    return (m * rbc1) / (sqrtf(v * rbc2) + eps);
+  }
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(kAdamThreads) adamw_kernel(const __grid_constant__ AdamWParams p) {
+  const AdamLane a{p.beta1, p.beta2, p.omb1, p.omb2, p.rbc1, p.rbc2, p.eps};
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.n4; i += stride) {
+    float4 U = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int r = 0; r < p.R; ++r) {
+      const float4 g = load_grad4(p.g[r], i, BF16);
+      float4 m = reinterpret_cast<const float4*>(p.m[r])[i];
+      float4 v = reinterpret_cast<const float4*>(p.v[r])[i];
+      U.x += a.update(g.x, m.x, v.x);
+      U.y += a.update(g.y, m.y, v.y);
+      U.z += a.update(g.z, m.z, v.z);
+      U.w += a.update(g.w, m.w, v.w);
+      reinterpret_cast<float4*>(p.m[r])[i] = m;
+      reinterpret_cast<float4*>(p.v[r])[i] = v;
+    }
+    float4 th = reinterpret_cast<const float4*>(p.theta)[i];
+    th.x = __fmaf_rn(-p.lr, __fmaf_rn(p.wd, th.x, U.x * p.rcpR), th.x);
+    th.y = __fmaf_rn(-p.lr, __fmaf_rn(p.wd, th.y, U.y * p.rcpR), th.y);
+    th.z = __fmaf_rn(-p.lr, __fmaf_rn(p.wd, th.z, U.z * p.rcpR), th.z);
+    th.w = __fmaf_rn(-p.lr, __fmaf_rn(p.wd, th.w, U.w * p.rcpR), th.w);
+    reinterpret_cast<float4*>(p.theta)[i] = th;
+  }
+}
+
+cudaError_t launch_adamw(const AdamWParams& p, bool bf16, int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kAdamThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  return bf16 ? cudaLaunchKernelEx(&cfg, adamw_kernel<true>, p) : cudaLaunchKernelEx(&cfg, adamw_kernel<false>, p);
+}
+
+}  // namespace demo

@@ -435,6 +435,63 @@ int demo_validate_payload(int64_t n, int chunk, int k, int wire, const void* idx
   return DEMO_OK;
 }
 
+int demo_adamw_step(float* theta, int64_t n, float beta1, float beta2, float eps, float lr, float weight_decay,
+                    int R, const void* const* g, int grad_dtype, float* const* m, float* const* v, uint64_t step,
+                    void* stream) {
+  if (n <= 0 || n % DEMO_CHUNK != 0 || n > kMaxN) return DEMO_EINVAL;
+  if (R < 1 || R > DEMO_MAX_REPLICAS) return DEMO_EINVAL;
+  if (grad_dtype != DEMO_GRAD_F32 && grad_dtype != DEMO_GRAD_BF16) return DEMO_EINVAL;
+  if (!std::isfinite(beta1) || !std::isfinite(beta2) || !std::isfinite(eps) || !std::isfinite(lr) ||
+      !std::isfinite(weight_decay))
+    return DEMO_EINVAL;
+  if (beta1 < 0.0f || beta1 >= 1.0f || beta2 < 0.0f || beta2 >= 1.0f || !(eps > 0.0f)) return DEMO_EINVAL;
+  if (theta == nullptr || g == nullptr || m == nullptr || v == nullptr) return DEMO_EINVAL;
+  for (int r = 0; r < R; ++r)
+    if (g[r] == nullptr || m[r] == nullptr || v[r] == nullptr) return DEMO_EINVAL;
+  if (!aligned16(theta)) return DEMO_EALIGN;
+  for (int r = 0; r < R; ++r)
+    if (!aligned16(g[r]) || !aligned16(m[r]) || !aligned16(v[r])) return DEMO_EALIGN;
+  // written buffers (theta, every m_r and v_r) must not overlap anything else
+  const size_t fb = static_cast<size_t>(n) * 4;
+  const size_t gb = static_cast<size_t>(n) * (grad_dtype == DEMO_GRAD_BF16 ? 2 : 4);
+  for (int r = 0; r < R; ++r) {
+    if (overlap(theta, fb, g[r], gb) || overlap(theta, fb, m[r], fb) || overlap(theta, fb, v[r], fb))
+      return DEMO_EINVAL;
+    for (int q = 0; q < R; ++q) {
+      if (overlap(m[r], fb, g[q], gb) || overlap(v[r], fb, g[q], gb) || overlap(m[r], fb, v[q], fb))
+        return DEMO_EINVAL;
+      if (q != r && (overlap(m[r], fb, m[q], fb) || overlap(v[r], fb, v[q], fb))) return DEMO_EINVAL;
+    }
+  }
+  DeviceState* st = nullptr;
+  const int s = current_state(&st);
+  if (s != DEMO_OK) return s;
+  AdamWParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.theta = theta;
+  for (int r = 0; r < R; ++r) {
+    p.g[r] = g[r];
+    p.m[r] = m[r];
+    p.v[r] = v[r];
+  }
+  p.n4 = n / 4;
+  p.R = R;
+  p.beta1 = beta1;
+  p.beta2 = beta2;
+  p.omb1 = static_cast<float>(1.0 - static_cast<double>(beta1));
+  p.omb2 = static_cast<float>(1.0 - static_cast<double>(beta2));
+  const double t = static_cast<double>(step) + 1.0;
+  p.rbc1 = static_cast<float>(1.0 / (1.0 - std::pow(static_cast<double>(beta1), t)));
+  p.rbc2 = static_cast<float>(1.0 / (1.0 - std::pow(static_cast<double>(beta2), t)));
+  p.eps = eps;
+  p.lr = lr;
+  p.wd = weight_decay;
+  p.rcpR = 1.0f / static_cast<float>(R);
+  const int64_t want = (p.n4 + 255) / 256;
+  const int grid = static_cast<int>(want < 8LL * st->sms ? want : 8LL * st->sms);
+  return to_status(launch_adamw(p, grad_dtype == DEMO_GRAD_BF16, grid, static_cast<cudaStream_t>(stream)));
+}
+
 int demo_device_fault(unsigned int* code) {
   if (code == nullptr) return DEMO_EINVAL;
   DeviceState* st = nullptr;

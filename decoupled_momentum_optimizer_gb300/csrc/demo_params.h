@@ -61,6 +61,21 @@ struct DecodeParams {
   unsigned int* fault;
 };
 
+// Decoupled AdamW (elementwise, grid-stride over groups of four parameters).
+struct AdamWParams {
+  float* theta;
+  const void* g[kMaxReplicas];
+  float* m[kMaxReplicas];
+  float* v[kMaxReplicas];
+  long long n4;  // n / 4
+  int R;
+  float beta1, beta2, omb1, omb2;  // beta and 1 - beta (exact in float32)
+  float rbc1, rbc2;                // 1 / (1 - beta^t), t = step + 1
+  float eps, lr, wd, rcpR;
+};
+
+cudaError_t launch_adamw(const AdamWParams& p, bool bf16, int grid, cudaStream_t st);
+
 // Launchers (one per translation unit).  `grid` CTAs of kStepWarps warps; each
 // warp walks the tiles gw, gw + kStepWarps * grid, ...
 constexpr int kStepWarps = 11;

@@ -202,6 +202,22 @@ int demo_step_wire(float* theta, int64_t n, int chunk, int k, float beta, float 
  */
 int demo_validate_payload(int64_t n, int chunk, int k, int wire, const void* idx_host, int64_t* first_bad);
 
+/*
+ * demo_adamw_step -- one Decoupled AdamW step over R replicas ("DeToNATION"
+ * notes, method section, "4. Decoupled AdamW": the first and second moments
+ * stay local to each replica; the ViT-B bandwidth table runs it with full
+ * synchronisation).  With t = step + 1 and every replica r:
+ *   m_r <- beta1 m_r + (1 - beta1) g_r,   v_r <- beta2 v_r + (1 - beta2) g_r^2
+ *   u_r  = (m_r / (1 - beta1^t)) / (sqrt(v_r / (1 - beta2^t)) + eps)
+ * then U = mean_r u_r (the dense sync) and theta <- theta - lr (U + weight_decay theta)
+ * (Loshchilov & Hutter's AdamW).  theta, m[r], v[r]: device float32 [n], updated
+ * in place; g[r]: device [n] of grad_dtype.  0 <= beta < 1, eps > 0, all finite;
+ * n a positive multiple of 32; 1 <= R <= 64.  Same error conventions as above.
+ */
+int demo_adamw_step(float* theta, int64_t n, float beta1, float beta2, float eps, float lr, float weight_decay,
+                    int R, const void* const* g, int grad_dtype, float* const* m, float* const* v, uint64_t step,
+                    void* stream);
+
 /* demo_status_string -- a static, human-readable name for a status code. */
 const char* demo_status_string(int status);
 

@@ -473,3 +473,37 @@ def payload_bytes_wire(mode, n, k, step=0, period=8, wire=WIRE_F32):
         vb = nc * kv * (4 if wire == WIRE_F32 else 2)
         ib = nc * k if mode == MODE_DEMO else 0
     return vb, ib
+
+
+# ----------------------------------------------------------------------------
+# Decoupled AdamW (moments local to each replica, update directions synced)
+# ----------------------------------------------------------------------------
+#
+# DeToNATION notes, method section, "4. Decoupled AdamW": an AdamW variant whose
+# first and second moments (the EMA of the gradient and of its square) are not
+# synchronised; the ViT-B bandwidth table runs it with full synchronisation.
+# Reading taken: every replica updates its own moments and forms its AdamW
+# direction u_r = m_hat_r / (sqrt(v_hat_r) + eps) (Loshchilov & Hutter's AdamW,
+# bias-corrected with the 1-based step t); the replicas' directions are averaged
+# densely (full sync) and theta <- theta - lr (mean_r u_r + wd theta).
+
+def adamw_step(theta, ms, vs, gs, *, beta1, beta2, eps, lr, wd, step_idx):
+    """One Decoupled-AdamW step over R replicas; step_idx is 0-based (t = step_idx + 1).
+
+    Returns (theta_new, [m_r], [v_r], U) with U the mean direction.
+    """
+    b1, b2, e, lr32, wd32 = f32(beta1), f32(beta2), f32(eps), f32(lr), f32(wd)
+    t = step_idx + 1
+    bc1 = 1.0 - b1 ** t
+    bc2 = 1.0 - b2 ** t
+    theta = np.asarray(theta, dtype=np.float64)
+    new_m, new_v, us = [], [], []
+    for m, v, g in zip(ms, vs, gs):
+        g = np.asarray(g, dtype=np.float64)
+        m = b1 * np.asarray(m, dtype=np.float64) + (1.0 - b1) * g
+        v = b2 * np.asarray(v, dtype=np.float64) + (1.0 - b2) * g * g
+        us.append((m / bc1) / (np.sqrt(v / bc2) + e))
+        new_m.append(m)
+        new_v.append(v)
+    U = sum(us) / len(us)
+    return theta - lr32 * (U + wd32 * theta), new_m, new_v, U

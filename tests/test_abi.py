@@ -178,3 +178,18 @@ def test_init_without_device(L):
     assert L.demo_init(0) == ENODEV
     code = ctypes.c_uint(0)
     assert L.demo_device_fault(ctypes.byref(code)) == ENOTINIT
+
+
+def test_adamw_argument_checks(L):
+    g = (ctypes.c_void_p * 1)(0x100000)
+    m = (ctypes.c_void_p * 1)(0x200000)
+    v = (ctypes.c_void_p * 1)(0x300000)
+    th = p(0x400000)
+    assert L.demo_adamw_step(th, 64, 0.9, 0.999, 1e-8, 1e-3, 0.0, 1, g, 0, m, v, 0, None) in (ENOTINIT, ENODEV)
+    assert L.demo_adamw_step(th, 48, 0.9, 0.999, 1e-8, 1e-3, 0.0, 1, g, 0, m, v, 0, None) == EINVAL
+    assert L.demo_adamw_step(th, 64, 1.0, 0.999, 1e-8, 1e-3, 0.0, 1, g, 0, m, v, 0, None) == EINVAL
+    assert L.demo_adamw_step(th, 64, 0.9, 0.999, 0.0, 1e-3, 0.0, 1, g, 0, m, v, 0, None) == EINVAL
+    assert L.demo_adamw_step(th, 64, 0.9, 0.999, 1e-8, 1e-3, 0.0, 0, g, 0, m, v, 0, None) == EINVAL
+    assert L.demo_adamw_step(p(0x400004), 64, 0.9, 0.999, 1e-8, 1e-3, 0.0, 1, g, 0, m, v, 0, None) == EALIGN
+    same = (ctypes.c_void_p * 1)(0x200000)
+    assert L.demo_adamw_step(th, 64, 0.9, 0.999, 1e-8, 1e-3, 0.0, 1, g, 0, m, same, 0, None) == EINVAL

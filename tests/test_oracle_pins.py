@@ -463,3 +463,46 @@ def test_ternary_wire_step_equals_signed_f32_step():
         assert np.array_equal(a, b)
     with pytest.raises(ValueError):
         ref.step(th, ms, gs, beta=0.9, lr=0.1, k=4, mode=ref.MODE_DEMO, sign=False, wire=ref.WIRE_TERNARY)
+
+
+# ----------------------------------------------------------------------------
+# Decoupled AdamW
+# ----------------------------------------------------------------------------
+
+def test_adamw_single_replica_matches_torch():
+    import torch
+
+    r = rng(30)
+    n = 5 * C
+    theta0 = r.standard_normal(n)
+    gs = [r.standard_normal(n) * 1e-2 for _ in range(4)]
+    kw = dict(beta1=0.9, beta2=0.999, eps=1e-8, lr=1e-3, wd=0.1)
+    p = torch.nn.Parameter(torch.tensor(theta0, dtype=torch.float64))
+    opt = torch.optim.AdamW([p], lr=ref.f32(1e-3), betas=(ref.f32(0.9), ref.f32(0.999)), eps=ref.f32(1e-8),
+                            weight_decay=ref.f32(0.1))
+    th, m, v = theta0, [np.zeros(n)], [np.zeros(n)]
+    for t, g in enumerate(gs):
+        p.grad = torch.tensor(g, dtype=torch.float64)
+        opt.step()
+        th, m, v, _ = ref.adamw_step(th, m, v, [g], step_idx=t, **kw)
+        assert np.abs(th - p.detach().numpy()).max() < 1e-14
+
+
+def test_adamw_first_step_closed_form_and_replica_mean():
+    r = rng(31)
+    n = 3 * C
+    theta0 = r.standard_normal(n)
+    g = r.standard_normal(n)
+    # t = 1: m_hat = g, v_hat = g^2, so u = g / (|g| + eps)
+    th, _, _, U = ref.adamw_step(theta0, [np.zeros(n)], [np.zeros(n)], [g], beta1=0.9, beta2=0.99, eps=1e-3,
+                                 lr=0.5, wd=0.0, step_idx=0)
+    e = float(np.float32(1e-3))
+    assert np.abs(U - g / (np.abs(g) + e)).max() < 1e-14
+    assert np.abs(th - (theta0 - 0.5 * U)).max() < 1e-14
+    # R identical replicas average to the single-replica direction; two opposite ones cancel
+    _, _, _, U3 = ref.adamw_step(theta0, [np.zeros(n)] * 3, [np.zeros(n)] * 3, [g] * 3, beta1=0.9, beta2=0.99,
+                                 eps=1e-3, lr=0.5, wd=0.0, step_idx=0)
+    assert np.abs(U3 - U).max() < 1e-15
+    _, _, _, U2 = ref.adamw_step(theta0, [np.zeros(n)] * 2, [np.zeros(n)] * 2, [g, -g], beta1=0.9, beta2=0.99,
+                                 eps=1e-3, lr=0.5, wd=0.0, step_idx=0)
+    assert np.abs(U2).max() == 0.0
