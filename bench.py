@@ -379,6 +379,34 @@ def time_adamw(dm, case, steps, warmup, stream):
     return a.elapsed_time(b) / steps
 
 
+def time_pipelined(dm, case, mode, k, sign, steps, warmup, stream, wire="f32", blocks=8):
+    """Mean time (ms) of demo_step_pipelined (split path, exchange overlapped on a second stream)."""
+    import torch
+
+    wl, n, R = case.wl, case.n, case.R
+    dev = case.theta.device
+    send = [dm.payload_buffers(mode, n, k, wire=wire, device=dev) for _ in range(R)]
+    recv = [dm.payload_buffers(mode, n, k, wire=wire, device=dev) for _ in range(R)]
+    comm = torch.cuda.Stream(device=dev)
+
+    def one(t):
+        dm.step_pipelined(case.theta, case.ring[t % len(case.ring)], case.ms, send, recv, k=k, beta=wl.beta,
+                          lr=wl.lr, mode=mode, sign=sign, step=t, wire=wire, blocks=blocks, stream=stream,
+                          comm_stream=comm)
+
+    for t in range(warmup):
+        one(t)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(steps):
+        one(warmup + i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
 def split_bytes(n, R, grad_bytes, mode, k, sync=True, wire="f32"):
     """Algorithmic bytes of the split path: R encodes (g, m, payload out) + decode (R payloads in, theta)."""
     import decoupled_momentum_optimizer_gb300 as dm
@@ -568,6 +596,8 @@ def sweep_cases():
     out.append(("t5_base", "demo", 4, True, 2, ("split:ternary", "split:bf16")))
     out.append(("t5_base", "random", 8, True, 2, ("split:ternary",)))
     out.append(("t5_base", "demo", 4, False, 2, ("split:bf16", "split:f16")))
+    # split path with the exchange (payload copies) overlapped on a second stream
+    out.append(("t5_base", "demo", 4, True, 2, ("pipe:f32:4", "pipe:f32:16", "pipe:ternary:16")))
     # Decoupled AdamW (moments local, directions averaged densely)
     for name in ("t5_base", "olmo2_1b_half", f"flat{1 << 28}"):
         out.append((name, "adamw", 0, False, 2, ("adamw",)))
@@ -619,6 +649,20 @@ def run_sweep(args):
             f.flush()
             print(f"{name:16s} {'adamw':16s} R={R:2d}  step {am:8.3f} ms {r2['fused_gbs']:7.0f} GB/s "
                   f"{100 * r2['fused_frac']:5.1f}%", flush=True)
+            continue
+        pipes = [x.split(":")[1:] for x in paths if x.startswith("pipe:")]
+        if pipes:
+            for wire, blocks in pipes:
+                pm = time_pipelined(dm, case, real_mode, k, sign, steps, warmup, stream, wire=wire, blocks=int(blocks))
+                # bytes: the split path's plus the exchange copies (read + write of every payload)
+                pb = split_bytes(n, R, case.grad_bytes, real_mode, k, wire=wire) + 2 * R * sum(
+                    dm.payload_bytes(real_mode, n, k, wire=wire))
+                r2 = dict(rec, mode=f"{mode}/{wire}/pipelined{blocks}", split_ms=pm, split_params_per_s=n / (pm * 1e-3),
+                          split_bytes=pb, split_gbs=pb / (pm * 1e-3) / 1e9, split_frac=pb / (pm * 1e-3) / 1e9 / peak)
+                f.write(json.dumps(r2) + "\n")
+                f.flush()
+                print(f"{name:16s} {mode + '/' + wire + '/pipe' + blocks:22s} R={R:2d}  {pm:8.3f} ms "
+                      f"{r2['split_gbs']:7.0f} GB/s", flush=True)
             continue
         wires = [x.split(":")[1] for x in paths if x.startswith("split:")]
         if wires:

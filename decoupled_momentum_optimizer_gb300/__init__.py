@@ -48,6 +48,10 @@ _SIGS = {
     "demo_adamw_step": (ctypes.c_int, [_c_vp, _c_i64, ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                        ctypes.c_float, ctypes.c_int, _c_vp, ctypes.c_int, _c_vp, _c_vp, _c_u64,
                                        _c_vp]),
+    "demo_step_pipelined": (ctypes.c_int, [_c_vp, _c_i64, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                           ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_vp,
+                                           ctypes.c_int, _c_vp, ctypes.c_int, _c_u64, _c_u64, ctypes.c_int, _c_vp,
+                                           _c_vp, _c_vp, _c_vp, ctypes.c_int, _c_vp, _c_vp]),
     "demo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "demo_device_fault": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint)]),
 }
@@ -224,6 +228,36 @@ def step(theta, gs, ms, *, k, beta, lr, mode="demo", sign=True, diloco_period=8,
     marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n) for r, m in enumerate(ms)])
     _check(lib().demo_step_wire(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr, gd, marr,
                                 diloco_period, seed, step, _wire(wire), _stream(stream)), "demo_step")
+
+
+def step_pipelined(theta, gs, ms, send, recv, *, k, beta, lr, mode="demo", sign=True, diloco_period=8, seed=0,
+                   step=0, wire="f32", blocks=8, stream=None, comm_stream=None):
+    """demo_step_pipelined: the split path with the payload exchange (send -> recv copies) overlapped.
+
+    ``send`` and ``recv`` are lists of R (vals, idx) pairs as made by payload_buffers.
+    """
+    import torch
+
+    init(theta.device.index)
+    n = theta.numel()
+    R = len(ms)
+    w = _wire(wire)
+    tp = _ptr(theta, (torch.float32,), "theta", n)
+    garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n) for r, g in enumerate(gs)])
+    marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n) for r, m in enumerate(ms)])
+
+    def arr(pairs, j, dts):
+        if pairs is None or pairs[0][j] is None:
+            return None
+        return (ctypes.c_void_p * R)(*[_ptr(pq[j], dts, "payload") for pq in pairs])
+
+    sv, si = arr(send, 0, _val_dtypes(w)), arr(send, 1, _idx_dtypes(w))
+    rv, ri = arr(recv, 0, _val_dtypes(w)), arr(recv, 1, _idx_dtypes(w))
+    cs = _stream(stream)
+    xs = _stream(comm_stream) if comm_stream is not None else cs
+    _check(lib().demo_step_pipelined(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr,
+                                     _grad_dtype(gs[0]), marr, diloco_period, seed, step, w, sv, si, rv, ri, blocks,
+                                     cs, xs), "demo_step_pipelined")
 
 
 def adamw_step(theta, gs, ms, vs, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, step=0, stream=None):

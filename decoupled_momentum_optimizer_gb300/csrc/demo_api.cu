@@ -1,5 +1,6 @@
 // C ABI of the DeMo shard step: argument checks, TMA tensor maps, launches.
 // The operations and their sources are described in include/demo.h.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -19,10 +20,14 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxN = int64_t(1) << 35;  // keeps every row coordinate within int32
 
+constexpr int kMaxBlocks = 64;  // blocks of the pipelined step
+
 struct DeviceState {
   bool ready = false;
   int sms = 0;
   unsigned int* fault = nullptr;
+  cudaEvent_t ev_enc[kMaxBlocks];  // block b encoded (compute stream)
+  cudaEvent_t ev_xch[kMaxBlocks];  // block b exchanged (communication stream)
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -160,7 +165,7 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
 template <int MAXR>
 int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mode, int R,
                const void* const* vals, const void* const* idx, uint64_t seed, uint64_t step, int wire,
-               cudaStream_t stream) {
+               cudaStream_t stream, int64_t chunk0 = 0) {
   DecodeParams<MAXR> p;
   std::memset(&p, 0, sizeof(p));
   const int64_t nc = n / DEMO_CHUNK;
@@ -172,6 +177,7 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
   }
   p.nc = nc;
   p.ntiles = (nc + 31) / 32;
+  p.chunk0 = chunk0;
   p.R = R;
   p.k = (mode == DEMO_MODE_DILOCO) ? DEMO_CHUNK : k;
   fill_selection(p, mode, p.k, seed, step);
@@ -188,6 +194,56 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
     e = launch_decode_large(p, mode, grid, stream);
   }
   return to_status(e);
+}
+
+// One replica's encode over n elements whose first chunk is chunk0 of the shard (arguments checked).
+int run_encode(DeviceState* st, const void* g, int grad_dtype, float* m, int64_t n, int k, float beta, int mode,
+               int sign, bool sends, uint64_t seed, uint64_t step, int wire, void* vals, void* idx, int64_t chunk0,
+               cudaStream_t stream) {
+  EncodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int64_t nc = n / DEMO_CHUNK;
+  const bool bf16 = grad_dtype == DEMO_GRAD_BF16;
+  if (!make_map(&p.g, g, nc, bf16) || !make_map(&p.m, m, nc, false)) return DEMO_ECUDA;
+  p.m_ptr = m;
+  p.vals = vals;
+  p.idx = idx;
+  p.nc = nc;
+  p.ntiles = (nc + 31) / 32;
+  p.chunk0 = chunk0;
+  p.k = (mode == DEMO_MODE_DILOCO) ? DEMO_CHUNK : k;
+  p.sign = sign;
+  p.sync = (mode == DEMO_MODE_DILOCO) ? (sends ? 1 : 0) : 1;
+  p.wire = wire;
+  fill_selection(p, mode, p.k, seed, step);
+  p.stride_mask = (mode == DEMO_MODE_STRIDE) ? stride_mask(p.stride_o, p.stride_ns, k) : 0u;
+  p.beta = beta;
+  p.fault = st->fault;
+  return to_status(launch_encode(p, mode, bf16, grid_for(p.ntiles, st), stream));
+}
+
+// Byte offset of the payload of the block starting at chunk c0 (tile t0 = c0 / 32) in a wire-format buffer.
+struct PayloadLayout {
+  size_t val_per_chunk = 0, idx_per_chunk = 0;  // float32 / 16-bit formats
+  size_t val_per_tile = 0, idx_per_tile = 0;    // ternary format
+  size_t vals_at(int64_t c0) const { return val_per_tile ? (c0 / 32) * val_per_tile : c0 * val_per_chunk; }
+  size_t idx_at(int64_t c0) const { return idx_per_tile ? (c0 / 32) * idx_per_tile : c0 * idx_per_chunk; }
+  // end of the payload of chunks before c1 (a partial last tile counts whole)
+  size_t vals_end(int64_t c1) const { return val_per_tile ? ((c1 + 31) / 32) * val_per_tile : c1 * val_per_chunk; }
+  size_t idx_end(int64_t c1) const { return idx_per_tile ? ((c1 + 31) / 32) * idx_per_tile : c1 * idx_per_chunk; }
+};
+
+PayloadLayout payload_layout(int mode, int k, int wire) {
+  PayloadLayout L;
+  const size_t kv = mode == DEMO_MODE_DILOCO ? DEMO_CHUNK : static_cast<size_t>(k);
+  if (wire == DEMO_WIRE_TERNARY) {
+    L.val_per_tile = kv * 8;
+    L.idx_per_tile = mode == DEMO_MODE_DEMO ? static_cast<size_t>(k) * 20 : 0;
+  } else {
+    L.val_per_chunk = kv * (wire == DEMO_WIRE_F32 ? 4 : 2);
+    L.idx_per_chunk = mode == DEMO_MODE_DEMO ? static_cast<size_t>(k) : 0;
+  }
+  return L;
 }
 
 }  // namespace
@@ -241,6 +297,11 @@ int demo_init(int device) {
   if (cudaGetSymbolAddress(&fault, g_fault_word) != cudaSuccess) return DEMO_ECUDA;
   if (cudaMemset(fault, 0, sizeof(unsigned int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
     return DEMO_ECUDA;
+  for (int b = 0; b < kMaxBlocks; ++b) {
+    if (cudaEventCreateWithFlags(&st.ev_enc[b], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&st.ev_xch[b], cudaEventDisableTiming) != cudaSuccess)
+      return DEMO_ECUDA;
+  }
   st.sms = sms;
   st.fault = static_cast<unsigned int*>(fault);
   st.ready = true;
@@ -294,26 +355,8 @@ int demo_encode_wire(const void* g, int grad_dtype, float* m, int64_t n, int chu
   DeviceState* st = nullptr;
   s = current_state(&st);
   if (s != DEMO_OK) return s;
-
-  EncodeParams p;
-  std::memset(&p, 0, sizeof(p));
-  const int64_t nc = n / DEMO_CHUNK;
-  const bool bf16 = grad_dtype == DEMO_GRAD_BF16;
-  if (!make_map(&p.g, g, nc, bf16) || !make_map(&p.m, m, nc, false)) return DEMO_ECUDA;
-  p.m_ptr = m;
-  p.vals = vals;
-  p.idx = idx;
-  p.nc = nc;
-  p.ntiles = (nc + 31) / 32;
-  p.k = (mode == DEMO_MODE_DILOCO) ? DEMO_CHUNK : k;
-  p.sign = sign;
-  p.sync = (mode == DEMO_MODE_DILOCO) ? (sends ? 1 : 0) : 1;
-  p.wire = wire;
-  fill_selection(p, mode, p.k, seed, step);
-  p.stride_mask = (mode == DEMO_MODE_STRIDE) ? stride_mask(p.stride_o, p.stride_ns, k) : 0u;
-  p.beta = beta;
-  p.fault = st->fault;
-  return to_status(launch_encode(p, mode, bf16, grid_for(p.ntiles, st), static_cast<cudaStream_t>(stream)));
+  return run_encode(st, g, grad_dtype, m, n, k, beta, mode, sign, sends, seed, step, wire, vals, idx, 0,
+                    static_cast<cudaStream_t>(stream));
 }
 
 int demo_encode(const void* g, int grad_dtype, float* m, int64_t n, int chunk, int k, float beta, int mode,
@@ -405,6 +448,113 @@ int demo_step(float* theta, int64_t n, int chunk, int k, float beta, float lr, i
               uint64_t step, void* stream) {
   return demo_step_wire(theta, n, chunk, k, beta, lr, mode, sign, R, g, grad_dtype, m, diloco_period, seed, step,
                         DEMO_WIRE_F32, stream);
+}
+
+int demo_step_pipelined(float* theta, int64_t n, int chunk, int k, float beta, float lr, int mode, int sign, int R,
+                        const void* const* g, int grad_dtype, float* const* m, int diloco_period, uint64_t seed,
+                        uint64_t step, int wire, void* const* send_vals, void* const* send_idx,
+                        void* const* recv_vals, void* const* recv_idx, int blocks, void* compute_stream,
+                        void* comm_stream) {
+  int s = check_shape(n, chunk, k, mode, diloco_period);
+  if (s != DEMO_OK) return s;
+  if (R < 1 || R > DEMO_MAX_REPLICAS || blocks < 1 || blocks > kMaxBlocks) return DEMO_EINVAL;
+  if (grad_dtype != DEMO_GRAD_F32 && grad_dtype != DEMO_GRAD_BF16) return DEMO_EINVAL;
+  if (sign != 0 && sign != 1) return DEMO_EINVAL;
+  if (!valid_wire(wire) || (wire == DEMO_WIRE_TERNARY && !sign)) return DEMO_EINVAL;
+  if (!std::isfinite(beta) || !std::isfinite(lr)) return DEMO_EINVAL;
+  if (theta == nullptr || g == nullptr || m == nullptr) return DEMO_EINVAL;
+  const bool sends = mode != DEMO_MODE_DILOCO || diloco_sync(step, diloco_period);
+  const bool demo = mode == DEMO_MODE_DEMO;
+  if (sends && (send_vals == nullptr || recv_vals == nullptr)) return DEMO_EINVAL;
+  if (sends && demo && (send_idx == nullptr || recv_idx == nullptr)) return DEMO_EINVAL;
+  for (int r = 0; r < R; ++r) {
+    if (g[r] == nullptr || m[r] == nullptr) return DEMO_EINVAL;
+    if (sends && (send_vals[r] == nullptr || recv_vals[r] == nullptr)) return DEMO_EINVAL;
+    if (sends && demo && (send_idx[r] == nullptr || recv_idx[r] == nullptr)) return DEMO_EINVAL;
+  }
+  if (!aligned16(theta)) return DEMO_EALIGN;
+  for (int r = 0; r < R; ++r) {
+    if (!aligned16(g[r]) || !aligned16(m[r])) return DEMO_EALIGN;
+    if (sends && (!aligned16(send_vals[r]) || !aligned16(recv_vals[r]))) return DEMO_EALIGN;
+    if (sends && demo && (!aligned16(send_idx[r]) || !aligned16(recv_idx[r]))) return DEMO_EALIGN;
+  }
+  const size_t fb = static_cast<size_t>(n) * 4;
+  const size_t gb = static_cast<size_t>(n) * (grad_dtype == DEMO_GRAD_BF16 ? 2 : 4);
+  for (int r = 0; r < R; ++r) {
+    if (overlap(m[r], fb, theta, fb)) return DEMO_EINVAL;
+    for (int q = 0; q < R; ++q) {
+      if (q != r && overlap(m[r], fb, m[q], fb)) return DEMO_EINVAL;
+      if (overlap(m[r], fb, g[q], gb)) return DEMO_EINVAL;
+    }
+    if (overlap(theta, fb, g[r], gb)) return DEMO_EINVAL;
+  }
+  DeviceState* st = nullptr;
+  s = current_state(&st);
+  if (s != DEMO_OK) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
+  cudaStream_t xs = static_cast<cudaStream_t>(comm_stream);
+
+  // blocks of whole 32-chunk tiles, so every wire format's payload splits at block boundaries
+  const int64_t nc = n / DEMO_CHUNK;
+  const int64_t T = (nc + 31) / 32;
+  const int64_t tpb = (T + blocks - 1) / blocks;
+  const int B = static_cast<int>((T + tpb - 1) / tpb);
+  const PayloadLayout L = payload_layout(mode, k, wire);
+  auto chunk_lo = [&](int b) { return std::min<int64_t>(static_cast<int64_t>(b) * tpb * 32, nc); };
+  auto chunk_hi = [&](int b) { return std::min<int64_t>(static_cast<int64_t>(b + 1) * tpb * 32, nc); };
+  auto at = [](const void* p, size_t off) { return static_cast<char*>(const_cast<void*>(p)) + off; };
+
+  auto decode_block = [&](int b) -> int {
+    const int64_t c0 = chunk_lo(b), c1 = chunk_hi(b);
+    const void* v[DEMO_MAX_REPLICAS];
+    const void* ix[DEMO_MAX_REPLICAS];
+    for (int r = 0; r < R; ++r) {
+      v[r] = at(recv_vals[r], L.vals_at(c0));
+      ix[r] = demo ? at(recv_idx[r], L.idx_at(c0)) : nullptr;
+    }
+    float* th = theta + c0 * DEMO_CHUNK;
+    const int64_t nb = (c1 - c0) * DEMO_CHUNK;
+    return R <= kSmallReplicas
+               ? run_decode<kSmallReplicas>(st, th, nb, k, lr, mode, R, v, ix, seed, step, wire, cs, c0)
+               : run_decode<kMaxReplicas>(st, th, nb, k, lr, mode, R, v, ix, seed, step, wire, cs, c0);
+  };
+
+  for (int b = 0; b < B; ++b) {
+    const int64_t c0 = chunk_lo(b), c1 = chunk_hi(b);
+    const int64_t nb = (c1 - c0) * DEMO_CHUNK;
+    for (int r = 0; r < R; ++r) {
+      const void* gb_ptr = at(g[r], static_cast<size_t>(c0) * DEMO_CHUNK * (grad_dtype == DEMO_GRAD_BF16 ? 2 : 4));
+      s = run_encode(st, gb_ptr, grad_dtype, m[r] + c0 * DEMO_CHUNK, nb, k, beta, mode, sign, sends, seed, step, wire,
+                     sends ? at(send_vals[r], L.vals_at(c0)) : nullptr,
+                     sends && demo ? at(send_idx[r], L.idx_at(c0)) : nullptr, c0, cs);
+      if (s != DEMO_OK) return s;
+    }
+    if (!sends) continue;
+    // the exchange of block b: a loopback copy of every replica's payload block on the communication stream
+    if (cudaEventRecord(st->ev_enc[b], cs) != cudaSuccess || cudaStreamWaitEvent(xs, st->ev_enc[b], 0) != cudaSuccess)
+      return DEMO_ECUDA;
+    for (int r = 0; r < R; ++r) {
+      if (cudaMemcpyAsync(at(recv_vals[r], L.vals_at(c0)), at(send_vals[r], L.vals_at(c0)),
+                          L.vals_end(c1) - L.vals_at(c0), cudaMemcpyDeviceToDevice, xs) != cudaSuccess)
+        return DEMO_ECUDA;
+      if (demo && cudaMemcpyAsync(at(recv_idx[r], L.idx_at(c0)), at(send_idx[r], L.idx_at(c0)),
+                                  L.idx_end(c1) - L.idx_at(c0), cudaMemcpyDeviceToDevice, xs) != cudaSuccess)
+        return DEMO_ECUDA;
+    }
+    if (cudaEventRecord(st->ev_xch[b], xs) != cudaSuccess) return DEMO_ECUDA;
+    // decode the previous block while this block's exchange is in flight
+    if (b >= 1) {
+      if (cudaStreamWaitEvent(cs, st->ev_xch[b - 1], 0) != cudaSuccess) return DEMO_ECUDA;
+      s = decode_block(b - 1);
+      if (s != DEMO_OK) return s;
+    }
+  }
+  if (sends) {
+    if (cudaStreamWaitEvent(cs, st->ev_xch[B - 1], 0) != cudaSuccess) return DEMO_ECUDA;
+    s = decode_block(B - 1);
+    if (s != DEMO_OK) return s;
+  }
+  return DEMO_OK;
 }
 
 int demo_validate_payload(int64_t n, int chunk, int k, int wire, const void* idx_host, int64_t* first_bad) {

@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
         if (valid) qs[pos * 32 + lane] = sum * p.rcpR;
       };
       if constexpr (MODE == kModeRandom) {
-        random_draws(p.hbase, static_cast<uint64_t>(c), p.k, take);
+        random_draws(p.hbase, static_cast<uint64_t>(c + p.chunk0), p.k, take);
       } else {
         for (int j = 0; j < p.k; ++j) take(j, stride_position(p.stride_o, p.stride_ns, j));
       }

@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
       };
       uint32_t P;
       if constexpr (MODE == kModeRandom) {
-        P = random_draws(p.hbase, static_cast<uint64_t>(c), p.k, emit);
+        P = random_draws(p.hbase, static_cast<uint64_t>(c + p.chunk0), p.k, emit);
       } else {
         for (int j = 0; j < p.k; ++j) emit(j, stride_position(p.stride_o, p.stride_ns, j));
         P = p.stride_mask;

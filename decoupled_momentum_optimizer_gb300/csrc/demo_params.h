@@ -38,6 +38,7 @@ struct EncodeParams {
   void* vals;  // wire-format payload values
   void* idx;   // DeMo indices (uint8 [nc][k], or uint32 bit-planes for the ternary format)
   long long nc, ntiles;
+  long long chunk0;  // shard index of the first chunk (the Random scheme hashes shard chunk indices)
   int k, sign, sync, wire;
   int stride_o, stride_ns;
   unsigned int stride_mask;
@@ -53,6 +54,7 @@ struct DecodeParams {
   const void* vals[MAXR];
   const void* idx[MAXR];
   long long nc, ntiles;
+  long long chunk0;  // shard index of the first chunk
   int R, k, wire;
   int stride_o, stride_ns;
   float lr, rcpR;

@@ -193,6 +193,27 @@ int demo_step_wire(float* theta, int64_t n, int chunk, int k, float beta, float 
                    uint64_t seed, uint64_t step, int wire, void* stream);
 
 /*
+ * demo_step_pipelined -- the split path with its exchange overlapped: the shard
+ * is cut into `blocks` blocks of whole 32-chunk tiles (1 <= blocks <= 64); for
+ * each block every replica's encode runs on `compute_stream` into send_vals /
+ * send_idx, the block's payloads are copied (the loopback of the replication
+ * group's all_gather / all-reduce) to recv_vals / recv_idx on `comm_stream`,
+ * and the block is decoded from the receive buffers on `compute_stream` while
+ * the next block's exchange is in flight (an overlap the DeToNATION notes list
+ * as not yet exploited, "limitations": CUDA-stream overlap of communication and
+ * computation).  Send and receive buffers are laid out as demo_encode_wire
+ * writes a whole shard; results are bit-identical to demo_step_wire.  The
+ * Random scheme hashes shard chunk indices, so blocks draw the same positions
+ * as a single call.  The call only enqueues work; on return the compute stream
+ * holds the whole step.  Events are taken from a pool created by demo_init.
+ */
+int demo_step_pipelined(float* theta, int64_t n, int chunk, int k, float beta, float lr, int mode, int sign, int R,
+                        const void* const* g, int grad_dtype, float* const* m, int diloco_period, uint64_t seed,
+                        uint64_t step, int wire, void* const* send_vals, void* const* send_idx,
+                        void* const* recv_vals, void* const* recv_idx, int blocks, void* compute_stream,
+                        void* comm_stream);
+
+/*
  * demo_validate_payload -- host-side check of one replica's DeMo indices
  * (host memory, wire layout as above): every chunk must list k distinct indices
  * in [0, 32) in ascending order.  Returns DEMO_OK, or DEMO_EINVAL with

@@ -1,0 +1,69 @@
+"""The split path with its exchange overlapped on a second stream
+(demo_step_pipelined) is bit-identical to the fused step for every scheme,
+wire format and block count."""
+
+import pytest
+import torch
+
+import decoupled_momentum_optimizer_gb300 as dm
+
+pytestmark = pytest.mark.gpu
+
+RAGGED = 32 * (31 * 32 + 8)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _init():
+    dm.init(0)
+    yield
+    assert dm.device_fault() == 0
+
+
+def cuda_normal(n, std, seed):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    return torch.randn(n, generator=g, device="cuda") * std
+
+
+CASES = [
+    ("demo", 4, True, 2, "f32", 1), ("demo", 4, True, 2, "f32", 3), ("demo", 4, True, 2, "ternary", 8),
+    ("demo", 1, False, 3, "bf16", 5), ("demo", 8, False, 2, "f16", 64),
+    ("random", 8, True, 2, "f32", 4), ("random", 1, True, 3, "ternary", 7), ("stride", 4, False, 2, "bf16", 2),
+    ("diloco", 1, True, 2, "ternary", 3), ("diloco", 1, False, 2, "f32", 4),
+]
+
+
+@pytest.mark.parametrize("mode,k,sign,R,wire,blocks", CASES, ids=lambda v: str(v))
+def test_pipelined_equals_fused(mode, k, sign, R, wire, blocks):
+    n = RAGGED
+    comm = torch.cuda.Stream()
+    theta0 = cuda_normal(n, 2e-2, 1)
+    m0 = [cuda_normal(n, 1e-2, 10 + r) for r in range(R)]
+    for step in (0, 1, 7):  # DiLoCo (period 8) syncs on step 7 only
+        gs = [cuda_normal(n, 1e-3, 20 + 3 * r + step) for r in range(R)]
+        th_f, ms_f = theta0.clone(), [m.clone() for m in m0]
+        dm.step(th_f, gs, ms_f, k=k, beta=0.99, lr=1e-2, mode=mode, sign=sign, seed=3, step=step, wire=wire)
+        th_p, ms_p = theta0.clone(), [m.clone() for m in m0]
+        send = [dm.payload_buffers(mode, n, k, step=step, wire=wire) for _ in range(R)]
+        recv = [dm.payload_buffers(mode, n, k, step=step, wire=wire) for _ in range(R)]
+        dm.step_pipelined(th_p, gs, ms_p, send if send[0][0] is not None else None,
+                          recv if recv[0][0] is not None else None, k=k, beta=0.99, lr=1e-2, mode=mode, sign=sign,
+                          seed=3, step=step, wire=wire, blocks=blocks, comm_stream=comm)
+        torch.cuda.synchronize()
+        assert torch.equal(th_f, th_p)
+        for a, b in zip(ms_f, ms_p):
+            assert torch.equal(a, b)
+
+
+def test_pipelined_argument_errors():
+    n = 32 * 64
+    th = torch.zeros(n, device="cuda")
+    g = torch.zeros(n, device="cuda")
+    m = torch.zeros(n, device="cuda")
+    send = [dm.payload_buffers("demo", n, 4)]
+    with pytest.raises(dm.DemoError):
+        dm.step_pipelined(th, [g], [m], send, send, k=4, beta=0.9, lr=0.1, blocks=0)
+    with pytest.raises(dm.DemoError):
+        dm.step_pipelined(th, [g], [m], send, send, k=4, beta=0.9, lr=0.1, blocks=65)
+    with pytest.raises(dm.DemoError):
+        dm.step_pipelined(th, [g], [m], None, None, k=4, beta=0.9, lr=0.1, blocks=2)
