@@ -56,10 +56,13 @@ def test_adamw_teacher_forced(R, bf16, n):
             assert not chunk_close(f64(vs[r]), v1[r], TOL)[0].any()
         # the direction: element-wise relative (no cancellation inside one replica's u)
         assert np.abs(f64(U) - Uo).max() <= TOL * np.abs(Uo).max()
-        # theta' = theta - lr (U + wd theta), one float32 rounding of each fma
-        want = (th0 - ref.f32(KW["lr"]) * (f64(U) + ref.f32(KW["weight_decay"]) * th0)).astype(np.float32)
-        got = f64(theta).astype(np.float32)
-        assert (np.abs(got.astype(np.float64) - want) <= 2 * np.spacing(np.abs(want))).all()
+        # theta' = theta - lr (U + wd theta) as two fused multiply-adds: the inner one rounds
+        # U + wd theta (error <= 2^-24 of it, scaled by lr), the outer one rounds theta'
+        inner = f64(U) + ref.f32(KW["weight_decay"]) * th0
+        want = th0 - ref.f32(KW["lr"]) * inner
+        got = f64(theta)
+        bound = np.spacing(np.abs(want).astype(np.float32)) + 2.0 ** -23 * ref.f32(KW["lr"]) * np.abs(inner)
+        assert (np.abs(got - want) <= bound).all()
 
 
 def test_adamw_single_replica_matches_torch_on_gpu():
