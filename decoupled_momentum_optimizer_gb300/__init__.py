@@ -52,6 +52,10 @@ _SIGS = {
                                            ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_vp,
                                            ctypes.c_int, _c_vp, ctypes.c_int, _c_u64, _c_u64, ctypes.c_int, _c_vp,
                                            _c_vp, _c_vp, _c_vp, ctypes.c_int, _c_vp, _c_vp]),
+    "demo_step_pipelined_static": (ctypes.c_int, [_c_vp, _c_i64, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                                  ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_vp,
+                                                  ctypes.c_int, _c_vp, ctypes.c_int, _c_u64, _c_u64, ctypes.c_int,
+                                                  ctypes.c_int, _c_vp, _c_vp]),
     "demo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "demo_device_fault": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint)]),
 }
@@ -258,6 +262,29 @@ def step_pipelined(theta, gs, ms, send, recv, *, k, beta, lr, mode="demo", sign=
     _check(lib().demo_step_pipelined(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr,
                                      _grad_dtype(gs[0]), marr, diloco_period, seed, step, w, sv, si, rv, ri, blocks,
                                      cs, xs), "demo_step_pipelined")
+
+
+def step_pipelined_static(theta, gs, ms, *, k, beta, lr, mode="demo", sign=True, diloco_period=8, seed=0, step=0,
+                          wire="f32", blocks=8, stream=None, comm_stream=None):
+    """demo_step_pipelined_static: the pipelined step with its payload buffers inside the library.
+
+    For callers that cannot allocate device memory when they step; the payloads
+    of all replicas must fit the library's fixed 32 MiB send / 32 MiB receive
+    scratch (DemoError with DEMO_ENOSPACE otherwise).
+    """
+    import torch
+
+    init(theta.device.index)
+    n = theta.numel()
+    R = len(ms)
+    tp = _ptr(theta, (torch.float32,), "theta", n)
+    garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n) for r, g in enumerate(gs)])
+    marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n) for r, m in enumerate(ms)])
+    cs = _stream(stream)
+    xs = _stream(comm_stream) if comm_stream is not None else cs
+    _check(lib().demo_step_pipelined_static(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr,
+                                            _grad_dtype(gs[0]), marr, diloco_period, seed, step, _wire(wire), blocks,
+                                            cs, xs), "demo_step_pipelined_static")
 
 
 def adamw_step(theta, gs, ms, vs, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, step=0, stream=None):

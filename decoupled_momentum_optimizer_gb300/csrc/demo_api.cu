@@ -258,6 +258,7 @@ const char* demo_status_string(int status) {
     case DEMO_ENODEV: return "DEMO_ENODEV: no sm_103 device";
     case DEMO_ECUDA: return "DEMO_ECUDA: CUDA call or launch failed";
     case DEMO_ENOTINIT: return "DEMO_ENOTINIT: demo_init was not called for the current device";
+    case DEMO_ENOSPACE: return "DEMO_ENOSPACE: the payloads need more than the library's fixed scratch";
     default: return "DEMO_UNKNOWN";
   }
 }
@@ -555,6 +556,71 @@ int demo_step_pipelined(float* theta, int64_t n, int chunk, int k, float beta, f
     if (s != DEMO_OK) return s;
   }
   return DEMO_OK;
+}
+
+}  // extern "C"
+
+// ----------------------------------------------------------------------------
+// Fixed scratch for demo_step_pipelined_static (callers that cannot allocate)
+// ----------------------------------------------------------------------------
+
+namespace {
+
+constexpr size_t kStaticHalfBytes = size_t(32) << 20;  // send half and receive half, 32 MiB each
+static __device__ __align__(256) unsigned char g_static_scratch[2 * kStaticHalfBytes];
+void* g_static_scratch_addr[kMaxDevices] = {};
+
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" {
+
+int demo_step_pipelined_static(float* theta, int64_t n, int chunk, int k, float beta, float lr, int mode, int sign,
+                               int R, const void* const* g, int grad_dtype, float* const* m, int diloco_period,
+                               uint64_t seed, uint64_t step, int wire, int blocks, void* compute_stream,
+                               void* comm_stream) {
+  if (R < 1 || R > DEMO_MAX_REPLICAS) return DEMO_EINVAL;
+  size_t ib = 0;
+  const size_t vb = demo_payload_bytes_wire(mode, n, chunk, k, step, diloco_period, wire, &ib);
+  const size_t per_replica = round256(vb) + round256(ib);
+  if (per_replica * static_cast<size_t>(R) > kStaticHalfBytes) return DEMO_ENOSPACE;
+
+  // Device address of the array on the current device, looked up once per device.
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return DEMO_ENOTINIT;
+  }
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_static_scratch_addr[dev] == nullptr) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_static_scratch) != cudaSuccess || addr == nullptr) return DEMO_ECUDA;
+      g_static_scratch_addr[dev] = addr;
+    }
+    base = g_static_scratch_addr[dev];
+  }
+
+  void* send_vals[DEMO_MAX_REPLICAS];
+  void* send_idx[DEMO_MAX_REPLICAS];
+  void* recv_vals[DEMO_MAX_REPLICAS];
+  void* recv_idx[DEMO_MAX_REPLICAS];
+  char* send = static_cast<char*>(base);
+  char* recv = send + kStaticHalfBytes;
+  for (int r = 0; r < R; ++r) {
+    const size_t off = static_cast<size_t>(r) * per_replica;
+    send_vals[r] = send + off;
+    recv_vals[r] = recv + off;
+    send_idx[r] = ib ? send + off + round256(vb) : nullptr;
+    recv_idx[r] = ib ? recv + off + round256(vb) : nullptr;
+  }
+  const bool payload = vb > 0;
+  return demo_step_pipelined(theta, n, chunk, k, beta, lr, mode, sign, R, g, grad_dtype, m, diloco_period, seed, step,
+                             wire, payload ? send_vals : nullptr, ib ? send_idx : nullptr,
+                             payload ? recv_vals : nullptr, ib ? recv_idx : nullptr, blocks, compute_stream,
+                             comm_stream);
 }
 
 int demo_validate_payload(int64_t n, int chunk, int k, int wire, const void* idx_host, int64_t* first_bad) {

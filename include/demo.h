@@ -107,7 +107,8 @@ enum demo_status {
   DEMO_EALIGN = -2,   /* a device pointer is not 16-byte aligned */
   DEMO_ENODEV = -3,   /* no device, or the device is not an sm_103 GPU */
   DEMO_ECUDA = -4,    /* a CUDA runtime call or a launch failed */
-  DEMO_ENOTINIT = -5  /* demo_init() was not called for the current device */
+  DEMO_ENOTINIT = -5, /* demo_init() was not called for the current device */
+  DEMO_ENOSPACE = -6  /* the request needs more than the library's fixed scratch */
 };
 
 /*
@@ -212,6 +213,35 @@ int demo_step_pipelined(float* theta, int64_t n, int chunk, int k, float beta, f
                         uint64_t step, int wire, void* const* send_vals, void* const* send_idx,
                         void* const* recv_vals, void* const* recv_idx, int blocks, void* compute_stream,
                         void* comm_stream);
+
+/*
+ * demo_step_pipelined_static -- demo_step_pipelined without caller-provided
+ * payload buffers and without any allocation.  The pages have no counterpart:
+ * this exists for callers that cannot allocate device memory when they step --
+ * for example a framework whose caching allocator already holds the device's
+ * memory, or a runtime that forbids allocation after start-up -- and so cannot
+ * provide the send / receive buffers demo_step_pipelined needs.
+ *
+ * The payload send and receive buffers live in one fixed array of 64 MiB of
+ * device memory inside the library (32 MiB for the R replicas' send payloads,
+ * 32 MiB for the receive payloads, each replica's buffers rounded up to 256
+ * bytes; demo_payload_bytes_wire gives the sizes).  Every GPU that loads the
+ * library holds that array until the process exits.  A request that does not
+ * fit returns DEMO_ENOSPACE and launches nothing.  The call allocates nothing:
+ * no cudaMalloc, no cudaFree, no library routine that allocates.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every call
+ * shares the one array and leaves the last step's payloads in it: each step's
+ * encode overwrites every payload word its decode reads, so nothing has to start
+ * at zero, but calls whose work overlaps on the GPU (on different streams, or
+ * different threads) race on the array.  Arguments and results are those of
+ * demo_step_pipelined, which this call runs with buffers inside the array.
+ */
+int demo_step_pipelined_static(float* theta, int64_t n, int chunk, int k, float beta, float lr, int mode,
+                               int sign, int R, const void* const* g, int grad_dtype, float* const* m,
+                               int diloco_period, uint64_t seed, uint64_t step, int wire, int blocks,
+                               void* compute_stream, void* comm_stream);
 
 /*
  * demo_validate_payload -- host-side check of one replica's DeMo indices
