@@ -11,10 +11,9 @@
 // replica's encode in registers and writes m_r back; the last item streams
 // theta, turns the accumulated payloads into Q and writes theta back.  Results
 // leave through the item's own slot: each lane writes its row into the
-// swizzled g tile, the warp reads it back transposed and issues 512-byte
-// coalesced stores.  The slot refills in two parts: item i + 2's m (or theta)
-// tile as soon as item i's inputs are in registers, its g tile once the store
-// has read gbuf back.  Shared memory per warp is 20 KB (two 8 KB slots and a 4 KB
+// swizzled tile, the warp reads it back transposed and issues 512-byte
+// coalesced stores, and the slot is immediately refilled with the load for
+// item i + 2.  Shared memory per warp is 20 KB (two 8 KB slots and a 4 KB
 // payload accumulator), so 11 warps fit on an SM.  With a 16-bit wire format
 // the accumulated values are rounded exactly as the split path's receiver
 // rounds them, so fused and split results stay bit-identical.
@@ -24,8 +23,8 @@
 namespace demo {
 
 struct alignas(1024) StepWarpSmem {
-  float gbuf[2][1024];  // slot s: g_r tile (f32 or bf16), then the stash and the rows on their way out
-  float mbuf[2][1024];  // slot s: m_r tile or the theta tile
+  float gbuf[2][1024];  // slot s: g_r tile (f32 or bf16), later the stash of kept coefficients; or theta
+  float mbuf[2][1024];  // slot s: m_r tile, later the new m_r on its way out
   float acc[32 * 32];   // DeMo: per-lane payload sums [u][lane]
 };
 
@@ -65,11 +64,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   }
   __syncwarp();
 
-  // Each item's tiles arrive in two parts on the slot's mbarrier (one expect_tx for
-  // both): the m tile (or the theta tile) goes into mbuf and is issued as soon as
-  // the slot's previous item has been read; the g tile goes into gbuf, which the
-  // previous item still uses as its stash and store staging, and is issued last.
-  auto issue_early = [&](long long item) {
+  auto issue = [&](long long item) {
     if (item >= nitems) return;
     const int s = static_cast<int>(item & 1);
     const long long t = gw + (item / ipt) * TW;
@@ -77,24 +72,16 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     const int y = static_cast<int>(t * 32);
     if (kind < p.R) {
       mbar_expect_tx(&bars[s], (BF16 ? kTileBytesBF16 : kTileBytesF32) + kTileBytesF32);
+      tma_load_2d(ws.gbuf[s], &p.g[kind], &bars[s], 0, y);
       tma_load_2d(ws.mbuf[s], &p.m[kind], &bars[s], 0, y);
     } else {
       mbar_expect_tx(&bars[s], kTileBytesF32);
-      tma_load_2d(ws.mbuf[s], &p.theta, &bars[s], 0, y);
+      tma_load_2d(ws.gbuf[s], &p.theta, &bars[s], 0, y);
     }
   };
-  auto issue_late = [&](long long item) {
-    if (item >= nitems) return;
-    const int s = static_cast<int>(item & 1);
-    const long long t = gw + (item / ipt) * TW;
-    const int kind = static_cast<int>(item % ipt);
-    if (kind < p.R) tma_load_2d(ws.gbuf[s], &p.g[kind], &bars[s], 0, static_cast<int>(t * 32));
-  };
   if (lane == 0) {
-    issue_early(0);
-    issue_late(0);
-    issue_early(1);
-    issue_late(1);
+    issue(0);
+    issue(1);
   }
 
   uint32_t P = 0;       // Random / Striding / DiLoCo: positions sent from this lane's chunk
@@ -144,15 +131,12 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       load_row_f32(ws.mbuf[s], lane, x);
 #pragma unroll
       for (int i = 0; i < 32; ++i) x[i] = __fmaf_rn(p.beta, x[i], gv[i]);
-      // every lane has read its rows: mbuf takes the next load now, gbuf becomes scratch
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) issue_early(item + 2);
 
       if constexpr (MODE == kModeDemo) {
         float X[32], Xs[32];
         dct32_forward(x, X);
         const uint32_t M = topk_select(X, p.k, Xs);
+        __syncwarp();  // every lane has read its g row: the g tile becomes the stash
         float* stash = ws.gbuf[s];
 #pragma unroll
         for (int u = 0; u < 32; ++u) stash[u * 32 + lane] = Xs[u];
@@ -209,15 +193,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = ((P >> i) & 1u) ? 0.0f : x[i];
       }
-      __syncwarp();  // all stash reads are done before the rows overwrite gbuf
-      store_tile_coalesced(ws.gbuf[s], lane, x, p.m_ptr[kind], row0, p.nc);
+      store_tile_coalesced(ws.mbuf[s], lane, x, p.m_ptr[kind], row0, p.nc);
     } else {
       // ---- decode: Q from the accumulated payloads, theta <- theta - lr Q
       float th[32];
-      load_row_f32(ws.mbuf[s], lane, th);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) issue_early(item + 2);
+      load_row_f32(ws.gbuf[s], lane, th);
       float Q[32];
       if constexpr (MODE == kModeDemo) {
         float Y[32];
@@ -234,13 +214,14 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       }
 #pragma unroll
       for (int i = 0; i < 32; ++i) th[i] = __fmaf_rn(-p.lr, Q[i], th[i]);
+      __syncwarp();  // every lane has read its theta row
       store_tile_coalesced(ws.gbuf[s], lane, th, p.theta_ptr, row0, p.nc);
     }
 
-    // gbuf has been read back by the coalesced store: it takes item + 2's g tile.
+    // The slot has been read and written back: refill it with item + 2.
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) issue_late(item + 2);
+    if (lane == 0) issue(item + 2);
   }
 }
 
