@@ -154,14 +154,17 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+STEP_KERNEL_SOURCES = ("demo_step.cu", "demo_common.cuh", "demo_params.h", "dct32_factors.cuh")
+
+
 def src_hash():
+    """Hash of the fused step kernel's sources (the kernel the roofline and traffic describe)."""
     import hashlib
 
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decoupled_momentum_optimizer_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in STEP_KERNEL_SOURCES:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
