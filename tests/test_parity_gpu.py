@@ -299,17 +299,32 @@ def sample_rows(nc, extra=(), count=4096):
 
 @pytest.mark.parametrize("name", ["t5_base", "vit_b16", "olmo2_1b_half"])
 def test_model_shards_sampled(name):
+    """Every run of the workload for its configured number of steps (T5-base 20, the others 10)."""
     wl = W.workload(name)
     n, R = wl.n, wl.R
     rows = sample_rows(n // C, wl.layout.pad_chunks())
     theta0 = W.make_theta0(wl, "cuda")
+    stats = {}
     for mode, k, sign in wl.runs:
         theta = theta0.clone()
         ms = [torch.zeros(n, device="cuda") for _ in range(R)]
         streams = [W.GradStream(wl, r, "cuda") for r in range(R)]
-        for t in range(2):
+        for t in range(wl.steps):
             gs = [s.next() for s in streams]
             theta, ms = check_step(theta, ms, gs, k=k, beta=wl.beta, lr=wl.lr, mode=mode, sign=sign, step=t,
-                                   rows=rows)
+                                   rows=rows, stats=stats)
         del ms
         torch.cuda.empty_cache()
+    assert stats["near_tie"] <= stats["chunks"] // 100
+
+
+@pytest.mark.parametrize("n,R,mode,k", [(1 << 30, 2, "demo", 4), (1 << 28, 8, "random", 8)])
+def test_largest_shards_sampled(n, R, mode, k):
+    """The largest shards of the size sweep, one step, on sampled chunks."""
+    rows = sample_rows(n // C)
+    theta = cuda_normal(n, 2e-2, 5)
+    ms = [cuda_normal(n, 1e-3, 6 + r) for r in range(R)]
+    gs = [cuda_normal(n, 1e-3, 20 + r) for r in range(R)]
+    check_step(theta, ms, gs, k=k, beta=0.999, lr=1e-3, mode=mode, sign=True, step=3, rows=rows)
+    del theta, ms, gs
+    torch.cuda.empty_cache()
