@@ -160,11 +160,13 @@ __device__ __forceinline__ void store_tile_coalesced(float* buf, int lane, const
   __syncwarp();
   const char* b = reinterpret_cast<const char*>(buf);
   const int j = lane & 7;
+  float4* dst = reinterpret_cast<float4*>(gbase + row0 * 32) + (lane >> 3) * 8 + j;
+  const int live = nrows - row0 >= 32 ? 32 : static_cast<int>(nrows - row0);  // rows of the tile inside the array
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int r = q * 4 + (lane >> 3);
     const float4 val = *reinterpret_cast<const float4*>(b + r * 128 + ((j ^ (r & 7)) << 4));
-    if (row0 + r < nrows) reinterpret_cast<float4*>(gbase + (row0 + r) * 32)[j] = val;
+    if (r < live) dst[q * 32] = val;
   }
 }
 

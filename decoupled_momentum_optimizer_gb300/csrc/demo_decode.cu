@@ -105,9 +105,10 @@ __device__ __forceinline__ void load_payload(const void* vals, const void* idx, 
 
 template <int MODE, int MAXR>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_constant__ DecodeParams<MAXR> p) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* base =
-      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // 1024-byte aligned start (the TMA swizzle patterns are relative to 1024-byte boundaries),
+  // derived by pointer arithmetic on the shared array so every access stays a shared-memory one
+  unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   DecWarpSmem& ws = reinterpret_cast<DecWarpSmem*>(base)[warp];

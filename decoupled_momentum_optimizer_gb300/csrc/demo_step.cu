@@ -34,9 +34,10 @@ static_assert(kStepSmem <= 232448, "shared memory per CTA");
 
 template <int MODE, bool BF16, int MAXR>
 __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_constant__ StepParams<MAXR> p) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* base =
-      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // 1024-byte aligned start (the TMA swizzle patterns are relative to 1024-byte boundaries),
+  // derived by pointer arithmetic on the shared array so every access stays a shared-memory one
+  unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   StepWarpSmem& ws = reinterpret_cast<StepWarpSmem*>(base)[warp];
@@ -64,24 +65,31 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   }
   __syncwarp();
 
-  auto issue = [&](long long item) {
-    if (item >= nitems) return;
-    const int s = static_cast<int>(item & 1);
-    const long long t = gw + (item / ipt) * TW;
-    const int kind = static_cast<int>(item % ipt);
-    const int y = static_cast<int>(t * 32);
-    if (kind < p.R) {
-      mbar_expect_tx(&bars[s], (BF16 ? kTileBytesBF16 : kTileBytesF32) + kTileBytesF32);
-      tma_load_2d(ws.gbuf[s], &p.g[kind], &bars[s], 0, y);
-      tma_load_2d(ws.mbuf[s], &p.m[kind], &bars[s], 0, y);
+  // Items are loaded strictly in order, so the loads keep their own (tile, kind)
+  // cursor instead of dividing item numbers by the items per tile.
+  long long ld_t = gw;
+  int ld_kind = 0, ld_slot = 0;
+  auto issue = [&]() {
+    if (ld_t >= p.ntiles) return;
+    const int y = static_cast<int>(ld_t * 32);
+    uint64_t* bar = &bars[ld_slot];
+    if (ld_kind < p.R) {
+      mbar_expect_tx(bar, (BF16 ? kTileBytesBF16 : kTileBytesF32) + kTileBytesF32);
+      tma_load_2d(ws.gbuf[ld_slot], &p.g[ld_kind], bar, 0, y);
+      tma_load_2d(ws.mbuf[ld_slot], &p.m[ld_kind], bar, 0, y);
     } else {
-      mbar_expect_tx(&bars[s], kTileBytesF32);
-      tma_load_2d(ws.gbuf[s], &p.theta, &bars[s], 0, y);
+      mbar_expect_tx(bar, kTileBytesF32);
+      tma_load_2d(ws.gbuf[ld_slot], &p.theta, bar, 0, y);
+    }
+    ld_slot ^= 1;
+    if (++ld_kind == ipt) {
+      ld_kind = 0;
+      ld_t += TW;
     }
   };
   if (lane == 0) {
-    issue(0);
-    issue(1);
+    issue();
+    issue();
   }
 
   uint32_t P = 0;       // Random / Striding / DiLoCo: positions sent from this lane's chunk
@@ -92,11 +100,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
 #pragma unroll
   for (int i = 0; i < 8; ++i) cnt8[i] = 0u;
 
+  long long t = gw;
+  int kind = 0;
   for (long long item = 0; item < nitems; ++item) {
     const int s = static_cast<int>(item & 1);
     const uint32_t par = static_cast<uint32_t>((item >> 1) & 1);
-    const long long t = gw + (item / ipt) * TW;
-    const int kind = static_cast<int>(item % ipt);
     const long long row0 = t * 32;
     const long long c = row0 + lane;
 
@@ -221,7 +229,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     // The slot has been read and written back: refill it with item + 2.
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) issue(item + 2);
+    if (lane == 0) issue();
+    if (++kind == ipt) {
+      kind = 0;
+      t += TW;
+    }
   }
 }
 
