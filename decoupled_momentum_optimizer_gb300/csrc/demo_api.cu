@@ -152,12 +152,13 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
   fill_rcp(p);
   p.wire = wire;
   p.fault = st->fault;
-  const int grid = grid_for(p.ntiles, st);
+  const int warps = step_warps(mode, p.k, bf16, R, p.sync != 0);
+  const int grid = grid_for(p.ntiles, st, warps);
   cudaError_t e;
   if constexpr (MAXR == kSmallReplicas) {
-    e = launch_step_small(p, mode, bf16, grid, stream);
+    e = launch_step_small(p, mode, bf16, warps, grid, stream);
   } else {
-    e = launch_step_large(p, mode, bf16, grid, stream);
+    e = launch_step_large(p, mode, bf16, warps, grid, stream);
   }
   return to_status(e);
 }

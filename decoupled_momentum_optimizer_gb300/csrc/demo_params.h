@@ -78,11 +78,23 @@ struct AdamWParams {
 
 cudaError_t launch_adamw(const AdamWParams& p, bool bf16, int grid, cudaStream_t st);
 
-// Launchers (one per translation unit).  `grid` CTAs of kStepWarps warps; each
-// warp walks the tiles gw, gw + kStepWarps * grid, ...
+// Launchers (one per translation unit).  `grid` CTAs of W warps (kStepWarps for
+// the encode and decode kernels); each warp walks the tiles gw, gw + W * grid, ...
+//
+// The fused step kernel is built for three resident warp counts per SM.  Its
+// data stream per item is fixed, its compute per item is not (Striding and
+// DiLoCo do almost none, DeMo's top-k grows with k), and once HBM is saturated
+// more resident warps only add memory requests in flight, which lowers the
+// DRAM rate.  step_warps() takes the fewest warps that still cover the item's
+// compute.
 constexpr int kStepWarps = 11;
-cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, bool bf16, int grid, cudaStream_t st);
-cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int grid, cudaStream_t st);
+constexpr int kStepWarpsMid = 8;
+constexpr int kStepWarpsLight = 6;
+int step_warps(int mode, int k, bool bf16, int R, bool sync);
+cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, bool bf16, int warps, int grid,
+                              cudaStream_t st);
+cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int warps, int grid,
+                              cudaStream_t st);
 cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int grid, cudaStream_t st);
 cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int grid, cudaStream_t st);
 cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int grid, cudaStream_t st);

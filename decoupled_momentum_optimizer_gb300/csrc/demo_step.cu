@@ -28,12 +28,13 @@ struct alignas(1024) StepWarpSmem {
   float acc[32 * 32];   // DeMo: per-lane payload sums [u][lane]
 };
 
-constexpr int kStepThreads = kStepWarps * 32;
-constexpr size_t kStepSmem = 1024 + kStepWarps * sizeof(StepWarpSmem) + kStepWarps * 16 + 272;
-static_assert(kStepSmem <= 232448, "shared memory per CTA");
+// Dynamic shared memory of a CTA of `warps` warps: alignment slack, the warps'
+// tiles, their two mbarriers each, and the replica-count reciprocal table.
+constexpr size_t step_smem(int warps) { return 1024 + warps * sizeof(StepWarpSmem) + warps * 16 + 272; }
+static_assert(step_smem(kStepWarps) <= 232448, "shared memory per CTA");
 
-template <int MODE, bool BF16, int MAXR>
-__global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_constant__ StepParams<MAXR> p) {
+template <int MODE, bool BF16, int MAXR, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, 1) step_kernel(const __grid_constant__ StepParams<MAXR> p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte aligned start (the TMA swizzle patterns are relative to 1024-byte boundaries),
   // derived by pointer arithmetic on the shared array so every access stays a shared-memory one
@@ -41,13 +42,13 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   StepWarpSmem& ws = reinterpret_cast<StepWarpSmem*>(base)[warp];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kStepWarps * sizeof(StepWarpSmem)) + 2 * warp;
-  float* rcp = reinterpret_cast<float*>(base + kStepWarps * sizeof(StepWarpSmem) + kStepWarps * 16);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + WARPS * sizeof(StepWarpSmem)) + 2 * warp;
+  float* rcp = reinterpret_cast<float*>(base + WARPS * sizeof(StepWarpSmem) + WARPS * 16);
   if (threadIdx.x <= kMaxReplicas) rcp[threadIdx.x] = p.rcp_tab[threadIdx.x];
   __syncthreads();
 
-  const long long gw = static_cast<long long>(blockIdx.x) * kStepWarps + warp;
-  const long long TW = static_cast<long long>(gridDim.x) * kStepWarps;
+  const long long gw = static_cast<long long>(blockIdx.x) * WARPS + warp;
+  const long long TW = static_cast<long long>(gridDim.x) * WARPS;
   if (gw >= p.ntiles) return;
   const long long ntw = (p.ntiles - 1 - gw) / TW + 1;
   const bool theta_item = !(MODE == kModeDiloco && !p.sync);
@@ -237,15 +238,29 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   }
 }
 
-template <int MAXR>
-static cudaError_t launch_step_t(const StepParams<MAXR>& p, int mode, bool bf16, int grid, cudaStream_t st) {
+// Resident warps per SM for one step, from the compute per item (measured on
+// 2^26 to 2^29-parameter shards, R = 2 and 8, float32 and bfloat16 gradients):
+// Striding and DiLoCo sync items are a multiply-add per element; Random adds
+// k hashes per chunk once per tile, i.e. shared by R + 1 items; DeMo adds the
+// transforms and k - 1 top-k rounds per replica, and from k = 7 on it needs
+// all eleven warps to keep HBM busy.
+int step_warps(int mode, int k, bool bf16, int R, bool sync) {
+  if (mode == kModeStride) return kStepWarpsLight;
+  if (mode == kModeDiloco) return sync ? kStepWarpsLight : kStepWarpsMid;
+  if (mode == kModeRandom) return k <= R + 1 ? kStepWarpsLight : kStepWarpsMid;
+  if (k == 1 && !bf16) return kStepWarpsLight;
+  return k <= 6 ? kStepWarpsMid : kStepWarps;
+}
+
+template <int MAXR, int WARPS>
+static cudaError_t launch_step_w(const StepParams<MAXR>& p, int mode, bool bf16, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kStepThreads);
-  cfg.dynamicSmemBytes = kStepSmem;
+  cfg.blockDim = dim3(WARPS * 32);
+  cfg.dynamicSmemBytes = step_smem(WARPS);
   cfg.stream = st;
 #define DEMO_LAUNCH(M, B) \
-  if (mode == M && bf16 == B) return cudaLaunchKernelEx(&cfg, step_kernel<M, B, MAXR>, p);
+  if (mode == M && bf16 == B) return cudaLaunchKernelEx(&cfg, step_kernel<M, B, MAXR, WARPS>, p);
   DEMO_LAUNCH(kModeDemo, false)
   DEMO_LAUNCH(kModeDemo, true)
   DEMO_LAUNCH(kModeRandom, false)
@@ -258,21 +273,32 @@ static cudaError_t launch_step_t(const StepParams<MAXR>& p, int mode, bool bf16,
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, bool bf16, int grid, cudaStream_t st) {
-  return launch_step_t(p, mode, bf16, grid, st);
-}
-
-cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int grid, cudaStream_t st) {
-  return launch_step_t(p, mode, bf16, grid, st);
-}
-
 template <int MAXR>
-static cudaError_t prepare_t() {
+static cudaError_t launch_step_t(const StepParams<MAXR>& p, int mode, bool bf16, int warps, int grid,
+                                 cudaStream_t st) {
+  if (warps == kStepWarpsLight) return launch_step_w<MAXR, kStepWarpsLight>(p, mode, bf16, grid, st);
+  if (warps == kStepWarpsMid) return launch_step_w<MAXR, kStepWarpsMid>(p, mode, bf16, grid, st);
+  if (warps == kStepWarps) return launch_step_w<MAXR, kStepWarps>(p, mode, bf16, grid, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, bool bf16, int warps, int grid,
+                              cudaStream_t st) {
+  return launch_step_t(p, mode, bf16, warps, grid, st);
+}
+
+cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int warps, int grid,
+                              cudaStream_t st) {
+  return launch_step_t(p, mode, bf16, warps, grid, st);
+}
+
+template <int MAXR, int WARPS>
+static cudaError_t prepare_w() {
   cudaError_t e = cudaSuccess;
-#define DEMO_ATTR(M, B)                                                                           \
-  if (e == cudaSuccess)                                                                           \
-    e = cudaFuncSetAttribute(step_kernel<M, B, MAXR>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                             static_cast<int>(kStepSmem));
+#define DEMO_ATTR(M, B)                                                                                  \
+  if (e == cudaSuccess)                                                                                  \
+    e = cudaFuncSetAttribute(step_kernel<M, B, MAXR, WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             static_cast<int>(step_smem(WARPS)));
   DEMO_ATTR(kModeDemo, false)
   DEMO_ATTR(kModeDemo, true)
   DEMO_ATTR(kModeRandom, false)
@@ -282,6 +308,14 @@ static cudaError_t prepare_t() {
   DEMO_ATTR(kModeDiloco, false)
   DEMO_ATTR(kModeDiloco, true)
 #undef DEMO_ATTR
+  return e;
+}
+
+template <int MAXR>
+static cudaError_t prepare_t() {
+  cudaError_t e = prepare_w<MAXR, kStepWarpsLight>();
+  if (e == cudaSuccess) e = prepare_w<MAXR, kStepWarpsMid>();
+  if (e == cudaSuccess) e = prepare_w<MAXR, kStepWarps>();
   return e;
 }
 
