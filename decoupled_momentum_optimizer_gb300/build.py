@@ -18,7 +18,7 @@ LIB_NAME = "libdemo_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 SOURCES = ["demo_api.cu", "demo_step.cu", "demo_encode.cu", "demo_decode.cu", "demo_adamw.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 
 
 def _nvcc():

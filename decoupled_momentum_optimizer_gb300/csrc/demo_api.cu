@@ -163,6 +163,36 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
   return to_status(e);
 }
 
+// Which replicas' payloads the decode kernel stages through shared memory: the
+// spans of one 32-chunk tile must be 16-byte multiples (so every tile's span
+// starts 16-byte aligned in a 16-byte aligned buffer), and the leading replicas
+// whose buffers are 16-byte aligned are staged while they fit kDecStageBytes.
+// DiLoCo payloads (4 KB of float32 per tile and replica) are always read directly.
+template <class P>
+void stage_payloads(P& p, int mode, int k, int wire, int R) {
+  p.nstaged = 0;
+  p.vspan = p.ispan = 0;
+  if (mode == DEMO_MODE_DILOCO) return;
+  const bool demo = mode == DEMO_MODE_DEMO;
+  size_t vs, is;
+  if (wire == DEMO_WIRE_TERNARY) {
+    vs = 8 * static_cast<size_t>(k);                // [tile][k][2] words
+    is = demo ? 20 * static_cast<size_t>(k) : 0;    // [tile][k][5] words
+  } else {
+    vs = 32 * static_cast<size_t>(k) * (wire == DEMO_WIRE_F32 ? 4 : 2);
+    is = demo ? 32 * static_cast<size_t>(k) : 0;    // uint8 [chunk][k]
+  }
+  const size_t span = vs + is;
+  if (vs % 16 || is % 16 || span > static_cast<size_t>(kDecStageBytes)) return;
+  int ns = 0;
+  while (ns < R && (ns + 1) * span <= static_cast<size_t>(kDecStageBytes) && aligned16(p.vals[ns]) &&
+         (!demo || aligned16(p.idx[ns])))
+    ++ns;
+  p.nstaged = ns;
+  p.vspan = static_cast<unsigned int>(vs);
+  p.ispan = static_cast<unsigned int>(is);
+}
+
 template <int MAXR>
 int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mode, int R,
                const void* const* vals, const void* const* idx, uint64_t seed, uint64_t step, int wire,
@@ -187,6 +217,7 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
   fill_rcp(p);
   p.wire = wire;
   p.fault = st->fault;
+  stage_payloads(p, mode, k, wire, R);
   const int grid = grid_for(p.ntiles, st);
   cudaError_t e;
   if constexpr (MAXR == kSmallReplicas) {
@@ -220,7 +251,8 @@ int run_encode(DeviceState* st, const void* g, int grad_dtype, float* m, int64_t
   p.stride_mask = (mode == DEMO_MODE_STRIDE) ? stride_mask(p.stride_o, p.stride_ns, k) : 0u;
   p.beta = beta;
   p.fault = st->fault;
-  return to_status(launch_encode(p, mode, bf16, grid_for(p.ntiles, st), stream));
+  const int warps = encode_warps(mode, p.k, wire);
+  return to_status(launch_encode(p, mode, bf16, warps, grid_for(p.ntiles, st, warps), stream));
 }
 
 // Byte offset of the payload of the block starting at chunk c0 (tile t0 = c0 / 32) in a wire-format buffer.

@@ -5,21 +5,26 @@
 // Nodes" (Paper-Notes, AAAI 2026), method section, "1. FlexDeMo" Algorithm 1
 // steps 6-7 (the synchronised Q_t), "2. Replication Schemes" table.
 //
-// Per warp, theta tiles of 32 chunks stream through a two-slot TMA ring; lane
-// i combines the payload entries of its chunk (replicas in order 0..R-1, read in
-// the payload's wire format) in shared-memory accumulators, forms Q and updates
-// its theta row, which leaves
-// through the tile's own slot with coalesced stores.  The arithmetic matches
-// the fused step operation by operation, so split and fused results are
-// bit-identical.
+// Per warp, theta tiles of 32 chunks stream through a two-slot TMA ring.  With
+// each theta tile the leading replicas' payload spans for the same 32 chunks
+// (contiguous in every wire format) arrive by 1-D bulk copies on the same
+// mbarrier, two items ahead, so their latency overlaps the work on earlier
+// tiles; replicas that do not fit the 2 KB staging area, spans that are not
+// 16-byte multiples and a ragged last tile are read directly.  Lane i combines
+// the payload entries of its chunk (replicas in order 0..R-1, read in the
+// payload's wire format) in shared-memory accumulators, forms Q and updates its
+// theta row, which leaves through the tile's own slot with coalesced stores.
+// The arithmetic matches the fused step operation by operation, so split and
+// fused results are bit-identical.
 #include "demo_common.cuh"
 #include "demo_params.h"
 
 namespace demo {
 
 struct alignas(1024) DecWarpSmem {
-  float tbuf[2][1024];  // theta tiles (and the theta rows on their way out)
-  float2 acc[32 * 32];  // DeMo: [u][lane] = (sum, count); others: [i][lane].x = Q scratch
+  float tbuf[2][1024];                    // theta tiles (and the theta rows on their way out)
+  float2 acc[32 * 32];                    // DeMo: [u][lane] = (sum, count); others: [i][lane].x = Q scratch
+  unsigned char stage[2][kDecStageBytes];  // slot s: staged payload spans, replica r at r * (vspan + ispan)
 };
 
 constexpr int kDecWarps = kStepWarps;
@@ -103,6 +108,43 @@ __device__ __forceinline__ void load_payload(const void* vals, const void* idx, 
   }
 }
 
+// Adds one replica's entries for chunk c (sum and count per slot u) to acc.
+// vals / idx address either the payload buffers (chunk c of tile `tile`) or a
+// staged copy of the tile's spans (c = lane, tile = 0).  `valid`: the chunk
+// exists; `reads`: the lane may read (per-chunk formats only for chunks that
+// exist; the ternary words belong to the whole tile and every lane reads them).
+__device__ __forceinline__ void demo_accumulate(float2* acc, int lane, const void* vals, const void* idx, int wire,
+                                                int k, long long c, long long tile, bool valid, bool reads) {
+  if (wire != kWireTernary && vector_kd(k)) {
+    if (valid) {
+      float pv[8];
+      uint32_t ilo, ihi;
+      load_payload(vals, idx, wire, c, k, pv, ilo, ihi);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j < k) {
+          const int u = ((j < 4 ? ilo >> (8 * j) : ihi >> (8 * (j - 4)))) & 31;
+          float2 a = acc[u * 32 + lane];
+          a.x += pv[j];
+          a.y += 1.0f;
+          acc[u * 32 + lane] = a;
+        }
+      }
+    }
+  } else {
+    for (int j = 0; j < k; ++j) {
+      const int u = reads ? payload_index(idx, wire, c, tile, lane, k, j) : 0;
+      const float v = reads ? payload_value(vals, wire, c, tile, lane, k, j) : 0.0f;
+      if (valid) {
+        float2 a = acc[u * 32 + lane];
+        a.x += v;
+        a.y += 1.0f;
+        acc[u * 32 + lane] = a;
+      }
+    }
+  }
+}
+
 template <int MODE, int MAXR>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_constant__ DecodeParams<MAXR> p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -131,12 +173,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
   for (int u = 0; u < 32; ++u) ws.acc[u * 32 + lane] = make_float2(0.0f, 0.0f);
   __syncwarp();
 
+  const uint32_t span = p.vspan + p.ispan;  // staged bytes per replica
   auto issue = [&](long long item) {
     if (item >= nitems) return;
     const int s = static_cast<int>(item & 1);
-    const int y = static_cast<int>((gw + item * TW) * 32);
-    mbar_expect_tx(&bars[s], kTileBytesF32);
-    tma_load_2d(ws.tbuf[s], &p.theta, &bars[s], 0, y);
+    const long long t = gw + item * TW;
+    const int ns = (t + 1) * 32 <= p.nc ? p.nstaged : 0;
+    mbar_expect_tx(&bars[s], kTileBytesF32 + ns * span);
+    tma_load_2d(ws.tbuf[s], &p.theta, &bars[s], 0, static_cast<int>(t * 32));
+    for (int r = 0; r < ns; ++r) {
+      unsigned char* d = ws.stage[s] + r * span;
+      bulk_load(d, static_cast<const unsigned char*>(p.vals[r]) + t * p.vspan, p.vspan, &bars[s]);
+      if (p.ispan) bulk_load(d + p.vspan, static_cast<const unsigned char*>(p.idx[r]) + t * p.ispan, p.ispan, &bars[s]);
+    }
   };
   if (lane == 0) {
     issue(0);
@@ -149,6 +198,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     const long long row0 = (gw + item * TW) * 32;
     const long long c = row0 + lane;
     const bool valid = c < p.nc;
+    const int ns = row0 + 32 <= p.nc ? p.nstaged : 0;  // replicas staged for this tile
 
     const bool ok = mbar_wait_bounded(&bars[s], par);
     if (!__all_sync(0xffffffffu, ok)) {
@@ -167,44 +217,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     float Q[32];
     if constexpr (MODE == kModeDemo) {
       const long long tile = row0 >> 5;
-      for (int r = 0; r < p.R; ++r) {
-        if (p.wire != kWireTernary && vector_kd(p.k)) {
-          if (valid) {
-            float pv[8];
-            uint32_t ilo, ihi;
-            load_payload(p.vals[r], p.idx[r], p.wire, c, p.k, pv, ilo, ihi);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (j < p.k) {
-                const int u = ((j < 4 ? ilo >> (8 * j) : ihi >> (8 * (j - 4)))) & 31;
-                float2 a = ws.acc[u * 32 + lane];
-                a.x += pv[j];
-                a.y += 1.0f;
-                ws.acc[u * 32 + lane] = a;
-              }
-            }
-          }
-        } else {
-          // Per-chunk formats are read only for chunks that exist; the ternary words
-          // belong to the whole tile and are read by every lane.
-          const bool reads = valid || p.wire == kWireTernary;
-          for (int j = 0; j < p.k; ++j) {
-            const int u = reads ? payload_index(p.idx[r], p.wire, c, tile, lane, p.k, j) : 0;
-            const float v = reads ? payload_value(p.vals[r], p.wire, c, tile, lane, p.k, j) : 0.0f;
-            if (valid) {
-              float2 a = ws.acc[u * 32 + lane];
-              a.x += v;
-              a.y += 1.0f;
-              ws.acc[u * 32 + lane] = a;
-            }
-          }
-        }
+      for (int r = 0; r < ns; ++r) {
+        const unsigned char* sv = ws.stage[s] + r * span;
+        demo_accumulate(ws.acc, lane, sv, sv + p.vspan, p.wire, p.k, lane, 0, true, true);
       }
+      const bool reads = valid || p.wire == kWireTernary;
+      for (int r = ns; r < p.R; ++r)
+        demo_accumulate(ws.acc, lane, p.vals[r], p.idx[r], p.wire, p.k, c, tile, valid, reads);
       float Y[32];
 #pragma unroll
       for (int u = 0; u < 32; ++u) {
         const float2 a = ws.acc[u * 32 + lane];
-        Y[u] = a.x * rcp[static_cast<int>(a.y)];
+        // a malformed payload (repeated indices) can count past the table: the
+        // reciprocal is then computed, with the same rounding as the table's
+        const int cnt = static_cast<int>(a.y);
+        Y[u] = a.x * (cnt <= kMaxReplicas ? rcp[cnt] : __frcp_rn(a.y));
         ws.acc[u * 32 + lane] = make_float2(0.0f, 0.0f);
       }
       dct32_inverse(Y, Q);
@@ -257,7 +284,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
       const bool reads = valid || p.wire == kWireTernary;  // as in the DeMo branch
       auto take = [&](int j, int pos) {
         float sum = 0.0f;
-        for (int r = 0; r < p.R; ++r) sum += reads ? payload_value(p.vals[r], p.wire, c, tile, lane, p.k, j) : 0.0f;
+        for (int r = 0; r < ns; ++r) sum += payload_value(ws.stage[s] + r * span, p.wire, lane, 0, lane, p.k, j);
+        for (int r = ns; r < p.R; ++r) sum += reads ? payload_value(p.vals[r], p.wire, c, tile, lane, p.k, j) : 0.0f;
         if (valid) qs[pos * 32 + lane] = sum * p.rcpR;
       };
       if constexpr (MODE == kModeRandom) {

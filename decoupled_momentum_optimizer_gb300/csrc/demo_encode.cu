@@ -23,9 +23,9 @@ struct alignas(1024) EncWarpSmem {
   float mbuf[2][1024];  // m tile, then the new m on its way out
 };
 
-constexpr int kEncWarps = kStepWarps;
-constexpr int kEncThreads = kEncWarps * 32;
-constexpr size_t kEncSmem = 1024 + kEncWarps * sizeof(EncWarpSmem) + kEncWarps * 16;
+// Dynamic shared memory of a CTA of `warps` warps: alignment slack, tiles, mbarriers.
+constexpr size_t enc_smem(int warps) { return 1024 + warps * sizeof(EncWarpSmem) + warps * 16; }
+static_assert(enc_smem(kStepWarps) <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ bool vector_k(int k) { return k == 1 || k == 2 || k == 4 || k == 8; }
 
@@ -144,8 +144,8 @@ __device__ __forceinline__ void put_row(void* vals, int wire, long long c, long 
   }
 }
 
-template <int MODE, bool BF16>
-__global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_constant__ EncodeParams p) {
+template <int MODE, bool BF16, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_constant__ EncodeParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte aligned start (the TMA swizzle patterns are relative to 1024-byte boundaries),
   // derived by pointer arithmetic on the shared array so every access stays a shared-memory one
@@ -153,10 +153,10 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   EncWarpSmem& ws = reinterpret_cast<EncWarpSmem*>(base)[warp];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kEncWarps * sizeof(EncWarpSmem)) + 2 * warp;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + WARPS * sizeof(EncWarpSmem)) + 2 * warp;
 
-  const long long gw = static_cast<long long>(blockIdx.x) * kEncWarps + warp;
-  const long long TW = static_cast<long long>(gridDim.x) * kEncWarps;
+  const long long gw = static_cast<long long>(blockIdx.x) * WARPS + warp;
+  const long long TW = static_cast<long long>(gridDim.x) * WARPS;
   if (gw >= p.ntiles) return;
   const long long nitems = (p.ntiles - 1 - gw) / TW + 1;
 
@@ -264,14 +264,29 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   }
 }
 
-cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int grid, cudaStream_t st) {
+// Resident warps per SM for one encode, from its compute per tile (measured on
+// 2^28 and T5-base-shaped shards): as in the fused step, fewer warps run
+// faster once HBM is saturated, unless the selection needs them (DeMo from
+// k = 7 on, and the ternary format's ballots); Striding runs best with all.
+int encode_warps(int mode, int k, int wire) {
+  if (mode == kModeDemo) {
+    if (wire == kWireTernary) return kStepWarps;
+    if (k == 1) return kStepWarpsLight;
+    return k <= 6 ? kStepWarpsMid : kStepWarps;
+  }
+  if (mode == kModeStride) return kStepWarps;
+  return kStepWarpsMid;
+}
+
+template <int WARPS>
+static cudaError_t launch_encode_w(const EncodeParams& p, int mode, bool bf16, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kEncThreads);
-  cfg.dynamicSmemBytes = kEncSmem;
+  cfg.blockDim = dim3(WARPS * 32);
+  cfg.dynamicSmemBytes = enc_smem(WARPS);
   cfg.stream = st;
 #define DEMO_LAUNCH(M, B) \
-  if (mode == M && bf16 == B) return cudaLaunchKernelEx(&cfg, encode_kernel<M, B>, p);
+  if (mode == M && bf16 == B) return cudaLaunchKernelEx(&cfg, encode_kernel<M, B, WARPS>, p);
   DEMO_LAUNCH(kModeDemo, false)
   DEMO_LAUNCH(kModeDemo, true)
   DEMO_LAUNCH(kModeRandom, false)
@@ -284,12 +299,20 @@ cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int grid, 
   return cudaErrorInvalidValue;
 }
 
-cudaError_t prepare_encode_kernels() {
+cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps, int grid, cudaStream_t st) {
+  if (warps == kStepWarpsLight) return launch_encode_w<kStepWarpsLight>(p, mode, bf16, grid, st);
+  if (warps == kStepWarpsMid) return launch_encode_w<kStepWarpsMid>(p, mode, bf16, grid, st);
+  if (warps == kStepWarps) return launch_encode_w<kStepWarps>(p, mode, bf16, grid, st);
+  return cudaErrorInvalidValue;
+}
+
+template <int WARPS>
+static cudaError_t prepare_encode_w() {
   cudaError_t e = cudaSuccess;
-#define DEMO_ATTR(M, B)                                                                      \
-  if (e == cudaSuccess)                                                                      \
-    e = cudaFuncSetAttribute(encode_kernel<M, B>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                             static_cast<int>(kEncSmem));
+#define DEMO_ATTR(M, B)                                                                             \
+  if (e == cudaSuccess)                                                                             \
+    e = cudaFuncSetAttribute(encode_kernel<M, B, WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             static_cast<int>(enc_smem(WARPS)));
   DEMO_ATTR(kModeDemo, false)
   DEMO_ATTR(kModeDemo, true)
   DEMO_ATTR(kModeRandom, false)
@@ -299,6 +322,13 @@ cudaError_t prepare_encode_kernels() {
   DEMO_ATTR(kModeDiloco, false)
   DEMO_ATTR(kModeDiloco, true)
 #undef DEMO_ATTR
+  return e;
+}
+
+cudaError_t prepare_encode_kernels() {
+  cudaError_t e = prepare_encode_w<kStepWarpsLight>();
+  if (e == cudaSuccess) e = prepare_encode_w<kStepWarpsMid>();
+  if (e == cudaSuccess) e = prepare_encode_w<kStepWarps>();
   return e;
 }
 

@@ -57,11 +57,19 @@ struct DecodeParams {
   long long chunk0;  // shard index of the first chunk
   int R, k, wire;
   int stride_o, stride_ns;
+  // Payload staging: replicas 0..nstaged-1 have their per-tile spans (vspan bytes
+  // of values, ispan bytes of indices at tile t * span) copied to shared memory
+  // with the theta tile; the others, and a ragged last tile, are read directly.
+  int nstaged;
+  unsigned int vspan, ispan;
   float lr, rcpR;
   unsigned long long hbase;
   float rcp_tab[kMaxReplicas + 1];
   unsigned int* fault;
 };
+
+// Shared-memory staging per decode slot for the replicas' payload spans.
+constexpr int kDecStageBytes = 2048;
 
 // Decoupled AdamW (elementwise, grid-stride over groups of four parameters).
 struct AdamWParams {
@@ -95,7 +103,8 @@ cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, boo
                               cudaStream_t st);
 cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int warps, int grid,
                               cudaStream_t st);
-cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int grid, cudaStream_t st);
+int encode_warps(int mode, int k, int wire);
+cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps, int grid, cudaStream_t st);
 cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int grid, cudaStream_t st);
 cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int grid, cudaStream_t st);
 

@@ -154,7 +154,9 @@ int demo_encode(const void* g, int grad_dtype, float* m, int64_t n, int chunk, i
  *           them (idx only for DeMo; pass NULL otherwise)
  *   lr      finite float
  * DiLoCo on a non-sync step leaves theta untouched and launches nothing.
- * A DeMo index byte is used modulo 32 (it never addresses outside the chunk).
+ * A DeMo index byte is used modulo 32 (it never addresses outside the chunk);
+ * an index repeated within a chunk is counted once per entry, as every
+ * received entry enters the scatter-mean.
  */
 int demo_decode_update(float* theta, int64_t n, int chunk, int k, float lr, int mode, int R,
                        const float* const* vals, const uint8_t* const* idx,

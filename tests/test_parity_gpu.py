@@ -269,6 +269,28 @@ def test_invalid_arguments_launch_nothing():
     assert torch.equal(theta, snap[0]) and torch.equal(m, snap[1])
 
 
+def test_decode_repeated_indices_count_every_entry():
+    """A malformed DeMo payload whose every index is 0 gives slot 0 of each chunk
+    R*k = 160 entries, more than the replica count the kernels tabulate
+    reciprocals for.  The decode still takes the mean over every entry, as the
+    oracle's scatter-mean counts them, both for the replicas staged through
+    shared memory and for the ones read directly, and stays inside its buffers."""
+    R, k, n = 40, 4, 32 * 32 * 3 + 32 * 5  # three full tiles and a ragged one
+    nc = n // C
+    gen = torch.Generator().manual_seed(11)
+    vals = [torch.randn(nc, k, generator=gen) * 1e-3 for _ in range(R)]
+    idx = torch.zeros(nc * k, dtype=torch.uint8, device="cuda")
+    Q = torch.zeros(n, device="cuda")
+    dm.decode_update(Q, [v.reshape(-1).cuda() for v in vals], [idx] * R, k=k, lr=-1.0, mode="demo", seed=0, step=0)
+    torch.cuda.synchronize()
+    _, Qref, Yref, cnt = ref.decode_update(np.zeros(n), [v.double().numpy() for v in vals],
+                                           [np.zeros((nc, k), dtype=np.int64)] * R, -1.0, ref.MODE_DEMO)
+    assert (cnt[:, 0] == R * k).all()
+    scale = np.abs(np.stack([v.double().numpy() for v in vals])).sum((0, 2)) / (R * k)  # mean |entry| per chunk
+    err = np.abs(f64(Q).reshape(nc, C) - Qref) / scale[:, None]
+    assert err.max() < 1e-5, err.max()
+
+
 def test_guard_bands_untouched():
     n = 32 * (64 + 5)
     pad = 4096 // 4
