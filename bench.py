@@ -158,13 +158,17 @@ STEP_KERNEL_SOURCES = ("demo_step.cu", "demo_common.cuh", "demo_params.h", "dct3
 
 
 def src_hash():
-    """Hash of the fused step kernel's sources (the kernel the roofline and traffic describe)."""
+    """Hash of the fused step kernel's sources and compile options (the kernel the roofline
+    and traffic describe); include paths are left out, so the hash is the same on every machine."""
     import hashlib
+
+    from decoupled_momentum_optimizer_gb300 import build
 
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decoupled_momentum_optimizer_gb300", "csrc")
     for f in STEP_KERNEL_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
+    h.update(" ".join(f for f in build.NVCC_FLAGS if not os.path.isabs(f)).encode())
     return h.hexdigest()[:16]
 
 
