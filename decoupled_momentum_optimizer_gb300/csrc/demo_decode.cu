@@ -21,9 +21,15 @@
 
 namespace demo {
 
+// One slot's running sum and number of received entries.
+struct alignas(8) SumCount {
+  float sum;
+  uint32_t cnt;
+};
+
 struct alignas(1024) DecWarpSmem {
   float tbuf[2][1024];                    // theta tiles (and the theta rows on their way out)
-  float2 acc[32 * 32];                    // DeMo: [u][lane] = (sum, count); others: [i][lane].x = Q scratch
+  SumCount acc[32 * 32];                  // DeMo: [u][lane]; others: [i][lane].sum = Q scratch
   unsigned char stage[2][kDecStageBytes];  // slot s: staged payload spans, replica r at r * (vspan + ispan)
 };
 
@@ -113,7 +119,7 @@ __device__ __forceinline__ void load_payload(const void* vals, const void* idx, 
 // staged copy of the tile's spans (c = lane, tile = 0).  `valid`: the chunk
 // exists; `reads`: the lane may read (per-chunk formats only for chunks that
 // exist; the ternary words belong to the whole tile and every lane reads them).
-__device__ __forceinline__ void demo_accumulate(float2* acc, int lane, const void* vals, const void* idx, int wire,
+__device__ __forceinline__ void demo_accumulate(SumCount* acc, int lane, const void* vals, const void* idx, int wire,
                                                 int k, long long c, long long tile, bool valid, bool reads) {
   if (wire != kWireTernary && vector_kd(k)) {
     if (valid) {
@@ -124,9 +130,9 @@ __device__ __forceinline__ void demo_accumulate(float2* acc, int lane, const voi
       for (int j = 0; j < 8; ++j) {
         if (j < k) {
           const int u = ((j < 4 ? ilo >> (8 * j) : ihi >> (8 * (j - 4)))) & 31;
-          float2 a = acc[u * 32 + lane];
-          a.x += pv[j];
-          a.y += 1.0f;
+          SumCount a = acc[u * 32 + lane];
+          a.sum += pv[j];
+          a.cnt += 1u;
           acc[u * 32 + lane] = a;
         }
       }
@@ -136,9 +142,9 @@ __device__ __forceinline__ void demo_accumulate(float2* acc, int lane, const voi
       const int u = reads ? payload_index(idx, wire, c, tile, lane, k, j) : 0;
       const float v = reads ? payload_value(vals, wire, c, tile, lane, k, j) : 0.0f;
       if (valid) {
-        float2 a = acc[u * 32 + lane];
-        a.x += v;
-        a.y += 1.0f;
+        SumCount a = acc[u * 32 + lane];
+        a.sum += v;
+        a.cnt += 1u;
         acc[u * 32 + lane] = a;
       }
     }
@@ -170,7 +176,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     fence_mbar_init();
   }
 #pragma unroll
-  for (int u = 0; u < 32; ++u) ws.acc[u * 32 + lane] = make_float2(0.0f, 0.0f);
+  for (int u = 0; u < 32; ++u) ws.acc[u * 32 + lane] = SumCount{0.0f, 0u};
   __syncwarp();
 
   const uint32_t span = p.vspan + p.ispan;  // staged bytes per replica
@@ -224,16 +230,31 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
       const bool reads = valid || p.wire == kWireTernary;
       for (int r = ns; r < p.R; ++r)
         demo_accumulate(ws.acc, lane, p.vals[r], p.idx[r], p.wire, p.k, c, tile, valid, reads);
+      if (p.R * p.k > kMaxReplicas) {
+        // Valid payloads count at most R entries per slot; a malformed one (an index
+        // repeated within a chunk) can count more than the reciprocal table covers.
+        // Such a slot is replaced by its mean and a count of one (rcp[1] = 1), the
+        // reciprocal rounded as the table's entries are.
+        uint32_t most = 0;
+#pragma unroll
+        for (int u = 0; u < 32; ++u) most = umax32(most, ws.acc[u * 32 + lane].cnt);
+        if (__any_sync(0xffffffffu, most > kMaxReplicas)) {
+#pragma unroll 1
+          for (int u = 0; u < 32; ++u) {
+            const SumCount a = ws.acc[u * 32 + lane];
+            if (a.cnt > kMaxReplicas)
+              ws.acc[u * 32 + lane] = SumCount{a.sum * __frcp_rn(static_cast<float>(a.cnt)), 1u};
+          }
+        }
+      }
       float Y[32];
 #pragma unroll
       for (int u = 0; u < 32; ++u) {
-        const float2 a = ws.acc[u * 32 + lane];
-        // a malformed payload (repeated indices) can count past the table: the
-        // reciprocal is then computed, with the same rounding as the table's
-        const int cnt = static_cast<int>(a.y);
-        Y[u] = a.x * (cnt <= kMaxReplicas ? rcp[cnt] : __frcp_rn(a.y));
-        ws.acc[u * 32 + lane] = make_float2(0.0f, 0.0f);
+        const SumCount a = ws.acc[u * 32 + lane];
+        Y[u] = a.sum * rcp[a.cnt];
       }
+#pragma unroll
+      for (int u = 0; u < 32; ++u) ws.acc[u * 32 + lane] = SumCount{0.0f, 0u};
       dct32_inverse(Y, Q);
     } else if constexpr (MODE == kModeDiloco) {
 #pragma unroll
