@@ -188,7 +188,8 @@ def ncu_traffic(workload, mode, k, R):
 
 
 def cpu_baseline(wl_name, mode, k, sign, R, seconds=10.0):
-    """Time the float64 oracle single-threaded in a fresh process on a sample of the workload."""
+    """Time the float64 oracle in a fresh process on a sample of the workload: one thread
+    (the reported value) and, beside it, with every host core available to BLAS."""
     code = r"""
 import json, os, sys, time
 sys.path.insert(0, %r)
@@ -214,15 +215,51 @@ while True:
         break
 print(json.dumps({"params_per_s": n * steps / el, "steps": steps, "seconds": el, "sample_params": n}))
 """ % (ROOT, mode, k, sign, R, seconds)
-    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
-    if r.returncode != 0:
-        return {"value": None, "unit": "params/s", "cores": 1, "kind": "oracle", "error": r.stderr[-300:]}
-    d = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": d["params_per_s"], "unit": "params/s", "cores": 1, "kind": "oracle",
-            "sample": f"{d['sample_params']} params (16384 chunks) of the {wl_name} workload, {mode} k={k} "
-                      f"sign={int(sign)} R={R}, {d['steps']} steps in {d['seconds']:.1f} s, "
-                      f"float64 numpy, one thread (BLAS threads = 1)"}
+    def run(threads):
+        t = str(threads)
+        env = dict(os.environ, OPENBLAS_NUM_THREADS=t, OMP_NUM_THREADS=t, MKL_NUM_THREADS=t)
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+        if r.returncode != 0:
+            return None, r.stderr[-300:]
+        return json.loads(r.stdout.strip().splitlines()[-1]), None
+
+    d, err = run(1)
+    if d is None:
+        return {"value": None, "unit": "params/s", "cores": 1, "kind": "oracle", "error": err}
+    out = {"value": d["params_per_s"], "unit": "params/s", "cores": 1, "kind": "oracle",
+           "sample": f"{d['sample_params']} params (16384 chunks) of the {wl_name} workload, {mode} k={k} "
+                     f"sign={int(sign)} R={R}, {d['steps']} steps in {d['seconds']:.1f} s, "
+                     f"float64 numpy, one thread (BLAS threads = 1)",
+           "host": host_cpu()}
+    ncpu = os.cpu_count() or 1
+    if ncpu > 1:
+        # the same sample with every host core available to BLAS (the oracle's elementwise
+        # numpy work stays on one thread, so this is its best case on this host)
+        d2, _ = run(ncpu)
+        if d2 is not None:
+            out["all_cores"] = {"value": d2["params_per_s"], "cores": ncpu, "steps": d2["steps"],
+                                "seconds": round(d2["seconds"], 2)}
+    return out
+
+
+def host_cpu():
+    """CPU description of this host (model name, or the ARM implementer/part codes) and its core count."""
+    import platform
+
+    desc = None
+    try:
+        fields = {}
+        for line in open("/proc/cpuinfo"):
+            if ":" in line:
+                key, val = (x.strip() for x in line.split(":", 1))
+                fields.setdefault(key, val)
+        if "model name" in fields:
+            desc = fields["model name"]
+        elif "CPU implementer" in fields:
+            desc = f"ARM implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    except OSError:
+        pass
+    return {"cpu": desc or platform.processor() or "unknown", "machine": platform.machine(), "cores": os.cpu_count()}
 
 
 # ----------------------------------------------------------------------------
