@@ -416,15 +416,22 @@ __device__ __forceinline__ int nth_set_bit(uint32_t v, int r) {
 // Random scheme: k draws for global chunk c by partial Fisher-Yates.  hbase is
 // sm(sm(seed) ^ step), hoisted to the host.  Calls f(j, position) for each draw
 // j in order and returns the mask of the k positions.
+// Draw j of a chunk whose hash is hc: the r-th still free position, r uniform
+// in [0, 32 - j); the position is taken out of free_mask.
+__device__ __forceinline__ int random_draw(uint64_t hc, int j, uint32_t& free_mask) {
+  const uint64_t h = splitmix64(hc ^ static_cast<uint64_t>(j));
+  const uint32_t r = static_cast<uint32_t>(((h >> 32) * static_cast<uint64_t>(32 - j)) >> 32);
+  const int p = nth_set_bit(free_mask, static_cast<int>(r));
+  free_mask &= ~(1u << p);
+  return p;
+}
+
 template <class F>
 __device__ __forceinline__ uint32_t random_draws(uint64_t hbase, uint64_t c, int k, F&& f) {
   const uint64_t hc = splitmix64(hbase ^ c);
   uint32_t free_mask = 0xffffffffu, sel = 0;
   for (int j = 0; j < k; ++j) {
-    const uint64_t h = splitmix64(hc ^ static_cast<uint64_t>(j));
-    const uint32_t r = static_cast<uint32_t>(((h >> 32) * static_cast<uint64_t>(32 - j)) >> 32);
-    const int p = nth_set_bit(free_mask, static_cast<int>(r));
-    free_mask &= ~(1u << p);
+    const int p = random_draw(hc, j, free_mask);
     sel |= 1u << p;
     f(j, p);
   }

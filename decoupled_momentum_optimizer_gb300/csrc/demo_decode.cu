@@ -302,17 +302,58 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
 #pragma unroll
       for (int i = 0; i < 32; ++i) qs[i * 32 + lane] = 0.0f;
       const long long tile = row0 >> 5;
-      const bool reads = valid || p.wire == kWireTernary;  // as in the DeMo branch
-      auto take = [&](int j, int pos) {
-        float sum = 0.0f;
-        for (int r = 0; r < ns; ++r) sum += payload_value(ws.stage[s] + r * span, p.wire, lane, 0, lane, p.k, j);
-        for (int r = ns; r < p.R; ++r) sum += reads ? payload_value(p.vals[r], p.wire, c, tile, lane, p.k, j) : 0.0f;
-        if (valid) qs[pos * 32 + lane] = sum * p.rcpR;
-      };
-      if constexpr (MODE == kModeRandom) {
-        random_draws(p.hbase, static_cast<uint64_t>(c + p.chunk0), p.k, take);
+      if (ns == p.R && p.k <= 8) {
+        // Every replica staged and k <= 8: sum the replicas' k values per draw
+        // (replicas in order; one vector load per replica when the format allows),
+        // then place each sum at its draw's position, with the draws unrolled.
+        float sum[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sum[j] = 0.0f;
+        const bool vec = p.wire != kWireTernary && vector_kd(p.k);
+        for (int r = 0; r < p.R; ++r) {
+          const unsigned char* sv = ws.stage[s] + r * span;
+          float pv[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) pv[j] = 0.0f;
+          if (vec) {
+            uint32_t ilo, ihi;
+            load_payload(sv, nullptr, p.wire, lane, p.k, pv, ilo, ihi);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (j < p.k) pv[j] = payload_value(sv, p.wire, lane, 0, lane, p.k, j);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) sum[j] += pv[j];
+        }
+        uint64_t hc = 0;
+        uint32_t free_mask = 0xffffffffu;
+        if constexpr (MODE == kModeRandom) hc = splitmix64(p.hbase ^ static_cast<uint64_t>(c + p.chunk0));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (j < p.k) {
+            int pos;
+            if constexpr (MODE == kModeRandom) {
+              pos = random_draw(hc, j, free_mask);
+            } else {
+              pos = stride_position(p.stride_o, p.stride_ns, j);
+            }
+            qs[pos * 32 + lane] = sum[j] * p.rcpR;
+          }
+        }
       } else {
-        for (int j = 0; j < p.k; ++j) take(j, stride_position(p.stride_o, p.stride_ns, j));
+        const bool reads = valid || p.wire == kWireTernary;  // as in the DeMo branch
+        auto take = [&](int j, int pos) {
+          float sum = 0.0f;
+          for (int r = 0; r < ns; ++r) sum += payload_value(ws.stage[s] + r * span, p.wire, lane, 0, lane, p.k, j);
+          for (int r = ns; r < p.R; ++r) sum += reads ? payload_value(p.vals[r], p.wire, c, tile, lane, p.k, j) : 0.0f;
+          if (valid) qs[pos * 32 + lane] = sum * p.rcpR;
+        };
+        if constexpr (MODE == kModeRandom) {
+          random_draws(p.hbase, static_cast<uint64_t>(c + p.chunk0), p.k, take);
+        } else {
+          for (int j = 0; j < p.k; ++j) take(j, stride_position(p.stride_o, p.stride_ns, j));
+        }
       }
 #pragma unroll
       for (int i = 0; i < 32; ++i) Q[i] = qs[i * 32 + lane];
