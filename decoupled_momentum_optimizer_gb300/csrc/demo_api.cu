@@ -163,16 +163,19 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
   return to_status(e);
 }
 
-// Which replicas' payloads the decode kernel stages through shared memory: the
-// spans of one 32-chunk tile must be 16-byte multiples (so every tile's span
-// starts 16-byte aligned in a 16-byte aligned buffer), and the leading replicas
-// whose buffers are 16-byte aligned are staged while they fit kDecStageBytes.
+// Which replicas' payloads the decode kernel stages through shared memory, and
+// the CTA shape that goes with it (returns its warp count).  The spans of one
+// 32-chunk tile must be 16-byte multiples (so every tile's span starts 16-byte
+// aligned in a 16-byte aligned buffer).  When every replica fits the 2 KB
+// staging area the decode runs 11 warps; when they fit only 3 KB it runs 10
+// warps with 3 KB (measured faster than staging some replicas); otherwise the
+// leading replicas that fit 2 KB are staged and the others read directly.
 // DiLoCo payloads (4 KB of float32 per tile and replica) are always read directly.
 template <class P>
-void stage_payloads(P& p, int mode, int k, int wire, int R) {
+int stage_payloads(P& p, int mode, int k, int wire, int R) {
   p.nstaged = 0;
   p.vspan = p.ispan = 0;
-  if (mode == DEMO_MODE_DILOCO) return;
+  if (mode == DEMO_MODE_DILOCO) return kStepWarps;
   const bool demo = mode == DEMO_MODE_DEMO;
   size_t vs, is;
   if (wire == DEMO_WIRE_TERNARY) {
@@ -183,14 +186,19 @@ void stage_payloads(P& p, int mode, int k, int wire, int R) {
     is = demo ? 32 * static_cast<size_t>(k) : 0;    // uint8 [chunk][k]
   }
   const size_t span = vs + is;
-  if (vs % 16 || is % 16 || span > static_cast<size_t>(kDecStageBytes)) return;
-  int ns = 0;
-  while (ns < R && (ns + 1) * span <= static_cast<size_t>(kDecStageBytes) && aligned16(p.vals[ns]) &&
-         (!demo || aligned16(p.idx[ns])))
-    ++ns;
+  if (vs % 16 || is % 16 || span > static_cast<size_t>(kDecStageBytes)) return kStepWarps;
+  int aligned = 0;  // leading replicas with 16-byte aligned buffers
+  while (aligned < R && aligned16(p.vals[aligned]) && (!demo || aligned16(p.idx[aligned]))) ++aligned;
+  int warps = kStepWarps;
+  int ns = static_cast<int>(std::min<size_t>(aligned, kDecStageBytes / span));
+  if (ns < R && aligned == R && R * span <= static_cast<size_t>(kDecStageBytesWide)) {
+    warps = kDecWarpsWide;
+    ns = R;
+  }
   p.nstaged = ns;
   p.vspan = static_cast<unsigned int>(vs);
   p.ispan = static_cast<unsigned int>(is);
+  return warps;
 }
 
 template <int MAXR>
@@ -217,13 +225,13 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
   fill_rcp(p);
   p.wire = wire;
   p.fault = st->fault;
-  stage_payloads(p, mode, k, wire, R);
-  const int grid = grid_for(p.ntiles, st);
+  const int warps = stage_payloads(p, mode, k, wire, R);
+  const int grid = grid_for(p.ntiles, st, warps);
   cudaError_t e;
   if constexpr (MAXR == kSmallReplicas) {
-    e = launch_decode_small(p, mode, grid, stream);
+    e = launch_decode_small(p, mode, warps, grid, stream);
   } else {
-    e = launch_decode_large(p, mode, grid, stream);
+    e = launch_decode_large(p, mode, warps, grid, stream);
   }
   return to_status(e);
 }

@@ -27,15 +27,22 @@ struct alignas(8) SumCount {
   uint32_t cnt;
 };
 
+template <int STAGE>
 struct alignas(1024) DecWarpSmem {
   float tbuf[2][1024];                    // theta tiles (and the theta rows on their way out)
   SumCount acc[32 * 32];                  // DeMo: [u][lane]; others: [i][lane].sum = Q scratch
-  unsigned char stage[2][kDecStageBytes];  // slot s: staged payload spans, replica r at r * (vspan + ispan)
+  unsigned char stage[2][STAGE];          // slot s: staged payload spans, replica r at r * (vspan + ispan)
 };
 
-constexpr int kDecWarps = kStepWarps;
-constexpr int kDecThreads = kDecWarps * 32;
-constexpr size_t kDecSmem = 1024 + kDecWarps * sizeof(DecWarpSmem) + kDecWarps * 16 + 272;
+// Two CTA shapes: 11 warps with 2 KB of staging per slot, or 10 warps with 3 KB
+// (for payloads whose replicas fit 3 KB but not 2 KB); both fill the SM's shared memory.
+__host__ __device__ constexpr int dec_stage(int warps) { return warps == kStepWarps ? kDecStageBytes : kDecStageBytesWide; }
+constexpr size_t dec_smem(int warps) {
+  return 1024 + warps * (2 * 4096 + 8 * 1024 + 2 * dec_stage(warps)) + warps * 16 + 272;
+}
+static_assert(sizeof(DecWarpSmem<kDecStageBytes>) == 2 * 4096 + 8 * 1024 + 2 * kDecStageBytes, "layout");
+static_assert(sizeof(DecWarpSmem<kDecStageBytesWide>) == 2 * 4096 + 8 * 1024 + 2 * kDecStageBytesWide, "layout");
+static_assert(dec_smem(kStepWarps) <= 232448 && dec_smem(kDecWarpsWide) <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ bool vector_kd(int k) { return k == 1 || k == 2 || k == 4 || k == 8; }
 
@@ -151,22 +158,23 @@ __device__ __forceinline__ void demo_accumulate(SumCount* acc, int lane, const v
   }
 }
 
-template <int MODE, int MAXR>
-__global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_constant__ DecodeParams<MAXR> p) {
+template <int MODE, int MAXR, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_constant__ DecodeParams<MAXR> p) {
+  using WarpSmem = DecWarpSmem<dec_stage(WARPS)>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte aligned start (the TMA swizzle patterns are relative to 1024-byte boundaries),
   // derived by pointer arithmetic on the shared array so every access stays a shared-memory one
   unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  DecWarpSmem& ws = reinterpret_cast<DecWarpSmem*>(base)[warp];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kDecWarps * sizeof(DecWarpSmem)) + 2 * warp;
-  float* rcp = reinterpret_cast<float*>(base + kDecWarps * sizeof(DecWarpSmem) + kDecWarps * 16);
+  WarpSmem& ws = reinterpret_cast<WarpSmem*>(base)[warp];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + WARPS * sizeof(WarpSmem)) + 2 * warp;
+  float* rcp = reinterpret_cast<float*>(base + WARPS * sizeof(WarpSmem) + WARPS * 16);
   if (threadIdx.x <= kMaxReplicas) rcp[threadIdx.x] = p.rcp_tab[threadIdx.x];
   __syncthreads();
 
-  const long long gw = static_cast<long long>(blockIdx.x) * kDecWarps + warp;
-  const long long TW = static_cast<long long>(gridDim.x) * kDecWarps;
+  const long long gw = static_cast<long long>(blockIdx.x) * WARPS + warp;
+  const long long TW = static_cast<long long>(gridDim.x) * WARPS;
   if (gw >= p.ntiles) return;
   const long long nitems = (p.ntiles - 1 - gw) / TW + 1;
 
@@ -369,46 +377,62 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
   }
 }
 
-template <int MAXR>
-static cudaError_t launch_decode_t(const DecodeParams<MAXR>& p, int mode, int grid, cudaStream_t st) {
+template <int MAXR, int WARPS>
+static cudaError_t launch_decode_w(const DecodeParams<MAXR>& p, int mode, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kDecThreads);
-  cfg.dynamicSmemBytes = kDecSmem;
+  cfg.blockDim = dim3(WARPS * 32);
+  cfg.dynamicSmemBytes = dec_smem(WARPS);
   cfg.stream = st;
   switch (mode) {
-    case kModeDemo: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR>, p);
-    case kModeRandom: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeRandom, MAXR>, p);
-    case kModeStride: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeStride, MAXR>, p);
-    case kModeDiloco: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDiloco, MAXR>, p);
+    case kModeDemo: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS>, p);
+    case kModeRandom: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeRandom, MAXR, WARPS>, p);
+    case kModeStride: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeStride, MAXR, WARPS>, p);
+    case kModeDiloco: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDiloco, MAXR, WARPS>, p);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int grid, cudaStream_t st) {
-  return launch_decode_t(p, mode, grid, st);
-}
-
-cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int grid, cudaStream_t st) {
-  return launch_decode_t(p, mode, grid, st);
-}
-
 template <int MAXR>
-static cudaError_t prepare_t() {
-  const int bytes = static_cast<int>(kDecSmem);
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<kModeDemo, MAXR>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+static cudaError_t launch_decode_t(const DecodeParams<MAXR>& p, int mode, int warps, int grid, cudaStream_t st) {
+  if (warps == kStepWarps) return launch_decode_w<MAXR, kStepWarps>(p, mode, grid, st);
+  if (warps == kDecWarpsWide) return launch_decode_w<MAXR, kDecWarpsWide>(p, mode, grid, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int grid,
+                                cudaStream_t st) {
+  return launch_decode_t(p, mode, warps, grid, st);
+}
+
+cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int grid,
+                                cudaStream_t st) {
+  return launch_decode_t(p, mode, warps, grid, st);
+}
+
+template <int MAXR, int WARPS>
+static cudaError_t prepare_w() {
+  const int bytes = static_cast<int>(dec_smem(WARPS));
+  cudaError_t e = cudaSuccess;
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_kernel<kModeRandom, MAXR>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = cudaFuncSetAttribute(decode_kernel<kModeDemo, MAXR, WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_kernel<kModeStride, MAXR>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = cudaFuncSetAttribute(decode_kernel<kModeRandom, MAXR, WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_kernel<kModeDiloco, MAXR>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = cudaFuncSetAttribute(decode_kernel<kModeStride, MAXR, WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_kernel<kModeDiloco, MAXR, WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes);
   return e;
 }
 
 cudaError_t prepare_decode_kernels() {
-  cudaError_t e = prepare_t<kSmallReplicas>();
-  if (e == cudaSuccess) e = prepare_t<kMaxReplicas>();
+  cudaError_t e = prepare_w<kSmallReplicas, kStepWarps>();
+  if (e == cudaSuccess) e = prepare_w<kSmallReplicas, kDecWarpsWide>();
+  if (e == cudaSuccess) e = prepare_w<kMaxReplicas, kStepWarps>();
+  if (e == cudaSuccess) e = prepare_w<kMaxReplicas, kDecWarpsWide>();
   return e;
 }
 

@@ -68,8 +68,11 @@ struct DecodeParams {
   unsigned int* fault;
 };
 
-// Shared-memory staging per decode slot for the replicas' payload spans.
+// Shared-memory staging per decode slot for the replicas' payload spans: 2 KB
+// with 11 warps per SM, or 3 KB with 10 warps when the replicas fit only that.
 constexpr int kDecStageBytes = 2048;
+constexpr int kDecStageBytesWide = 3072;
+constexpr int kDecWarpsWide = 10;
 
 // Decoupled AdamW (elementwise, grid-stride over groups of four parameters).
 struct AdamWParams {
@@ -105,8 +108,10 @@ cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool 
                               cudaStream_t st);
 int encode_warps(int mode, int k, int wire);
 cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps, int grid, cudaStream_t st);
-cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int grid, cudaStream_t st);
-cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int grid, cudaStream_t st);
+cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int grid,
+                                cudaStream_t st);
+cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int grid,
+                                cudaStream_t st);
 
 // Set the dynamic shared-memory limit of every kernel instantiation.
 cudaError_t prepare_step_kernels();
