@@ -38,7 +38,8 @@ def gpu_direction(theta, gs, ms, vs, step):
 
 
 @pytest.mark.parametrize("R,bf16,n", [(1, False, 32 * 1000), (2, False, 32 * 1003), (3, True, 32 * 777),
-                                      (2, False, 32)])
+                                      (2, False, 32), (4, False, 32 * 513),
+                                      (7, True, 32 * 611)])  # R > 4: replicas in batches of four
 def test_adamw_teacher_forced(R, bf16, n):
     theta = cuda_normal(n, 2e-2, 1)
     ms = [torch.zeros(n, device="cuda") for _ in range(R)]
