@@ -266,6 +266,18 @@ def host_cpu():
 # Reference arm: the CPU oracle, rank 0 only
 # ----------------------------------------------------------------------------
 
+def run_config(wl, R, mode, k, sign, world):
+    """The JSON line's `config`: the workload one GPU's step covers (both arms print the same)."""
+    step_bytes = algorithmic_bytes(wl.n, R, 2 if wl.g_dtype == "bf16" else 4, mode)
+    flush = step_bytes < 2 * L2_BYTES
+    return {"workload": f"{wl.name}: {wl.n} params, R={R} resident replicas, {mode} k={k}/32, "
+                        f"sign={'on' if sign else 'off'}, grads {wl.g_dtype}",
+            "n": wl.n, "R": R, "mode": mode, "k": k, "sign": bool(sign), "grad_dtype": wl.g_dtype,
+            "parallelism": f"one shard per GPU x {world}",
+            "l2": "L2 flushed (256 MB write) between steps" if flush else
+            f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step)"}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -296,7 +308,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "n": wl.n, "R": R, "mode": mode, "k": k, "sign": bool(sign)},
+        "config": run_config(wl, R, mode, k, sign, args.gpus),
         "cpu_baseline": {"value": value, "unit": "params/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -556,7 +568,7 @@ def main():
 
     sampler = ClockSampler(local)
     barrier()
-    step_ms, kernel_ms, flush = time_fused(dm, case, mode, k, sign, seed, args.steps, args.warmup, stream,
+    step_ms, kernel_ms, _ = time_fused(dm, case, mode, k, sign, seed, args.steps, args.warmup, stream,
                                            sampler=sampler)
     barrier()
     if world > 1:
@@ -605,12 +617,7 @@ def main():
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"{wl.name}: {n} params, R={R} resident replicas, {mode} k={k}/32, "
-                               f"sign={'on' if sign else 'off'}, grads {wl.g_dtype}",
-                   "n": n, "R": R, "mode": mode, "k": k, "sign": bool(sign), "grad_dtype": wl.g_dtype,
-                   "parallelism": f"one shard per GPU x {world}",
-                   "l2": "L2 flushed (256 MB write) between steps" if flush else
-                   f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB per step)"},
+        "config": run_config(wl, R, mode, k, sign, world),
         "achieved_gbs": achieved,
         "hbm_frac_of_peak": achieved / peak,
         "roofline": roof,
