@@ -47,6 +47,10 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--sweep", default=None, help="measure every configuration of the results table into this JSONL file")
+    p.add_argument("--only", choices=["split", "adamw"], default=None,
+                   help="time only this path on the workload (R encodes + one decode, or the Decoupled AdamW step) "
+                        "and print its time; for profiling those kernels")
+    p.add_argument("--wire", default="f32", help="payload wire format of --only split")
     return p.parse_args()
 
 
@@ -539,6 +543,8 @@ def main():
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.only:
+        return run_only(args)
 
     import torch
     import torch.distributed as dist
@@ -666,6 +672,28 @@ def sweep_cases():
         for mode, k in (("random", 1), ("random", 8), ("stride", 4), ("diloco", 1), ("diloco-sync", 1)):
             out.append((f"flat{1 << e}", mode, k, True, 2, ("fused", "split") if e == 26 else ("fused",)))
     return out
+
+
+def run_only(args):
+    """Time one path (split or AdamW) on the workload; prints a line of its own, not the bench line."""
+    import torch
+
+    import decoupled_momentum_optimizer_gb300 as dm
+
+    dm.init(0)
+    wl, mode, k, sign, R = workload_settings(args)
+    case = Case(wl, R, torch.device("cuda", 0), n_sets=2)
+    stream = torch.cuda.current_stream()
+    if args.only == "split":
+        ms = time_split(dm, case, mode, k, sign, 0, args.steps, args.warmup, stream, wire=args.wire)
+        nbytes = split_bytes(case.n, R, case.grad_bytes, mode, k, wire=args.wire)
+    else:
+        ms = time_adamw(dm, case, args.steps, args.warmup, stream)
+        nbytes = case.n * (R * (case.grad_bytes + 16) + 8)
+    print(json.dumps({"only": args.only, "workload": wl.name, "n": case.n, "mode": mode, "k": k, "R": R,
+                      "wire": args.wire if args.only == "split" else None, "ms": ms,
+                      "gbs": nbytes / (ms * 1e-3) / 1e9, "device_fault": dm.device_fault()}))
+    return 0
 
 
 def run_sweep(args):
