@@ -16,7 +16,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "demo_params.h"
+#include "demo_launch.h"
 
 namespace demo {
 

@@ -7,7 +7,7 @@
 
 #include "../../include/demo.h"
 #include "demo_common.cuh"
-#include "demo_params.h"
+#include "demo_launch.h"
 
 namespace {
 
@@ -259,7 +259,7 @@ int run_encode(DeviceState* st, const void* g, int grad_dtype, float* m, int64_t
   p.stride_mask = (mode == DEMO_MODE_STRIDE) ? stride_mask(p.stride_o, p.stride_ns, k) : 0u;
   p.beta = beta;
   p.fault = st->fault;
-  const int warps = encode_warps(mode, p.k, wire);
+  const int warps = encode_warps(mode, p.k, wire, bf16);
   return to_status(launch_encode(p, mode, bf16, warps, grid_for(p.ntiles, st, warps), stream));
 }
 

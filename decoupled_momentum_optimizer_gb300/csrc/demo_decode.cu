@@ -17,7 +17,7 @@
 // The arithmetic matches the fused step operation by operation, so split and
 // fused results are bit-identical.
 #include "demo_common.cuh"
-#include "demo_params.h"
+#include "demo_launch.h"
 
 namespace demo {
 

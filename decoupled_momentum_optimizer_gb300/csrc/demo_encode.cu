@@ -14,7 +14,7 @@
 // 4 or 8; or ternary bit-planes, one 32-bit word per warp tile and value slot
 // built with warp ballots.
 #include "demo_common.cuh"
-#include "demo_params.h"
+#include "demo_launch.h"
 
 namespace demo {
 
@@ -265,17 +265,21 @@ __global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_cons
 }
 
 // Resident warps per SM for one encode, from its compute per tile (measured on
-// 2^28 and T5-base-shaped shards): as in the fused step, fewer warps run
-// faster once HBM is saturated, unless the selection needs them (DeMo from
-// k = 7 on, and the ternary format's ballots); Striding runs best with all.
-int encode_warps(int mode, int k, int wire) {
+// the T5-base shard with float32 and the OLMo-shaped shard with bfloat16
+// gradients): as in the fused step, fewer warps run faster once HBM is
+// saturated, unless the selection needs them (DeMo from k = 7 on, the ternary
+// format's ballots); bfloat16 gradients bring less data per tile for the same
+// compute, so they take more warps.
+int encode_warps(int mode, int k, int wire, bool bf16) {
   if (mode == kModeDemo) {
     if (wire == kWireTernary) return kStepWarps;
+    if (bf16) return k == 1 ? kStepWarpsMid : kStepWarps;
     if (k == 1) return kStepWarpsLight;
     return k <= 6 ? kStepWarpsMid : kStepWarps;
   }
-  if (mode == kModeStride) return kStepWarps;
-  return kStepWarpsMid;
+  if (mode == kModeRandom) return bf16 ? kStepWarps : kStepWarpsMid;
+  if (mode == kModeStride) return bf16 ? kStepWarpsLight : kStepWarps;
+  return bf16 ? kStepWarpsLight : kStepWarpsMid;
 }
 
 template <int WARPS>

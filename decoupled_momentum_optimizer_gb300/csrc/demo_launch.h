@@ -1,0 +1,80 @@
+// Parameter blocks and launchers of the split-path kernels (encode, decode) and
+// of the Decoupled AdamW step.
+#pragma once
+
+#include "demo_params.h"
+
+namespace demo {
+
+struct EncodeParams {
+  CUtensorMap g;
+  CUtensorMap m;
+  float* m_ptr;
+  void* vals;  // wire-format payload values
+  void* idx;   // DeMo indices (uint8 [nc][k], or uint32 bit-planes for the ternary format)
+  long long nc, ntiles;
+  long long chunk0;  // shard index of the first chunk (the Random scheme hashes shard chunk indices)
+  int k, sign, sync, wire;
+  int stride_o, stride_ns;
+  unsigned int stride_mask;
+  float beta;
+  unsigned long long hbase;
+  unsigned int* fault;
+};
+
+template <int MAXR>
+struct DecodeParams {
+  CUtensorMap theta;
+  float* theta_ptr;
+  const void* vals[MAXR];
+  const void* idx[MAXR];
+  long long nc, ntiles;
+  long long chunk0;  // shard index of the first chunk
+  int R, k, wire;
+  int stride_o, stride_ns;
+  // Payload staging: replicas 0..nstaged-1 have their per-tile spans (vspan bytes
+  // of values, ispan bytes of indices at tile t * span) copied to shared memory
+  // with the theta tile; the others, and a ragged last tile, are read directly.
+  int nstaged;
+  unsigned int vspan, ispan;
+  float lr, rcpR;
+  unsigned long long hbase;
+  float rcp_tab[kMaxReplicas + 1];
+  unsigned int* fault;
+};
+
+// Shared-memory staging per decode slot for the replicas' payload spans: 2 KB
+// with 11 warps per SM, or 3 KB with 10 warps when the replicas fit only that.
+constexpr int kDecStageBytes = 2048;
+constexpr int kDecStageBytesWide = 3072;
+constexpr int kDecWarpsWide = 10;
+
+// Decoupled AdamW (elementwise, grid-stride over groups of four parameters).
+struct AdamWParams {
+  float* theta;
+  const void* g[kMaxReplicas];
+  float* m[kMaxReplicas];
+  float* v[kMaxReplicas];
+  long long n4;  // n / 4
+  int R;
+  float beta1, beta2, omb1, omb2;  // beta and 1 - beta (exact in float32)
+  float rbc1, rbc2;                // 1 / (1 - beta^t), t = step + 1
+  float eps, lr, wd, rcpR;
+};
+
+cudaError_t launch_adamw(const AdamWParams& p, bool bf16, int grid, cudaStream_t st);
+
+// The encode and decode kernels run kStepWarps warps per CTA unless their own
+// selection says otherwise (encode_warps, and the decode's staging shape).
+int encode_warps(int mode, int k, int wire, bool bf16);
+cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps, int grid, cudaStream_t st);
+cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int grid,
+                                cudaStream_t st);
+cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int grid,
+                                cudaStream_t st);
+
+// Set the dynamic shared-memory limit of every encode and decode kernel instantiation.
+cudaError_t prepare_encode_kernels();
+cudaError_t prepare_decode_kernels();
+
+}  // namespace demo

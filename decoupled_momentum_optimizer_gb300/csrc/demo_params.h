@@ -1,5 +1,6 @@
-// Kernel parameter blocks and launcher declarations of the DeMo shard step.
-// Tensor maps travel by value as __grid_constant__ kernel parameters.
+// The fused step kernel's parameter block and launchers, and the constants all
+// kernels share.  Tensor maps travel by value as __grid_constant__ kernel
+// parameters.  The split-path and AdamW kernels' blocks are in demo_launch.h.
 #pragma once
 
 #include <cuda.h>
@@ -31,66 +32,8 @@ struct StepParams {
   unsigned int* fault;
 };
 
-struct EncodeParams {
-  CUtensorMap g;
-  CUtensorMap m;
-  float* m_ptr;
-  void* vals;  // wire-format payload values
-  void* idx;   // DeMo indices (uint8 [nc][k], or uint32 bit-planes for the ternary format)
-  long long nc, ntiles;
-  long long chunk0;  // shard index of the first chunk (the Random scheme hashes shard chunk indices)
-  int k, sign, sync, wire;
-  int stride_o, stride_ns;
-  unsigned int stride_mask;
-  float beta;
-  unsigned long long hbase;
-  unsigned int* fault;
-};
-
-template <int MAXR>
-struct DecodeParams {
-  CUtensorMap theta;
-  float* theta_ptr;
-  const void* vals[MAXR];
-  const void* idx[MAXR];
-  long long nc, ntiles;
-  long long chunk0;  // shard index of the first chunk
-  int R, k, wire;
-  int stride_o, stride_ns;
-  // Payload staging: replicas 0..nstaged-1 have their per-tile spans (vspan bytes
-  // of values, ispan bytes of indices at tile t * span) copied to shared memory
-  // with the theta tile; the others, and a ragged last tile, are read directly.
-  int nstaged;
-  unsigned int vspan, ispan;
-  float lr, rcpR;
-  unsigned long long hbase;
-  float rcp_tab[kMaxReplicas + 1];
-  unsigned int* fault;
-};
-
-// Shared-memory staging per decode slot for the replicas' payload spans: 2 KB
-// with 11 warps per SM, or 3 KB with 10 warps when the replicas fit only that.
-constexpr int kDecStageBytes = 2048;
-constexpr int kDecStageBytesWide = 3072;
-constexpr int kDecWarpsWide = 10;
-
-// Decoupled AdamW (elementwise, grid-stride over groups of four parameters).
-struct AdamWParams {
-  float* theta;
-  const void* g[kMaxReplicas];
-  float* m[kMaxReplicas];
-  float* v[kMaxReplicas];
-  long long n4;  // n / 4
-  int R;
-  float beta1, beta2, omb1, omb2;  // beta and 1 - beta (exact in float32)
-  float rbc1, rbc2;                // 1 / (1 - beta^t), t = step + 1
-  float eps, lr, wd, rcpR;
-};
-
-cudaError_t launch_adamw(const AdamWParams& p, bool bf16, int grid, cudaStream_t st);
-
-// Launchers (one per translation unit).  `grid` CTAs of W warps (kStepWarps for
-// the encode and decode kernels); each warp walks the tiles gw, gw + W * grid, ...
+// Launchers (one per translation unit; the other kernels' are in demo_launch.h).
+// `grid` CTAs of W warps; each warp walks the tiles gw, gw + W * grid, ...
 //
 // The fused step kernel is built for three resident warp counts per SM.  Its
 // data stream per item is fixed, its compute per item is not (Striding and
@@ -106,16 +49,8 @@ cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, boo
                               cudaStream_t st);
 cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int warps, int grid,
                               cudaStream_t st);
-int encode_warps(int mode, int k, int wire);
-cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps, int grid, cudaStream_t st);
-cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int grid,
-                                cudaStream_t st);
-cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int grid,
-                                cudaStream_t st);
 
-// Set the dynamic shared-memory limit of every kernel instantiation.
+// Set the dynamic shared-memory limit of every step kernel instantiation.
 cudaError_t prepare_step_kernels();
-cudaError_t prepare_encode_kernels();
-cudaError_t prepare_decode_kernels();
 
 }  // namespace demo
