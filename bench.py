@@ -171,9 +171,33 @@ def src_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decoupled_momentum_optimizer_gb300", "csrc")
     for f in STEP_KERNEL_SOURCES:
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(strip_comments(open(os.path.join(csrc, f)).read()).encode())
     h.update(" ".join(f for f in build.NVCC_FLAGS if not os.path.isabs(f)).encode())
     return h.hexdigest()[:16]
+
+
+def strip_comments(src):
+    """C/C++ source without its comments and trailing blanks (string and character literals kept),
+    so that editing a comment does not change the source hash."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
 
 
 def ncu_traffic(workload, mode, k, R):

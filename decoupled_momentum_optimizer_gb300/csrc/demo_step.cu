@@ -14,9 +14,11 @@
 // swizzled tile, the warp reads it back transposed and issues 512-byte
 // coalesced stores, and the slot is immediately refilled with the load for
 // item i + 2.  Shared memory per warp is 20 KB (two 8 KB slots and a 4 KB
-// payload accumulator), so 11 warps fit on an SM.  With a 16-bit wire format
-// the accumulated values are rounded exactly as the split path's receiver
-// rounds them, so fused and split results stay bit-identical.
+// payload accumulator), so up to 11 warps fit on an SM; the kernel is built for
+// 6, 8 and 11 and the launch takes the fewest that cover the item's compute
+// (step_warps).  With a 16-bit wire format the accumulated values are rounded
+// exactly as the split path's receiver rounds them, so fused and split results
+// stay bit-identical.
 #include "demo_common.cuh"
 #include "demo_params.h"
 
