@@ -166,16 +166,16 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
 // Which replicas' payloads the decode kernel stages through shared memory, and
 // the CTA shape that goes with it (returns its warp count).  The spans of one
 // 32-chunk tile must be 16-byte multiples (so every tile's span starts 16-byte
-// aligned in a 16-byte aligned buffer).  When every replica fits the 2 KB
-// staging area the decode runs 11 warps; when they fit only 3 KB it runs 10
-// warps with 3 KB (measured faster than staging some replicas); otherwise the
-// leading replicas that fit 2 KB are staged and the others read directly.
-// DiLoCo payloads (4 KB of float32 per tile and replica) are always read directly.
+// aligned in a 16-byte aligned buffer).  The shape with the most warps whose
+// staging holds every replica is taken (measured faster than staging only some
+// with more warps); when none holds them all, 11 warps stage the leading
+// replicas that fit 2 KB and read the others directly.  DiLoCo payloads (4 KB
+// of float32 per tile and replica) are always read directly.
 template <class P>
 int stage_payloads(P& p, int mode, int k, int wire, int R) {
   p.nstaged = 0;
   p.vspan = p.ispan = 0;
-  if (mode == DEMO_MODE_DILOCO) return kStepWarps;
+  if (mode == DEMO_MODE_DILOCO) return kDecShapes[0];
   const bool demo = mode == DEMO_MODE_DEMO;
   size_t vs, is;
   if (wire == DEMO_WIRE_TERNARY) {
@@ -186,14 +186,20 @@ int stage_payloads(P& p, int mode, int k, int wire, int R) {
     is = demo ? 32 * static_cast<size_t>(k) : 0;    // uint8 [chunk][k]
   }
   const size_t span = vs + is;
-  if (vs % 16 || is % 16 || span > static_cast<size_t>(kDecStageBytes)) return kStepWarps;
+  const size_t small = static_cast<size_t>(dec_stage_bytes(kDecShapes[0]));
+  if (vs % 16 || is % 16 || span > small) return kDecShapes[0];
   int aligned = 0;  // leading replicas with 16-byte aligned buffers
   while (aligned < R && aligned16(p.vals[aligned]) && (!demo || aligned16(p.idx[aligned]))) ++aligned;
-  int warps = kStepWarps;
-  int ns = static_cast<int>(std::min<size_t>(aligned, kDecStageBytes / span));
-  if (ns < R && aligned == R && R * span <= static_cast<size_t>(kDecStageBytesWide)) {
-    warps = kDecWarpsWide;
-    ns = R;
+  int warps = kDecShapes[0];
+  int ns = static_cast<int>(std::min<size_t>(aligned, small / span));
+  if (ns < R && aligned == R) {
+    for (int w : kDecShapes) {
+      if (R * span <= static_cast<size_t>(dec_stage_bytes(w))) {
+        warps = w;
+        ns = R;
+        break;
+      }
+    }
   }
   p.nstaged = ns;
   p.vspan = static_cast<unsigned int>(vs);

@@ -34,15 +34,17 @@ struct alignas(1024) DecWarpSmem {
   unsigned char stage[2][STAGE];          // slot s: staged payload spans, replica r at r * (vspan + ispan)
 };
 
-// Two CTA shapes: 11 warps with 2 KB of staging per slot, or 10 warps with 3 KB
-// (for payloads whose replicas fit 3 KB but not 2 KB); both fill the SM's shared memory.
-__host__ __device__ constexpr int dec_stage(int warps) { return warps == kStepWarps ? kDecStageBytes : kDecStageBytesWide; }
+// Dynamic shared memory of a decode CTA of `warps` warps (see dec_stage_bytes).
 constexpr size_t dec_smem(int warps) {
-  return 1024 + warps * (2 * 4096 + 8 * 1024 + 2 * dec_stage(warps)) + warps * 16 + 272;
+  return 1024 + warps * (2 * 4096 + 8 * 1024 + 2 * dec_stage_bytes(warps)) + warps * 16 + 272;
 }
-static_assert(sizeof(DecWarpSmem<kDecStageBytes>) == 2 * 4096 + 8 * 1024 + 2 * kDecStageBytes, "layout");
-static_assert(sizeof(DecWarpSmem<kDecStageBytesWide>) == 2 * 4096 + 8 * 1024 + 2 * kDecStageBytesWide, "layout");
-static_assert(dec_smem(kStepWarps) <= 232448 && dec_smem(kDecWarpsWide) <= 232448, "shared memory per CTA");
+template <int W>
+constexpr bool dec_shape_fits() {
+  return sizeof(DecWarpSmem<dec_stage_bytes(W)>) == 2 * 4096 + 8 * 1024 + 2 * dec_stage_bytes(W) &&
+         dec_smem(W) <= 232448;
+}
+static_assert(dec_shape_fits<11>() && dec_shape_fits<10>() && dec_shape_fits<9>() && dec_shape_fits<8>(),
+              "decode shapes: layout and shared memory per CTA");
 
 __device__ __forceinline__ bool vector_kd(int k) { return k == 1 || k == 2 || k == 4 || k == 8; }
 
@@ -160,7 +162,7 @@ __device__ __forceinline__ void demo_accumulate(SumCount* acc, int lane, const v
 
 template <int MODE, int MAXR, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_constant__ DecodeParams<MAXR> p) {
-  using WarpSmem = DecWarpSmem<dec_stage(WARPS)>;
+  using WarpSmem = DecWarpSmem<dec_stage_bytes(WARPS)>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte aligned start (the TMA swizzle patterns are relative to 1024-byte boundaries),
   // derived by pointer arithmetic on the shared array so every access stays a shared-memory one
@@ -395,8 +397,10 @@ static cudaError_t launch_decode_w(const DecodeParams<MAXR>& p, int mode, int gr
 
 template <int MAXR>
 static cudaError_t launch_decode_t(const DecodeParams<MAXR>& p, int mode, int warps, int grid, cudaStream_t st) {
-  if (warps == kStepWarps) return launch_decode_w<MAXR, kStepWarps>(p, mode, grid, st);
-  if (warps == kDecWarpsWide) return launch_decode_w<MAXR, kDecWarpsWide>(p, mode, grid, st);
+  if (warps == 11) return launch_decode_w<MAXR, 11>(p, mode, grid, st);
+  if (warps == 10) return launch_decode_w<MAXR, 10>(p, mode, grid, st);
+  if (warps == 9) return launch_decode_w<MAXR, 9>(p, mode, grid, st);
+  if (warps == 8) return launch_decode_w<MAXR, 8>(p, mode, grid, st);
   return cudaErrorInvalidValue;
 }
 
@@ -429,10 +433,14 @@ static cudaError_t prepare_w() {
 }
 
 cudaError_t prepare_decode_kernels() {
-  cudaError_t e = prepare_w<kSmallReplicas, kStepWarps>();
-  if (e == cudaSuccess) e = prepare_w<kSmallReplicas, kDecWarpsWide>();
-  if (e == cudaSuccess) e = prepare_w<kMaxReplicas, kStepWarps>();
-  if (e == cudaSuccess) e = prepare_w<kMaxReplicas, kDecWarpsWide>();
+  cudaError_t e = prepare_w<kSmallReplicas, 11>();
+  if (e == cudaSuccess) e = prepare_w<kSmallReplicas, 10>();
+  if (e == cudaSuccess) e = prepare_w<kSmallReplicas, 9>();
+  if (e == cudaSuccess) e = prepare_w<kSmallReplicas, 8>();
+  if (e == cudaSuccess) e = prepare_w<kMaxReplicas, 11>();
+  if (e == cudaSuccess) e = prepare_w<kMaxReplicas, 10>();
+  if (e == cudaSuccess) e = prepare_w<kMaxReplicas, 9>();
+  if (e == cudaSuccess) e = prepare_w<kMaxReplicas, 8>();
   return e;
 }
 

@@ -43,11 +43,14 @@ struct DecodeParams {
   unsigned int* fault;
 };
 
-// Shared-memory staging per decode slot for the replicas' payload spans: 2 KB
-// with 11 warps per SM, or 3 KB with 10 warps when the replicas fit only that.
-constexpr int kDecStageBytes = 2048;
-constexpr int kDecStageBytesWide = 3072;
-constexpr int kDecWarpsWide = 10;
+// Decode CTA shapes: warps per SM and the shared-memory staging per slot for the
+// replicas' payload spans (each shape fills the SM's shared memory).  The launch
+// takes the shape with the most warps whose staging holds every replica's span;
+// when none does, 11 warps stage the replicas that fit 2 KB.
+__host__ __device__ constexpr int dec_stage_bytes(int warps) {
+  return warps >= 11 ? 2048 : warps == 10 ? 3072 : warps == 9 ? 4608 : 6144;
+}
+constexpr int kDecShapes[] = {11, 10, 9, 8};
 
 // Decoupled AdamW (elementwise, grid-stride over groups of four parameters).
 struct AdamWParams {
