@@ -76,7 +76,8 @@ def lib():
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with python -m decoupled_momentum_optimizer_gb300.build")
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "python -m decoupled_momentum_optimizer_gb300.build")
         try:  # load the CUDA runtime the way torch does, so both share one runtime
             import torch  # noqa: F401
         except ImportError:  # pragma: no cover
@@ -101,7 +102,9 @@ def init(device=None):
 
     if device is None:
         device = torch.cuda.current_device()
-    device = torch.device("cuda", device).index if not isinstance(device, int) else device
+    elif not isinstance(device, int):
+        device = torch.device(device)
+        device = device.index if device.index is not None else torch.cuda.current_device()
     if device not in _inited:
         _check(lib().demo_init(device), "demo_init")
         _inited.add(device)
@@ -117,13 +120,15 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _ptr(t, dtypes, name, n=None):
+def _ptr(t, dtypes, name, n=None, device=None):
     import torch
 
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be on a CUDA device (there is no CPU path)")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the call's other tensors on {device}")
     if t.dtype not in dtypes:
         raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
     if not t.is_contiguous():
@@ -131,6 +136,27 @@ def _ptr(t, dtypes, name, n=None):
     if n is not None and t.numel() != n:
         raise ValueError(f"{name} has {t.numel()} elements, expected {n}")
     return t.data_ptr()
+
+
+class _OnDevice:
+    """Makes the tensors' device current for a library call (the library launches on the
+    current device) and initialises the library there."""
+
+    def __init__(self, device):
+        import torch
+
+        if device.type != "cuda":
+            raise ValueError(f"tensors are on {device}: the library runs on CUDA devices only (there is no CPU path)")
+        self._ctx = torch.cuda.device(device)
+        self.device = device
+
+    def __enter__(self):
+        self._ctx.__enter__()
+        init(self.device.index)
+        return self
+
+    def __exit__(self, *exc):
+        return self._ctx.__exit__(*exc)
 
 
 def _grad_dtype(g):
@@ -187,15 +213,16 @@ def encode(g, m, vals, idx=None, *, k, beta, mode="demo", sign=True, diloco_peri
     """One replica's encode (demo_encode_wire): updates m in place, writes vals (and idx for DeMo)."""
     import torch
 
-    init(m.device.index)
-    n = m.numel()
-    w = _wire(wire)
-    gp = _ptr(g, (torch.float32, torch.bfloat16), "g", n)
-    mp = _ptr(m, (torch.float32,), "m", n)
-    vp = _ptr(vals, _val_dtypes(w), "vals") if vals is not None else None
-    ip = _ptr(idx, _idx_dtypes(w), "idx") if idx is not None else None
-    _check(lib().demo_encode_wire(gp, _grad_dtype(g), mp, n, CHUNK, k, beta, _mode(mode), int(bool(sign)),
-                                  diloco_period, seed, step, w, vp, ip, _stream(stream)), "demo_encode")
+    dev = m.device
+    with _OnDevice(dev):
+        n = m.numel()
+        w = _wire(wire)
+        gp = _ptr(g, (torch.float32, torch.bfloat16), "g", n, device=dev)
+        mp = _ptr(m, (torch.float32,), "m", n, device=dev)
+        vp = _ptr(vals, _val_dtypes(w), "vals", device=dev) if vals is not None else None
+        ip = _ptr(idx, _idx_dtypes(w), "idx", device=dev) if idx is not None else None
+        _check(lib().demo_encode_wire(gp, _grad_dtype(g), mp, n, CHUNK, k, beta, _mode(mode), int(bool(sign)),
+                                      diloco_period, seed, step, w, vp, ip, _stream(stream)), "demo_encode")
 
 
 def decode_update(theta, vals, idx=None, *, k, lr, mode="demo", diloco_period=8, seed=0, step=0, wire="f32",
@@ -203,17 +230,18 @@ def decode_update(theta, vals, idx=None, *, k, lr, mode="demo", diloco_period=8,
     """Scatter-mean of the R payloads in ``vals`` (and ``idx``) and theta -= lr Q (demo_decode_update_wire)."""
     import torch
 
-    init(theta.device.index)
-    n = theta.numel()
-    R = len(vals)
-    w = _wire(wire)
-    tp = _ptr(theta, (torch.float32,), "theta", n)
-    varr = (ctypes.c_void_p * R)(*[_ptr(v, _val_dtypes(w), f"vals[{r}]") for r, v in enumerate(vals)])
-    iarr = None
-    if idx is not None:
-        iarr = (ctypes.c_void_p * R)(*[_ptr(i, _idx_dtypes(w), f"idx[{r}]") for r, i in enumerate(idx)])
-    _check(lib().demo_decode_update_wire(tp, n, CHUNK, k, lr, _mode(mode), R, varr, iarr, diloco_period, seed, step,
-                                         w, _stream(stream)), "demo_decode_update")
+    dev = theta.device
+    with _OnDevice(dev):
+        n = theta.numel()
+        R = len(vals)
+        w = _wire(wire)
+        tp = _ptr(theta, (torch.float32,), "theta", n, device=dev)
+        varr = (ctypes.c_void_p * R)(*[_ptr(v, _val_dtypes(w), f"vals[{r}]", device=dev) for r, v in enumerate(vals)])
+        iarr = None
+        if idx is not None:
+            iarr = (ctypes.c_void_p * R)(*[_ptr(i, _idx_dtypes(w), f"idx[{r}]", device=dev) for r, i in enumerate(idx)])
+        _check(lib().demo_decode_update_wire(tp, n, CHUNK, k, lr, _mode(mode), R, varr, iarr, diloco_period, seed, step,
+                                             w, _stream(stream)), "demo_decode_update")
 
 
 def step(theta, gs, ms, *, k, beta, lr, mode="demo", sign=True, diloco_period=8, seed=0, step=0, wire="f32",
@@ -221,17 +249,20 @@ def step(theta, gs, ms, *, k, beta, lr, mode="demo", sign=True, diloco_period=8,
     """The fused shard step over R replicas (demo_step_wire); theta and every m_r update in place."""
     import torch
 
-    init(theta.device.index)
-    n = theta.numel()
-    R = len(ms)
-    if len(gs) != R:
-        raise ValueError("need one gradient per replica")
-    tp = _ptr(theta, (torch.float32,), "theta", n)
-    gd = _grad_dtype(gs[0])
-    garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n) for r, g in enumerate(gs)])
-    marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n) for r, m in enumerate(ms)])
-    _check(lib().demo_step_wire(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr, gd, marr,
-                                diloco_period, seed, step, _wire(wire), _stream(stream)), "demo_step")
+    dev = theta.device
+    with _OnDevice(dev):
+        n = theta.numel()
+        R = len(ms)
+        if len(gs) != R:
+            raise ValueError("need one gradient per replica")
+        tp = _ptr(theta, (torch.float32,), "theta", n, device=dev)
+        gd = _grad_dtype(gs[0])
+        garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n, device=dev)
+                                       for r, g in enumerate(gs)])
+        marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n, device=dev)
+                                       for r, m in enumerate(ms)])
+        _check(lib().demo_step_wire(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr, gd, marr,
+                                    diloco_period, seed, step, _wire(wire), _stream(stream)), "demo_step")
 
 
 def step_pipelined(theta, gs, ms, send, recv, *, k, beta, lr, mode="demo", sign=True, diloco_period=8, seed=0,
@@ -242,26 +273,29 @@ def step_pipelined(theta, gs, ms, send, recv, *, k, beta, lr, mode="demo", sign=
     """
     import torch
 
-    init(theta.device.index)
-    n = theta.numel()
-    R = len(ms)
-    w = _wire(wire)
-    tp = _ptr(theta, (torch.float32,), "theta", n)
-    garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n) for r, g in enumerate(gs)])
-    marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n) for r, m in enumerate(ms)])
+    dev = theta.device
+    with _OnDevice(dev):
+        n = theta.numel()
+        R = len(ms)
+        w = _wire(wire)
+        tp = _ptr(theta, (torch.float32,), "theta", n, device=dev)
+        garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n, device=dev)
+                                       for r, g in enumerate(gs)])
+        marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n, device=dev)
+                                       for r, m in enumerate(ms)])
 
-    def arr(pairs, j, dts):
-        if pairs is None or pairs[0][j] is None:
-            return None
-        return (ctypes.c_void_p * R)(*[_ptr(pq[j], dts, "payload") for pq in pairs])
+        def arr(pairs, j, dts):
+            if pairs is None or pairs[0][j] is None:
+                return None
+            return (ctypes.c_void_p * R)(*[_ptr(pq[j], dts, "payload", device=dev) for pq in pairs])
 
-    sv, si = arr(send, 0, _val_dtypes(w)), arr(send, 1, _idx_dtypes(w))
-    rv, ri = arr(recv, 0, _val_dtypes(w)), arr(recv, 1, _idx_dtypes(w))
-    cs = _stream(stream)
-    xs = _stream(comm_stream) if comm_stream is not None else cs
-    _check(lib().demo_step_pipelined(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr,
-                                     _grad_dtype(gs[0]), marr, diloco_period, seed, step, w, sv, si, rv, ri, blocks,
-                                     cs, xs), "demo_step_pipelined")
+        sv, si = arr(send, 0, _val_dtypes(w)), arr(send, 1, _idx_dtypes(w))
+        rv, ri = arr(recv, 0, _val_dtypes(w)), arr(recv, 1, _idx_dtypes(w))
+        cs = _stream(stream)
+        xs = _stream(comm_stream) if comm_stream is not None else cs
+        _check(lib().demo_step_pipelined(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr,
+                                         _grad_dtype(gs[0]), marr, diloco_period, seed, step, w, sv, si, rv, ri, blocks,
+                                         cs, xs), "demo_step_pipelined")
 
 
 def step_pipelined_static(theta, gs, ms, *, k, beta, lr, mode="demo", sign=True, diloco_period=8, seed=0, step=0,
@@ -274,34 +308,41 @@ def step_pipelined_static(theta, gs, ms, *, k, beta, lr, mode="demo", sign=True,
     """
     import torch
 
-    init(theta.device.index)
-    n = theta.numel()
-    R = len(ms)
-    tp = _ptr(theta, (torch.float32,), "theta", n)
-    garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n) for r, g in enumerate(gs)])
-    marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n) for r, m in enumerate(ms)])
-    cs = _stream(stream)
-    xs = _stream(comm_stream) if comm_stream is not None else cs
-    _check(lib().demo_step_pipelined_static(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr,
-                                            _grad_dtype(gs[0]), marr, diloco_period, seed, step, _wire(wire), blocks,
-                                            cs, xs), "demo_step_pipelined_static")
+    dev = theta.device
+    with _OnDevice(dev):
+        n = theta.numel()
+        R = len(ms)
+        tp = _ptr(theta, (torch.float32,), "theta", n, device=dev)
+        garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n, device=dev)
+                                       for r, g in enumerate(gs)])
+        marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n, device=dev)
+                                       for r, m in enumerate(ms)])
+        cs = _stream(stream)
+        xs = _stream(comm_stream) if comm_stream is not None else cs
+        _check(lib().demo_step_pipelined_static(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr,
+                                                _grad_dtype(gs[0]), marr, diloco_period, seed, step, _wire(wire),
+                                                blocks, cs, xs), "demo_step_pipelined_static")
 
 
 def adamw_step(theta, gs, ms, vs, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, step=0, stream=None):
     """One Decoupled AdamW step (demo_adamw_step): theta, every m_r and v_r update in place."""
     import torch
 
-    init(theta.device.index)
-    n = theta.numel()
-    R = len(ms)
-    if len(gs) != R or len(vs) != R:
-        raise ValueError("need one gradient, first and second moment per replica")
-    tp = _ptr(theta, (torch.float32,), "theta", n)
-    garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n) for r, g in enumerate(gs)])
-    marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n) for r, m in enumerate(ms)])
-    varr = (ctypes.c_void_p * R)(*[_ptr(v, (torch.float32,), f"v[{r}]", n) for r, v in enumerate(vs)])
-    _check(lib().demo_adamw_step(tp, n, beta1, beta2, eps, lr, weight_decay, R, garr, _grad_dtype(gs[0]), marr, varr,
-                                 step, _stream(stream)), "demo_adamw_step")
+    dev = theta.device
+    with _OnDevice(dev):
+        n = theta.numel()
+        R = len(ms)
+        if len(gs) != R or len(vs) != R:
+            raise ValueError("need one gradient, first and second moment per replica")
+        tp = _ptr(theta, (torch.float32,), "theta", n, device=dev)
+        garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n, device=dev)
+                                       for r, g in enumerate(gs)])
+        marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n, device=dev)
+                                       for r, m in enumerate(ms)])
+        varr = (ctypes.c_void_p * R)(*[_ptr(v, (torch.float32,), f"v[{r}]", n, device=dev)
+                                       for r, v in enumerate(vs)])
+        _check(lib().demo_adamw_step(tp, n, beta1, beta2, eps, lr, weight_decay, R, garr, _grad_dtype(gs[0]), marr,
+                                     varr, step, _stream(stream)), "demo_adamw_step")
 
 
 def validate_payload(idx_host, n, k, wire="f32"):

@@ -193,3 +193,23 @@ def test_adamw_argument_checks(L):
     assert L.demo_adamw_step(p(0x400004), 64, 0.9, 0.999, 1e-8, 1e-3, 0.0, 1, g, 0, m, v, 0, None) == EALIGN
     same = (ctypes.c_void_p * 1)(0x200000)
     assert L.demo_adamw_step(th, 64, 0.9, 0.999, 1e-8, 1e-3, 0.0, 1, g, 0, m, same, 0, None) == EINVAL
+
+
+def test_binding_refuses_cpu_tensors():
+    """The Python entry points fail loudly on CPU tensors: there is no CPU path."""
+    import torch
+
+    import decoupled_momentum_optimizer_gb300 as dm
+
+    n = 64
+    th, m, g, v = (torch.zeros(n) for _ in range(4))
+    calls = [
+        lambda: dm.step(th, [g], [m], k=4, beta=0.9, lr=0.1),
+        lambda: dm.encode(g, m, torch.zeros(8), torch.zeros(8, dtype=torch.uint8), k=4, beta=0.9),
+        lambda: dm.decode_update(th, [torch.zeros(8)], [torch.zeros(8, dtype=torch.uint8)], k=4, lr=0.1),
+        lambda: dm.adamw_step(th, [g], [m], [v], lr=1e-3),
+        lambda: dm.step_pipelined_static(th, [g], [m], k=4, beta=0.9, lr=0.1),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError, match="no CPU path"):
+            call()

@@ -292,6 +292,17 @@ def test_decode_repeated_indices_count_every_entry():
     assert err.max() < 1e-5, err.max()
 
 
+def test_binding_refuses_mixed_devices():
+    """A call whose tensors are not all on one CUDA device is refused before any launch."""
+    n = 32 * 64
+    theta = cuda_normal(n, 2e-2, 1)
+    g = cuda_normal(n, 1e-3, 2)
+    with pytest.raises(ValueError):
+        dm.step(theta, [g], [torch.zeros(n)], k=4, beta=0.9, lr=0.1)
+    with pytest.raises(ValueError):
+        dm.step(theta.cpu(), [g], [torch.zeros(n, device="cuda")], k=4, beta=0.9, lr=0.1)
+
+
 def test_guard_bands_untouched():
     n = 32 * (64 + 5)
     pad = 4096 // 4
