@@ -114,7 +114,7 @@ enum demo_status {
 /*
  * demo_init -- prepare the library for `device` and make it current.
  * Checks that the device is compute capability 10.3 (GB300), resolves the
- * tensor-map encoder from the driver and sets the kernels' shared-memory
+ * tensor-map encoder from the CUDA driver and sets the kernels' shared-memory
  * limits.  Idempotent; call it once per device before the other calls (and
  * before any stream capture).  Returns DEMO_OK, DEMO_ENODEV or DEMO_ECUDA.
  */

@@ -1,7 +1,7 @@
 """Parity harness: the CUDA library against the float64 oracle, step by step.
 
 Every check is teacher-forced: the oracle takes one step from the GPU's own
-float32 state (promoted exactly to float64), so each step is judged on its own.
+float32 state (promoted exactly to float64), so each step is checked on its own.
 For each step the harness
 
 * runs the split path (demo_encode per replica, demo_decode_update) and the
