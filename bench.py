@@ -215,55 +215,60 @@ def ncu_traffic(workload, mode, k, R):
     return None
 
 
-def cpu_baseline(wl_name, mode, k, sign, R, seconds=10.0):
-    """Time the float64 oracle in a fresh process on a sample of the workload: one thread
-    (the reported value) and, beside it, with every host core available to BLAS."""
-    code = r"""
-import json, os, sys, time
+_ORACLE_TIMER = r"""
+import json, sys, time
 sys.path.insert(0, %r)
 import numpy as np
 import oracle.demo_ref as ref
-mode, k, sign, R, budget = %r, %d, %r, %d, %f
-nc = 16384
+mode, k, sign, R, nc, budget, max_steps = %r, %d, %r, %d, %d, %f, %d
 n = nc * 32
 rng = np.random.default_rng(0)
 th = rng.standard_normal(n) * 2e-2
 ms = [np.zeros(n) for _ in range(R)]
-steps, t0 = 0, time.perf_counter()
-while True:
+steps, el = 0, 0.0
+for t in range(max_steps + 1):  # step 0 is an untimed warm-up
     gs = [rng.standard_normal(n).astype(np.float32).astype(np.float64) * 1e-3 for _ in range(R)]
     ts = time.perf_counter()
     th, ms, _ = ref.step(th, ms, gs, beta=0.999, lr=1e-3, k=k, mode=ref.__dict__["MODE_" + mode.upper()],
-                         sign=sign, step_idx=steps)
-    steps += 1
-    if steps == 1:
-        el = 0.0
-    el += time.perf_counter() - ts
-    if el >= budget or steps >= 1000:
-        break
+                         sign=sign, step_idx=t)
+    if t > 0:
+        el += time.perf_counter() - ts
+        steps += 1
+        if el >= budget:
+            break
 print(json.dumps({"params_per_s": n * steps / el, "steps": steps, "seconds": el, "sample_params": n}))
-""" % (ROOT, mode, k, sign, R, seconds)
-    def run(threads):
-        t = str(threads)
-        env = dict(os.environ, OPENBLAS_NUM_THREADS=t, OMP_NUM_THREADS=t, MKL_NUM_THREADS=t)
-        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
-        if r.returncode != 0:
-            return None, r.stderr[-300:]
-        return json.loads(r.stdout.strip().splitlines()[-1]), None
+"""
 
-    d, err = run(1)
+
+def oracle_time(mode, k, sign, R, nc, seconds, threads, max_steps=1000):
+    """Time the float64 oracle in a fresh process (BLAS/OpenMP threads = `threads`) on nc
+    chunks of synthetic input: one warm-up step, then steps until `seconds` or max_steps."""
+    code = _ORACLE_TIMER % (ROOT, mode, k, sign, R, nc, seconds, max_steps)
+    t = str(threads)
+    env = dict(os.environ, OPENBLAS_NUM_THREADS=t, OMP_NUM_THREADS=t, MKL_NUM_THREADS=t)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return None, r.stderr[-300:]
+    return json.loads(r.stdout.strip().splitlines()[-1]), None
+
+
+def cpu_baseline(wl_name, mode, k, sign, R, seconds=10.0):
+    """Time the float64 oracle in a fresh process on a sample of the workload: one thread
+    (the reported value) and, beside it, with every host core available to BLAS."""
+    nc = 16384
+    d, err = oracle_time(mode, k, sign, R, nc, seconds, 1)
     if d is None:
         return {"value": None, "unit": "params/s", "cores": 1, "kind": "oracle", "error": err}
     out = {"value": d["params_per_s"], "unit": "params/s", "cores": 1, "kind": "oracle",
-           "sample": f"{d['sample_params']} params (16384 chunks) of the {wl_name} workload, {mode} k={k} "
-                     f"sign={int(sign)} R={R}, {d['steps']} steps in {d['seconds']:.1f} s, "
-                     f"float64 numpy, one thread (BLAS threads = 1)",
+           "sample": f"{d['sample_params']} params ({nc} chunks) of the {wl_name} workload, {mode} k={k} "
+                     f"sign={int(sign)} R={R}, {d['steps']} timed steps in {d['seconds']:.1f} s after one "
+                     f"warm-up step, float64 numpy, one thread (BLAS threads = 1)",
            "host": host_cpu()}
     ncpu = os.cpu_count() or 1
     if ncpu > 1:
         # the same sample with every host core available to BLAS (the oracle's elementwise
         # numpy work stays on one thread, so this is its best case on this host)
-        d2, _ = run(ncpu)
+        d2, _ = oracle_time(mode, k, sign, R, nc, seconds, ncpu)
         if d2 is not None:
             out["all_cores"] = {"value": d2["params_per_s"], "cores": ncpu, "steps": d2["steps"],
                                 "seconds": round(d2["seconds"], 2)}
@@ -818,6 +823,20 @@ def run_sweep(args):
               + (f"  split {rec['split_ms']:8.3f} ms {rec['split_gbs']:7.0f} GB/s" if "split_ms" in rec else ""),
               flush=True)
     f.close()
+    # the float64 oracle on the host cores, on whole shards: the 65,536-parameter shard for its
+    # five steps and a 2^20 shard for three, with one BLAS thread and with every core
+    ncpu = os.cpu_count() or 1
+    for name, nc, steps in (("flat64k", 2048, 5), ("flat1048576", 32768, 3)):
+        for threads in sorted({1, ncpu}):
+            d, err = oracle_time("demo", 4, True, 2, nc, 1e9, threads, max_steps=steps)
+            rec = {"oracle": True, "workload": name, "n": nc * 32, "mode": "demo", "k": 4, "sign": True, "R": 2,
+                   "threads": threads, "host": host_cpu()}
+            rec.update(d if d is not None else {"error": err})
+            f.write(json.dumps(rec) + "\n")
+            f.flush()
+            if d is not None:
+                print(f"{name:16s} oracle {threads:3d} threads  {d['params_per_s']:10.3g} params/s "
+                      f"({d['steps']} steps, {d['seconds']:.2f} s)", flush=True)
     print(json.dumps({"sweep": args.sweep, "device_fault": dm.device_fault()}))
     return 0
 
