@@ -822,7 +822,6 @@ def run_sweep(args):
               f"{rec['fused_gbs']:7.0f} GB/s {100 * rec['fused_frac']:5.1f}%"
               + (f"  split {rec['split_ms']:8.3f} ms {rec['split_gbs']:7.0f} GB/s" if "split_ms" in rec else ""),
               flush=True)
-    f.close()
     # the float64 oracle on the host cores, on whole shards: the 65,536-parameter shard for its
     # five steps and a 2^20 shard for three, with one BLAS thread and with every core
     ncpu = os.cpu_count() or 1
@@ -837,6 +836,7 @@ def run_sweep(args):
             if d is not None:
                 print(f"{name:16s} oracle {threads:3d} threads  {d['params_per_s']:10.3g} params/s "
                       f"({d['steps']} steps, {d['seconds']:.2f} s)", flush=True)
+    f.close()
     print(json.dumps({"sweep": args.sweep, "device_fault": dm.device_fault()}))
     return 0
 
