@@ -94,6 +94,43 @@ def test_flat64k_demo_free_running():
     assert excl.sum() <= len(excl) // 100
 
 
+@pytest.mark.parametrize("mode,k,sign,period", [("demo", 4, False, 8), ("random", 8, True, 8),
+                                                ("random", 1, False, 8), ("stride", 4, True, 8),
+                                                ("diloco", 1, True, 2)])
+def test_flat64k_free_running_other_schemes(mode, k, sign, period):
+    """Five free-running GPU steps against five oracle steps for the other schemes and for
+    unsigned DeMo: theta's update and every m within 1e-5 per chunk."""
+    from parity import chunk_close
+
+    wl = W.workload("flat64k")
+    n, R = wl.n, wl.R
+    theta0 = W.make_theta0(wl, "cpu")
+    streams = [W.GradStream(wl, r, "cpu") for r in range(R)]
+    theta = theta0.cuda()
+    ms = [torch.zeros(n, device="cuda") for _ in range(R)]
+    th_o, ms_o = f64(theta0), [np.zeros(n) for _ in range(R)]
+    excl = np.zeros(n // C, dtype=bool)
+    for t in range(wl.steps):
+        gs = [s.next() for s in streams]
+        theta, ms = gpu_fused(theta, ms, [g.cuda() for g in gs], k=k, beta=wl.beta, lr=wl.lr, mode=mode,
+                              sign=sign, seed=4, step=t, period=period)
+        th_o, ms_o, info = ref.step(th_o, ms_o, [f64(g) for g in gs], beta=wl.beta, lr=wl.lr, k=k,
+                                    mode=ref.__dict__["MODE_" + mode.upper()], sign=sign, seed=4, step_idx=t,
+                                    period=period)
+        excl |= info["near_tie"]
+    torch.cuda.synchronize()
+    d_g = (f64(theta) - f64(theta0)).reshape(-1, C)
+    d_o = (th_o - f64(theta0)).reshape(-1, C)
+    slack = 5 * np.spacing(np.abs(f64(theta)).astype(np.float32)).reshape(-1, C)
+    bad = ((np.abs(d_g - d_o) > 1e-5 * np.abs(d_o).max(1, keepdims=True) + slack).any(1)) & ~excl
+    assert not bad.any(), f"delta theta differs in {bad.sum()} chunks"
+    for r in range(R):
+        bad, worst = chunk_close(f64(ms[r]), ms_o[r], 1e-5, excl)
+        assert not bad.any(), f"m[{r}] worst {worst}"
+    if mode != "demo":
+        assert not excl.any()  # positions do not depend on values: no near-ties to exclude
+
+
 # ----------------------------------------------------------------------------
 # Every mode, k, sign, R and gradient dtype on a ragged shard (31 tiles + 8 rows)
 # ----------------------------------------------------------------------------
