@@ -168,12 +168,15 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
 // 32-chunk tile must be 16-byte multiples (so every tile's span starts 16-byte
 // aligned in a 16-byte aligned buffer).  The shape with the most warps whose
 // staging holds every replica is taken (measured faster than staging only some
-// with more warps); when none holds them all, 11 warps stage the leading
-// replicas that fit 2 KB and read the others directly.  DiLoCo payloads (4 KB
-// of float32 per tile and replica) are always read directly.
+// with more warps).  When none holds them all, DeMo stages the replicas a group
+// at a time (the decode visits each full tile as one item per group), and the
+// other schemes stage the leading replicas that fit 2 KB and read the others
+// directly (in the real system they receive one all-reduced payload, not R).
+// DiLoCo payloads (4 KB of float32 per tile and replica) are always read directly.
 template <class P>
 int stage_payloads(P& p, int mode, int k, int wire, int R) {
   p.nstaged = 0;
+  p.group = 0;
   p.vspan = p.ispan = 0;
   if (mode == DEMO_MODE_DILOCO) return kDecShapes[0];
   const bool demo = mode == DEMO_MODE_DEMO;
@@ -199,6 +202,14 @@ int stage_payloads(P& p, int mode, int k, int wire, int R) {
         ns = R;
         break;
       }
+    }
+    // DeMo payloads that no shape holds whole (the receiver of an all_gather over many
+    // replicas): stage them a group at a time, one item per group, with the largest
+    // staging area (8 warps, 6 KB), so that each item moves as much as it can.
+    if (ns < R && demo) {
+      warps = kDecShapes[3];
+      p.group = static_cast<int>(static_cast<size_t>(dec_stage_bytes(warps)) / span);
+      ns = 0;
     }
   }
   p.nstaged = ns;
@@ -233,11 +244,13 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
   p.fault = st->fault;
   const int warps = stage_payloads(p, mode, k, wire, R);
   const int grid = grid_for(p.ntiles, st, warps);
+  const bool kv_ok = mode == DEMO_MODE_DEMO && wire != DEMO_WIRE_TERNARY && (k == 1 || k == 2 || k == 4 || k == 8);
+  const int kv = kv_ok ? k : 0;
   cudaError_t e;
   if constexpr (MAXR == kSmallReplicas) {
-    e = launch_decode_small(p, mode, warps, grid, stream);
+    e = launch_decode_small(p, mode, warps, kv, grid, stream);
   } else {
-    e = launch_decode_large(p, mode, warps, grid, stream);
+    e = launch_decode_large(p, mode, warps, kv, grid, stream);
   }
   return to_status(e);
 }

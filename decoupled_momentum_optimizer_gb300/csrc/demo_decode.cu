@@ -128,21 +128,50 @@ __device__ __forceinline__ void load_payload(const void* vals, const void* idx, 
 // staged copy of the tile's spans (c = lane, tile = 0).  `valid`: the chunk
 // exists; `reads`: the lane may read (per-chunk formats only for chunks that
 // exist; the ternary words belong to the whole tile and every lane reads them).
+// KV > 0: k is KV, known at compile time (a float32 or 16-bit format with k in
+// {1, 2, 4, 8}), so the vector load needs no dispatch on k and the entry loop runs
+// exactly k times; KV = 0: k is the runtime value.
+template <int KV>
 __device__ __forceinline__ void demo_accumulate(SumCount* acc, int lane, const void* vals, const void* idx, int wire,
-                                                int k, long long c, long long tile, bool valid, bool reads) {
-  if (wire != kWireTernary && vector_kd(k)) {
+                                                int k_runtime, long long c, long long tile, bool valid, bool reads) {
+  const int k = KV > 0 ? KV : k_runtime;
+  if (KV > 0 || (wire != kWireTernary && vector_kd(k))) {
     if (valid) {
       float pv[8];
       uint32_t ilo, ihi;
       load_payload(vals, idx, wire, c, k, pv, ilo, ihi);
+      constexpr int kMaxEntries = KV > 0 ? KV : 8;
+      int uu[kMaxEntries];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j < k) {
-          const int u = ((j < 4 ? ilo >> (8 * j) : ihi >> (8 * (j - 4)))) & 31;
-          SumCount a = acc[u * 32 + lane];
-          a.sum += pv[j];
-          a.cnt += 1u;
-          acc[u * 32 + lane] = a;
+      for (int j = 0; j < kMaxEntries; ++j) uu[j] = ((j < 4 ? ilo >> (8 * j) : ihi >> (8 * (j - 4)))) & 31;
+      bool ascending = false;
+      if constexpr (KV > 1) {
+        ascending = true;
+#pragma unroll
+        for (int j = 1; j < KV; ++j) ascending = ascending && uu[j] > uu[j - 1];
+      }
+      if (ascending) {
+        // A valid payload lists distinct slots in ascending order: read all k slots,
+        // then update and write them, instead of a chain of k dependent updates.
+        SumCount a[kMaxEntries];
+#pragma unroll
+        for (int j = 0; j < kMaxEntries; ++j) a[j] = acc[uu[j] * 32 + lane];
+#pragma unroll
+        for (int j = 0; j < kMaxEntries; ++j) {
+          a[j].sum += pv[j];
+          a[j].cnt += 1u;
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxEntries; ++j) acc[uu[j] * 32 + lane] = a[j];
+      } else {
+#pragma unroll
+        for (int j = 0; j < kMaxEntries; ++j) {
+          if (KV > 0 || j < k) {
+            SumCount a = acc[uu[j] * 32 + lane];
+            a.sum += pv[j];
+            a.cnt += 1u;
+            acc[uu[j] * 32 + lane] = a;
+          }
         }
       }
     }
@@ -160,7 +189,7 @@ __device__ __forceinline__ void demo_accumulate(SumCount* acc, int lane, const v
   }
 }
 
-template <int MODE, int MAXR, int WARPS>
+template <int MODE, int MAXR, int WARPS, int KV>
 __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_constant__ DecodeParams<MAXR> p) {
   using WarpSmem = DecWarpSmem<dec_stage_bytes(WARPS)>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -178,7 +207,26 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
   const long long gw = static_cast<long long>(blockIdx.x) * WARPS + warp;
   const long long TW = static_cast<long long>(gridDim.x) * WARPS;
   if (gw >= p.ntiles) return;
-  const long long nitems = (p.ntiles - 1 - gw) / TW + 1;
+  const long long ntw = (p.ntiles - 1 - gw) / TW + 1;  // tiles of this warp
+  // Items: one per tile, or (DeMo, group > 0) one per group of replicas on full tiles.
+  const int G = MODE == kModeDemo ? p.group : 0;
+  const int ngf = G > 0 ? (p.R + G - 1) / G : 1;  // items of a full tile
+  const bool own_ragged = (p.nc & 31) != 0 && (p.ntiles - 1 - gw) % TW == 0;
+  const long long nitems = ntw * ngf - (own_ragged ? ngf - 1 : 0);
+  auto full = [&](long long t) { return (t + 1) * 32 <= p.nc; };
+  // Replicas staged by item g of tile t: [r0, r1).  The last item of a tile also holds
+  // the theta tile and reads the replicas [r1, R) directly (none when grouped).
+  auto staged_range = [&](long long t, int g, int& r0, int& r1) {
+    if (!full(t)) {
+      r0 = r1 = 0;
+    } else if (G > 0) {
+      r0 = g * G;
+      r1 = r0 + G < p.R ? r0 + G : p.R;
+    } else {
+      r0 = 0;
+      r1 = p.nstaged;
+    }
+  };
 
   if (lane == 0) {
     mbar_init(&bars[0], 1);
@@ -190,31 +238,46 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
   __syncwarp();
 
   const uint32_t span = p.vspan + p.ispan;  // staged bytes per replica
-  auto issue = [&](long long item) {
-    if (item >= nitems) return;
-    const int s = static_cast<int>(item & 1);
-    const long long t = gw + item * TW;
-    const int ns = (t + 1) * 32 <= p.nc ? p.nstaged : 0;
-    mbar_expect_tx(&bars[s], kTileBytesF32 + ns * span);
-    tma_load_2d(ws.tbuf[s], &p.theta, &bars[s], 0, static_cast<int>(t * 32));
-    for (int r = 0; r < ns; ++r) {
-      unsigned char* d = ws.stage[s] + r * span;
-      bulk_load(d, static_cast<const unsigned char*>(p.vals[r]) + t * p.vspan, p.vspan, &bars[s]);
-      if (p.ispan) bulk_load(d + p.vspan, static_cast<const unsigned char*>(p.idx[r]) + t * p.ispan, p.ispan, &bars[s]);
+  // Items are loaded strictly in order: the loads keep their own (tile, item) cursor.
+  long long ld_t = gw;
+  int ld_g = 0, ld_slot = 0;
+  auto issue = [&]() {
+    if (ld_t >= p.ntiles) return;
+    const int items = full(ld_t) ? ngf : 1;
+    const bool last = ld_g == items - 1;
+    int r0, r1;
+    staged_range(ld_t, ld_g, r0, r1);
+    uint64_t* bar = &bars[ld_slot];
+    mbar_expect_tx(bar, (last ? kTileBytesF32 : 0) + (r1 - r0) * span);
+    if (last) tma_load_2d(ws.tbuf[ld_slot], &p.theta, bar, 0, static_cast<int>(ld_t * 32));
+    for (int r = r0; r < r1; ++r) {
+      unsigned char* d = ws.stage[ld_slot] + (r - r0) * span;
+      bulk_load(d, static_cast<const unsigned char*>(p.vals[r]) + ld_t * p.vspan, p.vspan, bar);
+      if (p.ispan) bulk_load(d + p.vspan, static_cast<const unsigned char*>(p.idx[r]) + ld_t * p.ispan, p.ispan, bar);
+    }
+    ld_slot ^= 1;
+    if (++ld_g == items) {
+      ld_g = 0;
+      ld_t += TW;
     }
   };
   if (lane == 0) {
-    issue(0);
-    issue(1);
+    issue();
+    issue();
   }
 
+  long long t = gw;
+  int g = 0;
   for (long long item = 0; item < nitems; ++item) {
     const int s = static_cast<int>(item & 1);
     const uint32_t par = static_cast<uint32_t>((item >> 1) & 1);
-    const long long row0 = (gw + item * TW) * 32;
+    const long long row0 = t * 32;
     const long long c = row0 + lane;
     const bool valid = c < p.nc;
-    const int ns = row0 + 32 <= p.nc ? p.nstaged : 0;  // replicas staged for this tile
+    const int items = full(t) ? ngf : 1;
+    const bool last = g == items - 1;
+    int r0, ns;  // replicas staged by this item: [r0, ns)
+    staged_range(t, g, r0, ns);
 
     const bool ok = mbar_wait_bounded(&bars[s], par);
     if (!__all_sync(0xffffffffu, ok)) {
@@ -227,19 +290,30 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
       return;
     }
 
+    if constexpr (MODE == kModeDemo) {
+      for (int r = r0; r < ns; ++r) {
+        const unsigned char* sv = ws.stage[s] + (r - r0) * span;
+        demo_accumulate<KV>(ws.acc, lane, sv, sv + p.vspan, p.wire, p.k, lane, 0, true, true);
+      }
+    }
+    if (!last) {
+      // a group of replicas only: the slot is read, refill it with the load two items on
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) issue();
+      ++g;
+      continue;
+    }
+
     float th[32];
     load_row_f32(ws.tbuf[s], lane, th);
 
     float Q[32];
     if constexpr (MODE == kModeDemo) {
       const long long tile = row0 >> 5;
-      for (int r = 0; r < ns; ++r) {
-        const unsigned char* sv = ws.stage[s] + r * span;
-        demo_accumulate(ws.acc, lane, sv, sv + p.vspan, p.wire, p.k, lane, 0, true, true);
-      }
       const bool reads = valid || p.wire == kWireTernary;
       for (int r = ns; r < p.R; ++r)
-        demo_accumulate(ws.acc, lane, p.vals[r], p.idx[r], p.wire, p.k, c, tile, valid, reads);
+        demo_accumulate<KV>(ws.acc, lane, p.vals[r], p.idx[r], p.wire, p.k, c, tile, valid, reads);
       if (p.R * p.k > kMaxReplicas) {
         // Valid payloads count at most R entries per slot; a malformed one (an index
         // repeated within a chunk) can count more than the reciprocal table covers.
@@ -375,60 +449,71 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
     store_tile_coalesced(ws.tbuf[s], lane, th, p.theta_ptr, row0, p.nc);
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) issue(item + 2);
+    if (lane == 0) issue();
+    g = 0;
+    t += TW;
   }
 }
 
 template <int MAXR, int WARPS>
-static cudaError_t launch_decode_w(const DecodeParams<MAXR>& p, int mode, int grid, cudaStream_t st) {
+static cudaError_t launch_decode_w(const DecodeParams<MAXR>& p, int mode, int kv, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(WARPS * 32);
   cfg.dynamicSmemBytes = dec_smem(WARPS);
   cfg.stream = st;
   switch (mode) {
-    case kModeDemo: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS>, p);
-    case kModeRandom: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeRandom, MAXR, WARPS>, p);
-    case kModeStride: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeStride, MAXR, WARPS>, p);
-    case kModeDiloco: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDiloco, MAXR, WARPS>, p);
+    case kModeDemo:
+      switch (kv) {
+        case 1: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS, 1>, p);
+        case 2: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS, 2>, p);
+        case 4: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS, 4>, p);
+        case 8: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS, 8>, p);
+        default: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS, 0>, p);
+      }
+    case kModeRandom: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeRandom, MAXR, WARPS, 0>, p);
+    case kModeStride: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeStride, MAXR, WARPS, 0>, p);
+    case kModeDiloco: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDiloco, MAXR, WARPS, 0>, p);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <int MAXR>
-static cudaError_t launch_decode_t(const DecodeParams<MAXR>& p, int mode, int warps, int grid, cudaStream_t st) {
-  if (warps == 11) return launch_decode_w<MAXR, 11>(p, mode, grid, st);
-  if (warps == 10) return launch_decode_w<MAXR, 10>(p, mode, grid, st);
-  if (warps == 9) return launch_decode_w<MAXR, 9>(p, mode, grid, st);
-  if (warps == 8) return launch_decode_w<MAXR, 8>(p, mode, grid, st);
+static cudaError_t launch_decode_t(const DecodeParams<MAXR>& p, int mode, int warps, int kv, int grid,
+                                   cudaStream_t st) {
+  if (warps == 11) return launch_decode_w<MAXR, 11>(p, mode, kv, grid, st);
+  if (warps == 10) return launch_decode_w<MAXR, 10>(p, mode, kv, grid, st);
+  if (warps == 9) return launch_decode_w<MAXR, 9>(p, mode, kv, grid, st);
+  if (warps == 8) return launch_decode_w<MAXR, 8>(p, mode, kv, grid, st);
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int grid,
+cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int kv, int grid,
                                 cudaStream_t st) {
-  return launch_decode_t(p, mode, warps, grid, st);
+  return launch_decode_t(p, mode, warps, kv, grid, st);
 }
 
-cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int grid,
+cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int kv, int grid,
                                 cudaStream_t st) {
-  return launch_decode_t(p, mode, warps, grid, st);
+  return launch_decode_t(p, mode, warps, kv, grid, st);
+}
+
+template <class K>
+static cudaError_t set_smem(K kernel, int bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 template <int MAXR, int WARPS>
 static cudaError_t prepare_w() {
   const int bytes = static_cast<int>(dec_smem(WARPS));
-  cudaError_t e = cudaSuccess;
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_kernel<kModeDemo, MAXR, WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_kernel<kModeRandom, MAXR, WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             bytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_kernel<kModeStride, MAXR, WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             bytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_kernel<kModeDiloco, MAXR, WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             bytes);
+  cudaError_t e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, 0>, bytes);
+  if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, 1>, bytes);
+  if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, 2>, bytes);
+  if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, 4>, bytes);
+  if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, 8>, bytes);
+  if (e == cudaSuccess) e = set_smem(decode_kernel<kModeRandom, MAXR, WARPS, 0>, bytes);
+  if (e == cudaSuccess) e = set_smem(decode_kernel<kModeStride, MAXR, WARPS, 0>, bytes);
+  if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDiloco, MAXR, WARPS, 0>, bytes);
   return e;
 }
 

@@ -37,6 +37,10 @@ struct DecodeParams {
   // with the theta tile; the others, and a ragged last tile, are read directly.
   int nstaged;
   unsigned int vspan, ispan;
+  // DeMo with more replicas than a staging area holds: each full tile is visited as
+  // ceil(R / group) items, item i staging replicas [i * group, (i + 1) * group) and the
+  // last one also the theta tile; 0 = one item per tile.
+  int group;
   float lr, rcpR;
   unsigned long long hbase;
   float rcp_tab[kMaxReplicas + 1];
@@ -71,9 +75,11 @@ cudaError_t launch_adamw(const AdamWParams& p, bool bf16, int grid, cudaStream_t
 // selection says otherwise (encode_warps, and the decode's staging shape).
 int encode_warps(int mode, int k, int wire, bool bf16);
 cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps, int grid, cudaStream_t st);
-cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int grid,
+// kv: DeMo's k when the decode is specialised for it (1, 2, 4 or 8 with a float32 or
+// 16-bit format), else 0.
+cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int kv, int grid,
                                 cudaStream_t st);
-cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int grid,
+cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int kv, int grid,
                                 cudaStream_t st);
 
 // Set the dynamic shared-memory limit of every encode and decode kernel instantiation.

@@ -3,7 +3,8 @@
 The fused step is compiled for 6, 8 and 11 warps per SM (each with a small and a
 large parameter block), the encode for 6, 8 and 11, and the decode for four
 (warps, staging) shapes; the host picks among them by mode, k, R, gradient dtype
-and wire format.  Each case below lands on a different branch of that choice
+and wire format (DeMo payloads too large for every shape are staged a group
+of replicas per item).  Each case below lands on a different branch of that choice
 (noted beside it) and runs the teacher-forced harness of tests/parity.py for
 two steps: split and fused bit-identical, payloads, momentum and Q against the
 oracle.  The shard has three full 32-chunk tiles and a ragged one of five chunks,
@@ -49,8 +50,9 @@ CASES = [
     ("demo", 4, 4, False, "f32", "decode 10 warps / 3 KB (R x span = 2560)"),
     ("demo", 4, 6, False, "f32", "fused 8, large block; decode 9 warps / 4.5 KB"),
     ("demo", 4, 9, False, "f32", "decode 8 warps / 6 KB (5760)"),
-    ("demo", 4, 10, False, "f32", "decode 11 warps, three replicas staged, seven direct"),
-    ("demo", 8, 5, False, "f32", "fused 11, large block; decode 11 partial"),
+    ("demo", 4, 10, False, "f32", "decode in groups of three replicas per item (four items per tile)"),
+    ("demo", 8, 5, False, "f32", "fused 11, large block; decode one replica per item"),
+    ("random", 8, 7, False, "f32", "decode 11 warps, two replicas staged, five direct"),
     ("demo", 4, 2, False, "ternary", "encode ternary 11; decode bit-planes staged"),
 ]
 
