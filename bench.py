@@ -661,7 +661,7 @@ def main():
         "e2e": e2e,
         "device_fault": fault,
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:  # the CPU baseline is taken at N = 1 only
         line["cpu_baseline"] = cpu_baseline(wl.name, mode, k, sign, R)
     print(json.dumps(line), flush=True)
     if world > 1:
