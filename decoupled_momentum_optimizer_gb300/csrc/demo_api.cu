@@ -278,8 +278,9 @@ int run_encode(DeviceState* st, const void* g, int grad_dtype, float* m, int64_t
   p.stride_mask = (mode == DEMO_MODE_STRIDE) ? stride_mask(p.stride_o, p.stride_ns, k) : 0u;
   p.beta = beta;
   p.fault = st->fault;
-  const int warps = encode_warps(mode, p.k, wire, bf16);
-  return to_status(launch_encode(p, mode, bf16, warps, grid_for(p.ntiles, st, warps), stream));
+  int kv = 0;
+  const int warps = encode_warps(mode, p.k, wire, bf16, &kv);
+  return to_status(launch_encode(p, mode, bf16, warps, kv, grid_for(p.ntiles, st, warps), stream));
 }
 
 // Byte offset of the payload of the block starting at chunk c0 (tile t0 = c0 / 32) in a wire-format buffer.

@@ -41,9 +41,10 @@ struct PayloadOut {
   bool valid, vec;
   float pv[8];
   uint32_t ilo, ihi;
+  bool tern;  // wire == kWireTernary (a constant false in the k-specialised DeMo kernels)
 
   __device__ __forceinline__ void put(int j, int u, float v) {
-    if (wire == kWireTernary) {
+    if (tern) {
       const uint32_t nz = __ballot_sync(0xffffffffu, valid && v != 0.0f);
       const uint32_t ng = __ballot_sync(0xffffffffu, valid && v < 0.0f);
       uint32_t* vw = static_cast<uint32_t*>(vals) + (tile * k + j) * 2;
@@ -76,7 +77,7 @@ struct PayloadOut {
 
   // Vector store of the collected entries (k in {1, 2, 4, 8}, value formats other than ternary).
   __device__ __forceinline__ void finish() {
-    if (wire == kWireTernary || !vec || !valid) return;
+    if (tern || !vec || !valid) return;
     uint8_t* irow = idx ? static_cast<uint8_t*>(idx) + c * k : nullptr;
     if (wire == kWireF32) {
       float* vrow = static_cast<float*>(vals) + c * k;
@@ -144,7 +145,10 @@ __device__ __forceinline__ void put_row(void* vals, int wire, long long c, long 
   }
 }
 
-template <int MODE, bool BF16, int WARPS>
+// KV > 0 (DeMo, a float32 or 16-bit format, k in {1, 2, 4, 8}): k is KV at compile
+// time, so the payload loop unrolls, each entry goes straight to its register and the
+// vector store needs no dispatch on k; KV = 0: k is the runtime value.
+template <int MODE, bool BF16, int WARPS, int KV>
 __global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_constant__ EncodeParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte aligned start (the TMA swizzle patterns are relative to 1024-byte boundaries),
@@ -212,14 +216,21 @@ __global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_cons
       const uint32_t M = topk_select(X, p.k, Xs);
 #pragma unroll
       for (int u = 0; u < 32; ++u) scratch[u * 32 + lane] = Xs[u];
-      PayloadOut out{p.vals, p.idx, c, row0 >> 5, lane, p.k, p.wire, valid, vector_k(p.k) && p.wire != kWireTernary,
-                     {0, 0, 0, 0, 0, 0, 0, 0}, 0u, 0u};
+      const bool tern = KV > 0 ? false : p.wire == kWireTernary;
+      PayloadOut out{p.vals, p.idx, c, row0 >> 5, lane, KV > 0 ? KV : p.k, p.wire, valid,
+                     KV > 0 ? true : vector_k(p.k) && !tern, {0, 0, 0, 0, 0, 0, 0, 0}, 0u, 0u, tern};
       uint32_t mm = M;
-      for (int j = 0; j < p.k; ++j) {  // payload in ascending u
+      auto entry = [&](int j) {  // payload in ascending u
         const int u = __ffs(mm) - 1;
         mm &= mm - 1;
         const float v = scratch[u * 32 + lane];
         out.put(j, u, p.sign ? sign3(v) : v);
+      };
+      if constexpr (KV > 0) {
+#pragma unroll
+        for (int j = 0; j < KV; ++j) entry(j);
+      } else {
+        for (int j = 0; j < p.k; ++j) entry(j);
       }
       out.finish();
       float q[32];
@@ -240,7 +251,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_cons
 #pragma unroll
       for (int i = 0; i < 32; ++i) scratch[i * 32 + lane] = x[i];
       PayloadOut out{p.vals, nullptr, c, row0 >> 5, lane, p.k, p.wire, valid,
-                     vector_k(p.k) && p.wire != kWireTernary, {0, 0, 0, 0, 0, 0, 0, 0}, 0u, 0u};
+                     vector_k(p.k) && p.wire != kWireTernary, {0, 0, 0, 0, 0, 0, 0, 0}, 0u, 0u,
+                     p.wire == kWireTernary};
       auto emit = [&](int j, int pos) {
         const float v = scratch[pos * 32 + lane];
         out.put(j, pos, p.sign ? sign3(v) : v);
@@ -264,17 +276,26 @@ __global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_cons
   }
 }
 
-// Resident warps per SM for one encode, from its compute per tile (measured on
-// the T5-base shard with float32 and the OLMo-shaped shard with bfloat16
-// gradients): as in the fused step, fewer warps run faster once HBM is
-// saturated, unless the selection needs them (DeMo from k = 7 on, the ternary
-// format's ballots); bfloat16 gradients bring less data per tile for the same
-// compute, so they take more warps.
-int encode_warps(int mode, int k, int wire, bool bf16) {
+// Resident warps per SM for one encode, and whether DeMo runs the kernel compiled for
+// its k (*kv = k) or the runtime-k one (*kv = 0), from its compute per tile (measured
+// jointly on the T5-base shard with float32 and the OLMo-shaped shard with bfloat16
+// gradients): as in the fused step, fewer warps run faster once HBM is saturated,
+// unless the selection needs them (DeMo from k = 7 on, the ternary format's ballots).
+// The k-compiled kernel issues fewer instructions and so wants fewer warps; bfloat16
+// gradients bring less data per tile for the same compute and want more.
+int encode_warps(int mode, int k, int wire, bool bf16, int* kv) {
+  *kv = 0;
   if (mode == kModeDemo) {
     if (wire == kWireTernary) return kStepWarps;
+    if (k == 1 || k == 2 || k == 4 || k == 8) {
+      if (!bf16 && k <= 2) {
+        *kv = k;
+        return kStepWarpsLight;
+      }
+      if (bf16 ? k >= 2 : k == 8) *kv = k;
+      return kStepWarpsMid;
+    }
     if (bf16) return k == 1 ? kStepWarpsMid : kStepWarps;
-    if (k == 1) return kStepWarpsLight;
     return k <= 6 ? kStepWarpsMid : kStepWarps;
   }
   if (mode == kModeRandom) return bf16 ? kStepWarps : kStepWarpsMid;
@@ -282,17 +303,28 @@ int encode_warps(int mode, int k, int wire, bool bf16) {
   return bf16 ? kStepWarpsLight : kStepWarpsMid;
 }
 
+template <int WARPS, bool BF16>
+static cudaError_t launch_encode_demo(const cudaLaunchConfig_t& cfg, const EncodeParams& p, int kv) {
+  switch (kv) {
+    case 1: return cudaLaunchKernelEx(&cfg, encode_kernel<kModeDemo, BF16, WARPS, 1>, p);
+    case 2: return cudaLaunchKernelEx(&cfg, encode_kernel<kModeDemo, BF16, WARPS, 2>, p);
+    case 4: return cudaLaunchKernelEx(&cfg, encode_kernel<kModeDemo, BF16, WARPS, 4>, p);
+    case 8: return cudaLaunchKernelEx(&cfg, encode_kernel<kModeDemo, BF16, WARPS, 8>, p);
+    default: return cudaLaunchKernelEx(&cfg, encode_kernel<kModeDemo, BF16, WARPS, 0>, p);
+  }
+}
+
 template <int WARPS>
-static cudaError_t launch_encode_w(const EncodeParams& p, int mode, bool bf16, int grid, cudaStream_t st) {
+static cudaError_t launch_encode_w(const EncodeParams& p, int mode, bool bf16, int kv, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(WARPS * 32);
   cfg.dynamicSmemBytes = enc_smem(WARPS);
   cfg.stream = st;
+  if (mode == kModeDemo)
+    return bf16 ? launch_encode_demo<WARPS, true>(cfg, p, kv) : launch_encode_demo<WARPS, false>(cfg, p, kv);
 #define DEMO_LAUNCH(M, B) \
-  if (mode == M && bf16 == B) return cudaLaunchKernelEx(&cfg, encode_kernel<M, B, WARPS>, p);
-  DEMO_LAUNCH(kModeDemo, false)
-  DEMO_LAUNCH(kModeDemo, true)
+  if (mode == M && bf16 == B) return cudaLaunchKernelEx(&cfg, encode_kernel<M, B, WARPS, 0>, p);
   DEMO_LAUNCH(kModeRandom, false)
   DEMO_LAUNCH(kModeRandom, true)
   DEMO_LAUNCH(kModeStride, false)
@@ -303,28 +335,37 @@ static cudaError_t launch_encode_w(const EncodeParams& p, int mode, bool bf16, i
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps, int grid, cudaStream_t st) {
-  if (warps == kStepWarpsLight) return launch_encode_w<kStepWarpsLight>(p, mode, bf16, grid, st);
-  if (warps == kStepWarpsMid) return launch_encode_w<kStepWarpsMid>(p, mode, bf16, grid, st);
-  if (warps == kStepWarps) return launch_encode_w<kStepWarps>(p, mode, bf16, grid, st);
+cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps, int kv, int grid,
+                          cudaStream_t st) {
+  if (warps == kStepWarpsLight) return launch_encode_w<kStepWarpsLight>(p, mode, bf16, kv, grid, st);
+  if (warps == kStepWarpsMid) return launch_encode_w<kStepWarpsMid>(p, mode, bf16, kv, grid, st);
+  if (warps == kStepWarps) return launch_encode_w<kStepWarps>(p, mode, bf16, kv, grid, st);
   return cudaErrorInvalidValue;
 }
 
 template <int WARPS>
 static cudaError_t prepare_encode_w() {
   cudaError_t e = cudaSuccess;
-#define DEMO_ATTR(M, B)                                                                             \
-  if (e == cudaSuccess)                                                                             \
-    e = cudaFuncSetAttribute(encode_kernel<M, B, WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+#define DEMO_ATTR(M, B, KV)                                                                             \
+  if (e == cudaSuccess)                                                                                 \
+    e = cudaFuncSetAttribute(encode_kernel<M, B, WARPS, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                              static_cast<int>(enc_smem(WARPS)));
-  DEMO_ATTR(kModeDemo, false)
-  DEMO_ATTR(kModeDemo, true)
-  DEMO_ATTR(kModeRandom, false)
-  DEMO_ATTR(kModeRandom, true)
-  DEMO_ATTR(kModeStride, false)
-  DEMO_ATTR(kModeStride, true)
-  DEMO_ATTR(kModeDiloco, false)
-  DEMO_ATTR(kModeDiloco, true)
+  DEMO_ATTR(kModeDemo, false, 0)
+  DEMO_ATTR(kModeDemo, false, 1)
+  DEMO_ATTR(kModeDemo, false, 2)
+  DEMO_ATTR(kModeDemo, false, 4)
+  DEMO_ATTR(kModeDemo, false, 8)
+  DEMO_ATTR(kModeDemo, true, 0)
+  DEMO_ATTR(kModeDemo, true, 1)
+  DEMO_ATTR(kModeDemo, true, 2)
+  DEMO_ATTR(kModeDemo, true, 4)
+  DEMO_ATTR(kModeDemo, true, 8)
+  DEMO_ATTR(kModeRandom, false, 0)
+  DEMO_ATTR(kModeRandom, true, 0)
+  DEMO_ATTR(kModeStride, false, 0)
+  DEMO_ATTR(kModeStride, true, 0)
+  DEMO_ATTR(kModeDiloco, false, 0)
+  DEMO_ATTR(kModeDiloco, true, 0)
 #undef DEMO_ATTR
   return e;
 }

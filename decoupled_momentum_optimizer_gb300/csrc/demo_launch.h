@@ -73,8 +73,11 @@ cudaError_t launch_adamw(const AdamWParams& p, bool bf16, int grid, cudaStream_t
 
 // The encode and decode kernels run kStepWarps warps per CTA unless their own
 // selection says otherwise (encode_warps, and the decode's staging shape).
-int encode_warps(int mode, int k, int wire, bool bf16);
-cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps, int grid, cudaStream_t st);
+int encode_warps(int mode, int k, int wire, bool bf16, int* kv);
+// kv: DeMo's k when the encode is specialised for it (1, 2, 4 or 8 with a float32 or
+// 16-bit format), else 0.
+cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps, int kv, int grid,
+                          cudaStream_t st);
 // kv: DeMo's k when the decode is specialised for it (1, 2, 4 or 8 with a float32 or
 // 16-bit format), else 0.
 cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int kv, int grid,

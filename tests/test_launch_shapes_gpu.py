@@ -1,8 +1,9 @@
 """Every launch shape the library picks, checked once on a small ragged shard.
 
 The fused step is compiled for 6, 8 and 11 warps per SM (each with a small and a
-large parameter block), the encode for 6, 8 and 11, and the decode for four
-(warps, staging) shapes; the host picks among them by mode, k, R, gradient dtype
+large parameter block), the encode for 6, 8 and 11 (DeMo also for k = 1, 2, 4, 8
+at compile time), and the decode for four (warps, staging) shapes (DeMo also for
+k = 1, 2, 4, 8); the host picks among them by mode, k, R, gradient dtype
 and wire format (DeMo payloads too large for every shape are staged a group
 of replicas per item).  Each case below lands on a different branch of that choice
 (noted beside it) and runs the teacher-forced harness of tests/parity.py for
@@ -40,9 +41,11 @@ CASES = [
     ("random", 8, 2, True, "f32", "encode bf16 11"),
     ("random", 8, 5, False, "f32", "fused 8, large block; decode 8 warps / 6 KB"),
     ("random", 3, 3, False, "ternary", "decode ternary bit-planes, k not a power of two"),
-    ("demo", 1, 2, False, "f32", "fused 6 (f32 k = 1); encode 6"),
-    ("demo", 1, 2, True, "f32", "fused 8 (bf16 k = 1); encode bf16 8"),
-    ("demo", 2, 2, True, "f32", "encode bf16 11"),
+    ("demo", 1, 2, False, "f32", "fused 6 (f32 k = 1); encode k-compiled, 6 warps"),
+    ("demo", 1, 2, True, "f32", "fused 8 (bf16 k = 1); encode runtime k, 8 warps"),
+    ("demo", 2, 2, True, "f32", "encode bf16 gradients, k-compiled, 8 warps"),
+    ("demo", 2, 2, False, "f32", "encode f32 gradients, k-compiled, 6 warps"),
+    ("demo", 8, 2, True, "bf16", "encode k-compiled, 8 warps; 16-bit payload"),
     ("demo", 5, 2, False, "f32", "fused 8; encode 8; decode scalar entries"),
     ("demo", 6, 2, False, "bf16", "fused 8 (k = 6); 16-bit payload"),
     ("demo", 7, 2, False, "f32", "fused 11 (k = 7); encode 11; decode 10 warps / 3 KB"),
