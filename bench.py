@@ -714,7 +714,9 @@ def run_only(args):
     case = Case(wl, R, torch.device("cuda", 0), n_sets=2)
     stream = torch.cuda.current_stream()
     if args.only == "split":
-        ms = time_split(dm, case, mode, k, sign, 0, args.steps, args.warmup, stream, wire=args.wire)
+        # DiLoCo: period 1, so that every timed step is a sync step (the one with a payload)
+        ms = time_split(dm, case, mode, k, sign, 0, args.steps, args.warmup, stream, wire=args.wire,
+                        diloco_period=1 if mode == "diloco" else 8)
         nbytes = split_bytes(case.n, R, case.grad_bytes, mode, k, wire=args.wire)
     else:
         ms = time_adamw(dm, case, args.steps, args.warmup, stream)

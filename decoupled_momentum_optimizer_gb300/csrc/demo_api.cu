@@ -218,10 +218,36 @@ int stage_payloads(P& p, int mode, int k, int wire, int R) {
   return warps;
 }
 
+// The DiLoCo sync step's decode is elementwise (every replica sends its whole
+// momentum): one grid-stride pass over groups of four parameters.
+template <int MAXR>
+int run_dense_decode(DeviceState* st, float* theta, int64_t n, float lr, int R, const void* const* vals, int wire,
+                     cudaStream_t stream) {
+  DenseParams<MAXR> p;
+  std::memset(&p, 0, sizeof(p));
+  p.theta = theta;
+  for (int r = 0; r < R; ++r) p.vals[r] = vals[r];
+  p.n4 = n / 4;
+  p.R = R;
+  p.wire = wire;
+  p.lr = lr;
+  p.rcpR = 1.0f / static_cast<float>(R);
+  const int64_t want = (p.n4 + 255) / 256;
+  const int grid = static_cast<int>(want < 8LL * st->sms ? want : 8LL * st->sms);
+  cudaError_t e;
+  if constexpr (MAXR == kSmallReplicas) {
+    e = launch_dense_small(p, grid, stream);
+  } else {
+    e = launch_dense_large(p, grid, stream);
+  }
+  return to_status(e);
+}
+
 template <int MAXR>
 int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mode, int R,
                const void* const* vals, const void* const* idx, uint64_t seed, uint64_t step, int wire,
                cudaStream_t stream, int64_t chunk0 = 0) {
+  if (mode == DEMO_MODE_DILOCO) return run_dense_decode<MAXR>(st, theta, n, lr, R, vals, wire, stream);
   DecodeParams<MAXR> p;
   std::memset(&p, 0, sizeof(p));
   const int64_t nc = n / DEMO_CHUNK;

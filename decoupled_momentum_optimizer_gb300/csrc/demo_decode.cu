@@ -1,5 +1,6 @@
-// Split-path decode: scatter-mean of R replicas' payloads, inverse transform,
-// theta <- theta - lr Q.
+// Split-path decode of the DeMo, Random and Striding schemes: scatter-mean of R
+// replicas' payloads, inverse transform, theta <- theta - lr Q.  (The DiLoCo sync
+// step's decode is elementwise and lives in demo_dense.cu.)
 //
 // "DeToNATION: Decoupled Torch Network-Aware Training on Interlinked Online
 // Nodes" (Paper-Notes, AAAI 2026), method section, "1. FlexDeMo" Algorithm 1
@@ -340,46 +341,6 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
 #pragma unroll
       for (int u = 0; u < 32; ++u) ws.acc[u * 32 + lane] = SumCount{0.0f, 0u};
       dct32_inverse(Y, Q);
-    } else if constexpr (MODE == kModeDiloco) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) Q[i] = 0.0f;
-      for (int r = 0; r < p.R; ++r) {
-        if (p.wire == kWireTernary) {
-          const uint2* w = reinterpret_cast<const uint2*>(p.vals[r]) + (row0 >> 5) * 32;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const uint2 b = w[j];
-            const float v = ((b.x >> lane) & 1u) ? (((b.y >> lane) & 1u) ? -1.0f : 1.0f) : 0.0f;
-            Q[j] += valid ? v : 0.0f;
-          }
-        } else if (valid) {
-          if (p.wire == kWireF32) {
-            const float4* vrow = reinterpret_cast<const float4*>(static_cast<const float*>(p.vals[r]) + c * 32);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float4 v = vrow[j];
-              Q[4 * j + 0] += v.x;
-              Q[4 * j + 1] += v.y;
-              Q[4 * j + 2] += v.z;
-              Q[4 * j + 3] += v.w;
-            }
-          } else {
-            const uint4* vrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.vals[r]) + c * 32);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint4 v = vrow[j];
-              const uint32_t h[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                Q[8 * j + 2 * i] += wire_from_bits16(h[i] & 0xffffu, p.wire);
-                Q[8 * j + 2 * i + 1] += wire_from_bits16(h[i] >> 16, p.wire);
-              }
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) Q[i] *= p.rcpR;
     } else {
       // Random / Striding: every replica sent the same positions; Q = mean at those positions.
       float* qs = reinterpret_cast<float*>(ws.acc);  // [i][lane] scratch (first 4 KB)
@@ -473,7 +434,6 @@ static cudaError_t launch_decode_w(const DecodeParams<MAXR>& p, int mode, int kv
       }
     case kModeRandom: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeRandom, MAXR, WARPS, 0>, p);
     case kModeStride: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeStride, MAXR, WARPS, 0>, p);
-    case kModeDiloco: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDiloco, MAXR, WARPS, 0>, p);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -513,7 +473,6 @@ static cudaError_t prepare_w() {
   if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, 8>, bytes);
   if (e == cudaSuccess) e = set_smem(decode_kernel<kModeRandom, MAXR, WARPS, 0>, bytes);
   if (e == cudaSuccess) e = set_smem(decode_kernel<kModeStride, MAXR, WARPS, 0>, bytes);
-  if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDiloco, MAXR, WARPS, 0>, bytes);
   return e;
 }
 

@@ -1,0 +1,83 @@
+// Dense decode: the DiLoCo sync step's receiver, theta <- theta - lr * mean_r(v_r).
+//
+// "DeToNATION: Decoupled Torch Network-Aware Training on Interlinked Online
+// Nodes" (Paper-Notes, AAAI 2026), "2. Replication Schemes" table (DiLoCo: full
+// synchronisation every n steps) and "1. FlexDeMo" Algorithm 1 step 7.
+//
+// On a sync step every replica sends its whole momentum, so Q = Y and the update is
+// elementwise.  A grid-stride loop over groups of four parameters reads every
+// replica's four values (one 16-byte load for float32, 8 bytes for 16-bit formats,
+// the tile's bit-plane words for the ternary format), all of a group's loads before
+// any arithmetic, and updates theta with one 16-byte load and store.  The sum runs
+// over the replicas in order from 0, then is scaled by 1/R and applied with one FMA,
+// exactly as the fused step does, so the two stay bit-identical.
+#include "demo_common.cuh"
+#include "demo_launch.h"
+
+namespace demo {
+
+constexpr int kDenseThreads = 256;
+
+// The four values of replica payload `v` for parameters 4i .. 4i + 3 (chunk c = 4i / 32,
+// positions j .. j + 3 within it), as the receiver decodes them.
+__device__ __forceinline__ float4 dense_values(const void* v, int wire, long long i) {
+  if (wire == kWireF32) return reinterpret_cast<const float4*>(v)[i];
+  if (wire == kWireTernary) {
+    const long long e = 4 * i;
+    const long long c = e >> 5;
+    const int j = static_cast<int>(e & 31);
+    const int bit = static_cast<int>(c & 31);
+    // words [tile][32 positions][2]: nonzero and negative bit-planes, bit = chunk within the tile
+    const uint4 w01 = reinterpret_cast<const uint4*>(v)[((c >> 5) * 32 + j) / 2];
+    const uint4 w23 = reinterpret_cast<const uint4*>(v)[((c >> 5) * 32 + j) / 2 + 1];
+    auto val = [bit](uint32_t nz, uint32_t ng) {
+      return ((nz >> bit) & 1u) ? (((ng >> bit) & 1u) ? -1.0f : 1.0f) : 0.0f;
+    };
+    return make_float4(val(w01.x, w01.y), val(w01.z, w01.w), val(w23.x, w23.y), val(w23.z, w23.w));
+  }
+  const uint2 h = reinterpret_cast<const uint2*>(v)[i];
+  return make_float4(wire_from_bits16(h.x & 0xffffu, wire), wire_from_bits16(h.x >> 16, wire),
+                     wire_from_bits16(h.y & 0xffffu, wire), wire_from_bits16(h.y >> 16, wire));
+}
+
+template <int MAXR>
+__global__ void __launch_bounds__(kDenseThreads) dense_decode_kernel(const __grid_constant__ DenseParams<MAXR> p) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.n4; i += stride) {
+    const float4 th0 = reinterpret_cast<const float4*>(p.theta)[i];
+    float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int r0 = 0; r0 < p.R; r0 += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        if (r0 + b < p.R) v[b] = dense_values(p.vals[r0 + b], p.wire, i);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        if (r0 + b < p.R) {
+          s.x += v[b].x;
+          s.y += v[b].y;
+          s.z += v[b].z;
+          s.w += v[b].w;
+        }
+      }
+    }
+    float4 th = th0;
+    th.x = __fmaf_rn(-p.lr, s.x * p.rcpR, th.x);
+    th.y = __fmaf_rn(-p.lr, s.y * p.rcpR, th.y);
+    th.z = __fmaf_rn(-p.lr, s.z * p.rcpR, th.z);
+    th.w = __fmaf_rn(-p.lr, s.w * p.rcpR, th.w);
+    reinterpret_cast<float4*>(p.theta)[i] = th;
+  }
+}
+
+cudaError_t launch_dense_small(const DenseParams<kSmallReplicas>& p, int grid, cudaStream_t st) {
+  dense_decode_kernel<kSmallReplicas><<<grid, kDenseThreads, 0, st>>>(p);
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_dense_large(const DenseParams<kMaxReplicas>& p, int grid, cudaStream_t st) {
+  dense_decode_kernel<kMaxReplicas><<<grid, kDenseThreads, 0, st>>>(p);
+  return cudaPeekAtLastError();
+}
+
+}  // namespace demo

@@ -56,6 +56,19 @@ __host__ __device__ constexpr int dec_stage_bytes(int warps) {
 }
 constexpr int kDecShapes[] = {11, 10, 9, 8};
 
+// Dense decode (the DiLoCo sync step's receiver; elementwise over groups of four).
+template <int MAXR>
+struct DenseParams {
+  float* theta;
+  const void* vals[MAXR];  // each replica's whole momentum in the wire format
+  long long n4;            // n / 4
+  int R, wire;
+  float lr, rcpR;
+};
+
+cudaError_t launch_dense_small(const DenseParams<kSmallReplicas>& p, int grid, cudaStream_t st);
+cudaError_t launch_dense_large(const DenseParams<kMaxReplicas>& p, int grid, cudaStream_t st);
+
 // Decoupled AdamW (elementwise, grid-stride over groups of four parameters).
 struct AdamWParams {
   float* theta;
