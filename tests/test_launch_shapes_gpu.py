@@ -64,3 +64,25 @@ CASES = [
 def test_launch_shape(mode, k, R, bf16, wire, note):
     sign = wire == "ternary" or mode in ("random", "stride")
     run_steps(N, R, k, mode, sign, 2, g_std=1e-3, period=2 if mode == "diloco" else 8, bf16=bf16, seed=5, wire=wire)
+
+
+# A shard of 1,501 tiles (the last one ragged) lies between one wave of six-warp CTAs
+# (152 x 6 = 912 tiles) and two waves of eight-warp CTAs (2,432): the fused step and the
+# encode that would take six warps take eight.  Every 97th chunk is checked against the oracle.
+N_SMALL = 32 * (32 * 1500 + 7)
+SMALL_CASES = [
+    ("demo", 1, 2, False, "f32", "fused and encode (k-compiled k = 1) 6 -> 8 warps"),
+    ("stride", 4, 2, False, "f32", "fused 6 -> 8 warps"),
+    ("random", 2, 2, False, "f32", "fused 6 -> 8 warps (k <= R + 1)"),
+    ("diloco", 1, 2, True, "f32", "fused 6 -> 8 warps (sync step); encode bf16 6 -> 8"),
+]
+
+
+@pytest.mark.parametrize("mode,k,R,bf16,wire,note", SMALL_CASES, ids=lambda v: str(v))
+def test_small_shard_shape(mode, k, R, bf16, wire, note):
+    import numpy as np
+
+    sign = mode in ("random", "stride") or k == 1
+    rows = np.arange(0, N_SMALL // 32, 97)
+    run_steps(N_SMALL, R, k, mode, sign, 2, g_std=1e-3, period=2 if mode == "diloco" else 8, bf16=bf16, seed=7,
+              wire=wire, rows=rows)
