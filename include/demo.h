@@ -50,6 +50,13 @@
  *     combined in the fixed order r = 0..R-1 (no floating-point atomics).
  *   - Non-finite inputs produce unspecified values, never out-of-bounds
  *     accesses.
+ *   - demo_encode(_wire), demo_decode_update(_wire), demo_step(_wire),
+ *     demo_step_pipelined and demo_adamw_step make only kernel launches, event
+ *     records and waits and asynchronous device copies on the given streams, so
+ *     they may be captured into a CUDA graph (after demo_init).  A captured call
+ *     keeps the arguments it was captured with, step and seed included: each
+ *     replay repeats that step on the buffers' contents at replay time.
+ *     demo_init and demo_device_fault synchronise and must not be captured.
  */
 #ifndef DEMO_GB300_H
 #define DEMO_GB300_H
