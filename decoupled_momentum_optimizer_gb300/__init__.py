@@ -110,59 +110,85 @@ def init(device=None):
         _inited.add(device)
 
 
-def _stream(stream):
+def _stream(stream, device_index):
+    """The cudaStream_t to launch on: the given stream, else torch's current stream of the device."""
     import torch
 
     if stream is None:
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)  # torch's own launch path reads it this way
+        return raw(device_index) if raw is not None else torch.cuda.current_stream(device_index).cuda_stream
     if isinstance(stream, int):
-        return ctypes.c_void_p(stream)
-    return ctypes.c_void_p(stream.cuda_stream)
+        return stream
+    return stream.cuda_stream
 
 
-def _ptr(t, dtypes, name, n=None, device=None):
+def _ptr(t, dtypes, name, n=None, device_index=None, r=None):
+    """The device pointer of a checked tensor (``name``, with replica ``r`` if given, names it in errors)."""
     import torch
 
     if not isinstance(t, torch.Tensor):
-        raise TypeError(f"{name} must be a torch.Tensor")
+        raise TypeError(f"{_name(name, r)} must be a torch.Tensor")
     if not t.is_cuda:
-        raise ValueError(f"{name} must be on a CUDA device (there is no CPU path)")
-    if device is not None and t.device != device:
-        raise ValueError(f"{name} is on {t.device}, the call's other tensors on {device}")
+        raise ValueError(f"{_name(name, r)} must be on a CUDA device (there is no CPU path)")
+    if device_index is not None and t.get_device() != device_index:
+        raise ValueError(f"{_name(name, r)} is on {t.device}, the call's other tensors on cuda:{device_index}")
     if t.dtype not in dtypes:
-        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+        raise TypeError(f"{_name(name, r)} has dtype {t.dtype}, expected one of {dtypes}")
     if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
+        raise ValueError(f"{_name(name, r)} must be contiguous")
     if n is not None and t.numel() != n:
-        raise ValueError(f"{name} has {t.numel()} elements, expected {n}")
+        raise ValueError(f"{_name(name, r)} has {t.numel()} elements, expected {n}")
     return t.data_ptr()
+
+
+def _name(name, r):
+    return name if r is None else f"{name}[{r}]"
+
+
+def _ptrs(ts, dtypes, name, n, device_index):
+    """A host array of the R tensors' device pointers (each checked as by _ptr)."""
+    return (ctypes.c_void_p * len(ts))(*[_ptr(t, dtypes, name, n, device_index, r) for r, t in enumerate(ts)])
 
 
 class _OnDevice:
     """Makes the tensors' device current for a library call (the library launches on the
-    current device) and initialises the library there."""
+    current device) and initialises the library there; ``index`` is that device."""
+
+    __slots__ = ("index", "_ctx")
 
     def __init__(self, device):
-        import torch
-
         if device.type != "cuda":
             raise ValueError(f"tensors are on {device}: the library runs on CUDA devices only (there is no CPU path)")
-        self._ctx = torch.cuda.device(device)
-        self.device = device
+        self.index = device.index
+        self._ctx = None
 
     def __enter__(self):
-        self._ctx.__enter__()
-        init(self.device.index)
+        import torch
+
+        if self.index is None:
+            self.index = torch.cuda.current_device()
+        elif torch.cuda.current_device() != self.index:
+            self._ctx = torch.cuda.device(self.index)
+            self._ctx.__enter__()
+        if self.index not in _inited:
+            init(self.index)
         return self
 
     def __exit__(self, *exc):
-        return self._ctx.__exit__(*exc)
+        if self._ctx is not None:
+            return self._ctx.__exit__(*exc)
+        return False
 
 
 def _grad_dtype(g):
+    """The library's code for a gradient tensor's dtype (float32 or bfloat16; anything else is refused)."""
     import torch
 
-    return GRAD_BF16 if g.dtype == torch.bfloat16 else GRAD_F32
+    if g.dtype == torch.float32:
+        return GRAD_F32
+    if g.dtype == torch.bfloat16:
+        return GRAD_BF16
+    raise TypeError(f"gradients must be float32 or bfloat16, got {g.dtype}")
 
 
 def _mode(mode):
@@ -213,16 +239,16 @@ def encode(g, m, vals, idx=None, *, k, beta, mode="demo", sign=True, diloco_peri
     """One replica's encode (demo_encode_wire): updates m in place, writes vals (and idx for DeMo)."""
     import torch
 
-    dev = m.device
-    with _OnDevice(dev):
+    with _OnDevice(m.device) as d:
         n = m.numel()
         w = _wire(wire)
-        gp = _ptr(g, (torch.float32, torch.bfloat16), "g", n, device=dev)
-        mp = _ptr(m, (torch.float32,), "m", n, device=dev)
-        vp = _ptr(vals, _val_dtypes(w), "vals", device=dev) if vals is not None else None
-        ip = _ptr(idx, _idx_dtypes(w), "idx", device=dev) if idx is not None else None
-        _check(lib().demo_encode_wire(gp, _grad_dtype(g), mp, n, CHUNK, k, beta, _mode(mode), int(bool(sign)),
-                                      diloco_period, seed, step, w, vp, ip, _stream(stream)), "demo_encode")
+        gd = _grad_dtype(g)
+        gp = _ptr(g, (g.dtype,), "g", n, d.index)
+        mp = _ptr(m, (torch.float32,), "m", n, d.index)
+        vp = _ptr(vals, _val_dtypes(w), "vals", None, d.index) if vals is not None else None
+        ip = _ptr(idx, _idx_dtypes(w), "idx", None, d.index) if idx is not None else None
+        _check(lib().demo_encode_wire(gp, gd, mp, n, CHUNK, k, beta, _mode(mode), int(bool(sign)), diloco_period,
+                                      seed, step, w, vp, ip, _stream(stream, d.index)), "demo_encode")
 
 
 def decode_update(theta, vals, idx=None, *, k, lr, mode="demo", diloco_period=8, seed=0, step=0, wire="f32",
@@ -230,39 +256,39 @@ def decode_update(theta, vals, idx=None, *, k, lr, mode="demo", diloco_period=8,
     """Scatter-mean of the R payloads in ``vals`` (and ``idx``) and theta -= lr Q (demo_decode_update_wire)."""
     import torch
 
-    dev = theta.device
-    with _OnDevice(dev):
+    with _OnDevice(theta.device) as d:
         n = theta.numel()
-        R = len(vals)
         w = _wire(wire)
-        tp = _ptr(theta, (torch.float32,), "theta", n, device=dev)
-        varr = (ctypes.c_void_p * R)(*[_ptr(v, _val_dtypes(w), f"vals[{r}]", device=dev) for r, v in enumerate(vals)])
-        iarr = None
-        if idx is not None:
-            iarr = (ctypes.c_void_p * R)(*[_ptr(i, _idx_dtypes(w), f"idx[{r}]", device=dev) for r, i in enumerate(idx)])
-        _check(lib().demo_decode_update_wire(tp, n, CHUNK, k, lr, _mode(mode), R, varr, iarr, diloco_period, seed, step,
-                                             w, _stream(stream)), "demo_decode_update")
+        tp = _ptr(theta, (torch.float32,), "theta", n, d.index)
+        varr = _ptrs(vals, _val_dtypes(w), "vals", None, d.index)
+        iarr = _ptrs(idx, _idx_dtypes(w), "idx", None, d.index) if idx is not None else None
+        _check(lib().demo_decode_update_wire(tp, n, CHUNK, k, lr, _mode(mode), len(vals), varr, iarr, diloco_period,
+                                             seed, step, w, _stream(stream, d.index)), "demo_decode_update")
+
+
+def _replica_arrays(theta, gs, ms, index):
+    """Checked pointers of theta and of the R gradients and momenta (one gradient dtype for all)."""
+    import torch
+
+    n = theta.numel()
+    if len(gs) != len(ms):
+        raise ValueError("need one gradient per replica")
+    if not gs:
+        raise ValueError("need at least one replica")
+    gd = _grad_dtype(gs[0])
+    tp = _ptr(theta, (torch.float32,), "theta", n, index)
+    garr = _ptrs(gs, (gs[0].dtype,), "g", n, index)
+    marr = _ptrs(ms, (torch.float32,), "m", n, index)
+    return n, tp, gd, garr, marr
 
 
 def step(theta, gs, ms, *, k, beta, lr, mode="demo", sign=True, diloco_period=8, seed=0, step=0, wire="f32",
          stream=None):
     """The fused shard step over R replicas (demo_step_wire); theta and every m_r update in place."""
-    import torch
-
-    dev = theta.device
-    with _OnDevice(dev):
-        n = theta.numel()
-        R = len(ms)
-        if len(gs) != R:
-            raise ValueError("need one gradient per replica")
-        tp = _ptr(theta, (torch.float32,), "theta", n, device=dev)
-        gd = _grad_dtype(gs[0])
-        garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n, device=dev)
-                                       for r, g in enumerate(gs)])
-        marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n, device=dev)
-                                       for r, m in enumerate(ms)])
-        _check(lib().demo_step_wire(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr, gd, marr,
-                                    diloco_period, seed, step, _wire(wire), _stream(stream)), "demo_step")
+    with _OnDevice(theta.device) as d:
+        n, tp, gd, garr, marr = _replica_arrays(theta, gs, ms, d.index)
+        _check(lib().demo_step_wire(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), len(ms), garr, gd, marr,
+                                    diloco_period, seed, step, _wire(wire), _stream(stream, d.index)), "demo_step")
 
 
 def step_pipelined(theta, gs, ms, send, recv, *, k, beta, lr, mode="demo", sign=True, diloco_period=8, seed=0,
@@ -271,31 +297,22 @@ def step_pipelined(theta, gs, ms, send, recv, *, k, beta, lr, mode="demo", sign=
 
     ``send`` and ``recv`` are lists of R (vals, idx) pairs as made by payload_buffers.
     """
-    import torch
-
-    dev = theta.device
-    with _OnDevice(dev):
-        n = theta.numel()
-        R = len(ms)
+    with _OnDevice(theta.device) as d:
+        n, tp, gd, garr, marr = _replica_arrays(theta, gs, ms, d.index)
         w = _wire(wire)
-        tp = _ptr(theta, (torch.float32,), "theta", n, device=dev)
-        garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n, device=dev)
-                                       for r, g in enumerate(gs)])
-        marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n, device=dev)
-                                       for r, m in enumerate(ms)])
 
         def arr(pairs, j, dts):
             if pairs is None or pairs[0][j] is None:
                 return None
-            return (ctypes.c_void_p * R)(*[_ptr(pq[j], dts, "payload", device=dev) for pq in pairs])
+            return _ptrs([pq[j] for pq in pairs], dts, "payload", None, d.index)
 
         sv, si = arr(send, 0, _val_dtypes(w)), arr(send, 1, _idx_dtypes(w))
         rv, ri = arr(recv, 0, _val_dtypes(w)), arr(recv, 1, _idx_dtypes(w))
-        cs = _stream(stream)
-        xs = _stream(comm_stream) if comm_stream is not None else cs
-        _check(lib().demo_step_pipelined(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr,
-                                         _grad_dtype(gs[0]), marr, diloco_period, seed, step, w, sv, si, rv, ri, blocks,
-                                         cs, xs), "demo_step_pipelined")
+        cs = _stream(stream, d.index)
+        xs = _stream(comm_stream, d.index) if comm_stream is not None else cs
+        _check(lib().demo_step_pipelined(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), len(ms), garr, gd,
+                                         marr, diloco_period, seed, step, w, sv, si, rv, ri, blocks, cs, xs),
+               "demo_step_pipelined")
 
 
 def step_pipelined_static(theta, gs, ms, *, k, beta, lr, mode="demo", sign=True, diloco_period=8, seed=0, step=0,
@@ -306,43 +323,26 @@ def step_pipelined_static(theta, gs, ms, *, k, beta, lr, mode="demo", sign=True,
     of all replicas must fit the library's fixed 32 MiB send / 32 MiB receive
     scratch (DemoError with DEMO_ENOSPACE otherwise).
     """
-    import torch
-
-    dev = theta.device
-    with _OnDevice(dev):
-        n = theta.numel()
-        R = len(ms)
-        tp = _ptr(theta, (torch.float32,), "theta", n, device=dev)
-        garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n, device=dev)
-                                       for r, g in enumerate(gs)])
-        marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n, device=dev)
-                                       for r, m in enumerate(ms)])
-        cs = _stream(stream)
-        xs = _stream(comm_stream) if comm_stream is not None else cs
-        _check(lib().demo_step_pipelined_static(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), R, garr,
-                                                _grad_dtype(gs[0]), marr, diloco_period, seed, step, _wire(wire),
-                                                blocks, cs, xs), "demo_step_pipelined_static")
+    with _OnDevice(theta.device) as d:
+        n, tp, gd, garr, marr = _replica_arrays(theta, gs, ms, d.index)
+        cs = _stream(stream, d.index)
+        xs = _stream(comm_stream, d.index) if comm_stream is not None else cs
+        _check(lib().demo_step_pipelined_static(tp, n, CHUNK, k, beta, lr, _mode(mode), int(bool(sign)), len(ms),
+                                                garr, gd, marr, diloco_period, seed, step, _wire(wire), blocks, cs,
+                                                xs), "demo_step_pipelined_static")
 
 
 def adamw_step(theta, gs, ms, vs, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, step=0, stream=None):
     """One Decoupled AdamW step (demo_adamw_step): theta, every m_r and v_r update in place."""
     import torch
 
-    dev = theta.device
-    with _OnDevice(dev):
-        n = theta.numel()
-        R = len(ms)
-        if len(gs) != R or len(vs) != R:
+    with _OnDevice(theta.device) as d:
+        if len(vs) != len(ms):
             raise ValueError("need one gradient, first and second moment per replica")
-        tp = _ptr(theta, (torch.float32,), "theta", n, device=dev)
-        garr = (ctypes.c_void_p * R)(*[_ptr(g, (gs[0].dtype,), f"g[{r}]", n, device=dev)
-                                       for r, g in enumerate(gs)])
-        marr = (ctypes.c_void_p * R)(*[_ptr(m, (torch.float32,), f"m[{r}]", n, device=dev)
-                                       for r, m in enumerate(ms)])
-        varr = (ctypes.c_void_p * R)(*[_ptr(v, (torch.float32,), f"v[{r}]", n, device=dev)
-                                       for r, v in enumerate(vs)])
-        _check(lib().demo_adamw_step(tp, n, beta1, beta2, eps, lr, weight_decay, R, garr, _grad_dtype(gs[0]), marr,
-                                     varr, step, _stream(stream)), "demo_adamw_step")
+        n, tp, gd, garr, marr = _replica_arrays(theta, gs, ms, d.index)
+        varr = _ptrs(vs, (torch.float32,), "v", n, d.index)
+        _check(lib().demo_adamw_step(tp, n, beta1, beta2, eps, lr, weight_decay, len(ms), garr, gd, marr, varr, step,
+                                     _stream(stream, d.index)), "demo_adamw_step")
 
 
 def validate_payload(idx_host, n, k, wire="f32"):

@@ -340,6 +340,28 @@ def test_binding_refuses_mixed_devices():
         dm.step(theta.cpu(), [g], [torch.zeros(n, device="cuda")], k=4, beta=0.9, lr=0.1)
 
 
+def test_binding_refuses_other_gradient_dtypes():
+    """Gradients are float32 or bfloat16; float16 ones are refused by every entry point, not read as float32."""
+    n = 32 * 64
+    theta = cuda_normal(n, 2e-2, 1)
+    g = cuda_normal(n, 1e-3, 2).half()
+    m = torch.zeros(n, device="cuda")
+    v = torch.zeros(n, device="cuda")
+    vals, idx = dm.payload_buffers("demo", n, 4)
+    with pytest.raises(TypeError):
+        dm.step(theta, [g], [m], k=4, beta=0.9, lr=0.1)
+    with pytest.raises(TypeError):
+        dm.encode(g, m, vals, idx, k=4, beta=0.9)
+    with pytest.raises(TypeError):
+        dm.adamw_step(theta, [g], [m], [v], lr=1e-3)
+    with pytest.raises(TypeError):
+        dm.step_pipelined(theta, [g], [m], [(vals, idx)], [(vals, idx)], k=4, beta=0.9, lr=0.1)
+    with pytest.raises(TypeError):
+        dm.step_pipelined_static(theta, [g], [m], k=4, beta=0.9, lr=0.1)
+    torch.cuda.synchronize()
+    assert (m == 0).all() and (v == 0).all()
+
+
 def test_guard_bands_untouched():
     n = 32 * (64 + 5)
     pad = 4096 // 4
