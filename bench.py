@@ -445,6 +445,43 @@ def time_split(dm, case, mode, k, sign, seed, steps, warmup, stream, diloco_peri
     return a.elapsed_time(b) / steps
 
 
+def time_split_graph(dm, case, mode, k, sign, seed, steps, warmup, stream, wire="f32"):
+    """Mean time (ms) of the split path (R demo_encode + one demo_decode_update) captured once into a
+    CUDA graph and replayed back to back; the graph keeps its captured step index."""
+    import torch
+
+    wl, n, R = case.wl, case.n, case.R
+    dev = case.theta.device
+    bufs = [dm.payload_buffers(mode, n, k, wire=wire, device=dev) for _ in range(R)]
+    vals = [b[0] for b in bufs]
+    idx = [b[1] for b in bufs] if mode == "demo" else None
+    g = case.ring[0]
+
+    def one():
+        for r in range(R):
+            dm.encode(g[r], case.ms[r], vals[r], idx[r] if idx else None, k=k, beta=wl.beta, mode=mode, sign=sign,
+                      seed=seed, step=1, wire=wire)
+        dm.decode_update(case.theta, vals, idx, k=k, lr=wl.lr, mode=mode, seed=seed, step=1, wire=wire)
+
+    one()  # the first call of each kernel shape happens outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        one()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
 def time_adamw(dm, case, steps, warmup, stream):
     """Mean time (ms) of one Decoupled AdamW step (demo_adamw_step) over the case's replicas."""
     import torch
@@ -697,6 +734,10 @@ def sweep_cases():
     for R in (1, 8, 64):
         out.append((f"flat{1 << 26}", "demo", 4, True, R, ("fused", "split")))
     out.append((f"flat{1 << 30}", "demo", 4, True, 8, ("fused",)))
+    # the split path on small shards, eager against a CUDA graph replay
+    for e in (20, 22, 24):
+        out.append((f"flat{1 << e}", "demo", 4, True, 2, ("graph",)))
+        out.append((f"flat{1 << e}", "random", 8, True, 2, ("graph",)))
     for e in (24, 26, 28):
         for mode, k in (("random", 1), ("random", 8), ("stride", 4), ("diloco", 1), ("diloco-sync", 1)):
             out.append((f"flat{1 << e}", mode, k, True, 2, ("fused", "split") if e == 26 else ("fused",)))
@@ -754,6 +795,19 @@ def run_sweep(args):
         period = 8
         step0 = 7 if sync else 0
         rec = {"workload": name, "n": n, "mode": mode, "k": k, "sign": sign, "R": R, "grad_dtype": case.wl.g_dtype}
+        steps, warmup = (args.steps, args.warmup) if not real_mode == "diloco" else (1, 0)
+        if "graph" in paths:
+            # the split path on a small shard: R + 1 calls eagerly (host-bound) and as one replayed graph
+            em = time_split(dm, case, real_mode, k, sign, 0, 10 * steps, warmup, stream)
+            gm = time_split_graph(dm, case, real_mode, k, sign, 0, 10 * steps, warmup, stream)
+            sb = split_bytes(n, R, case.grad_bytes, real_mode, k)
+            r2 = dict(rec, mode=f"{mode}/graph", split_ms=em, split_graph_ms=gm, split_bytes=sb,
+                      split_graph_gbs=sb / (gm * 1e-3) / 1e9, split_graph_frac=sb / (gm * 1e-3) / 1e9 / peak)
+            f.write(json.dumps(r2) + "\n")
+            f.flush()
+            print(f"{name:16s} {mode + '/graph':16s} k={k:2d} sign={int(sign)} R={R:2d}  split eager {em * 1e3:7.1f} us"
+                  f"  graph {gm * 1e3:7.1f} us {r2['split_graph_gbs']:7.0f} GB/s", flush=True)
+            continue
         if mode == "adamw":
             am = time_adamw(dm, case, args.steps, args.warmup, stream)
             ab = n * (R * (case.grad_bytes + 16) + 8)
@@ -793,7 +847,6 @@ def run_sweep(args):
                       f"{r2['split_gbs']:7.0f} GB/s  payload {r2['payload_bytes_per_replica'] / 1e6:8.2f} MB/replica",
                       flush=True)
             continue
-        steps, warmup = (args.steps, args.warmup) if not real_mode == "diloco" else (1, 0)
         if real_mode == "diloco":
             # one step at a time so that every timed step is (or is not) a sync step
             ms_list, l_list = [], []
