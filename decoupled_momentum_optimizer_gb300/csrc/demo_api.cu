@@ -451,7 +451,16 @@ int demo_encode_wire(const void* g, int grad_dtype, float* m, int64_t n, int chu
   if (sends && !aligned16(vals)) return DEMO_EALIGN;
   if (mode == DEMO_MODE_DEMO && !aligned16(idx)) return DEMO_EALIGN;
   const size_t gb = static_cast<size_t>(n) * (grad_dtype == DEMO_GRAD_BF16 ? 2 : 4);
-  if (overlap(g, gb, m, static_cast<size_t>(n) * 4)) return DEMO_EINVAL;
+  const size_t fb = static_cast<size_t>(n) * 4;
+  if (overlap(g, gb, m, fb)) return DEMO_EINVAL;
+  if (sends) {
+    // the payload is written: it may overlap neither the gradient, the momentum nor itself
+    size_t ib = 0;
+    const size_t vb = demo_payload_bytes_wire(mode, n, DEMO_CHUNK, k, step, diloco_period, wire, &ib);
+    if (overlap(vals, vb, g, gb) || overlap(vals, vb, m, fb)) return DEMO_EINVAL;
+    if (mode == DEMO_MODE_DEMO && (overlap(idx, ib, g, gb) || overlap(idx, ib, m, fb) || overlap(idx, ib, vals, vb)))
+      return DEMO_EINVAL;
+  }
   DeviceState* st = nullptr;
   s = current_state(&st);
   if (s != DEMO_OK) return s;
@@ -485,6 +494,17 @@ int demo_decode_update_wire(float* theta, int64_t n, int chunk, int k, float lr,
   for (int r = 0; r < R && sends; ++r) {
     if (!aligned16(vals[r])) return DEMO_EALIGN;
     if (mode == DEMO_MODE_DEMO && !aligned16(idx[r])) return DEMO_EALIGN;
+  }
+  if (sends) {
+    // theta is written while the payloads are read: no payload may overlap it (payloads are
+    // read only and may be shared between replicas)
+    size_t ib = 0;
+    const size_t vb = demo_payload_bytes_wire(mode, n, DEMO_CHUNK, k, step, diloco_period, wire, &ib);
+    const size_t fb = static_cast<size_t>(n) * 4;
+    for (int r = 0; r < R; ++r) {
+      if (overlap(theta, fb, vals[r], vb)) return DEMO_EINVAL;
+      if (mode == DEMO_MODE_DEMO && overlap(theta, fb, idx[r], ib)) return DEMO_EINVAL;
+    }
   }
   DeviceState* st = nullptr;
   s = current_state(&st);
@@ -587,6 +607,29 @@ int demo_step_pipelined(float* theta, int64_t n, int chunk, int k, float beta, f
       if (overlap(m[r], fb, g[q], gb)) return DEMO_EINVAL;
     }
     if (overlap(theta, fb, g[r], gb)) return DEMO_EINVAL;
+  }
+  if (sends) {
+    // every send and receive buffer is written: each must be apart from theta, every m and g,
+    // and every other payload buffer
+    size_t ib = 0;
+    const size_t vb = demo_payload_bytes_wire(mode, n, DEMO_CHUNK, k, step, diloco_period, wire, &ib);
+    const int nbuf = demo ? 4 : 2;
+    auto buf = [&](int r, int j) -> const void* {
+      const void* const* a[4] = {send_vals, recv_vals, send_idx, recv_idx};
+      return a[j][r];
+    };
+    auto len = [&](int j) { return j < 2 ? vb : ib; };
+    for (int r = 0; r < R; ++r) {
+      for (int j = 0; j < nbuf; ++j) {
+        const void* b = buf(r, j);
+        if (overlap(b, len(j), theta, fb)) return DEMO_EINVAL;
+        for (int q = 0; q < R; ++q) {
+          if (overlap(b, len(j), m[q], fb) || overlap(b, len(j), g[q], gb)) return DEMO_EINVAL;
+          for (int i = 0; i < nbuf; ++i)
+            if ((q != r || i != j) && overlap(b, len(j), buf(q, i), len(i))) return DEMO_EINVAL;
+        }
+      }
+    }
   }
   DeviceState* st = nullptr;
   s = current_state(&st);

@@ -149,6 +149,8 @@ size_t demo_payload_bytes(int mode, int64_t n, int chunk, int k, uint64_t step,
  *   k       1..32 (Striding: a divisor of 32; ignored by DiLoCo)
  *   beta    finite float; sign: 0 or 1; diloco_period >= 1 (DiLoCo only)
  *   seed, step: the shared index seed and the 0-based step counter
+ * vals and idx (of demo_payload_bytes' sizes) may overlap neither g, m nor
+ * each other (DEMO_EINVAL), nor may m overlap g.
  */
 int demo_encode(const void* g, int grad_dtype, float* m, int64_t n, int chunk, int k,
                 float beta, int mode, int sign, int diloco_period, uint64_t seed,
@@ -163,7 +165,8 @@ int demo_encode(const void* g, int grad_dtype, float* m, int64_t n, int chunk, i
  * DiLoCo on a non-sync step leaves theta untouched and launches nothing.
  * A DeMo index byte is used modulo 32 (it never addresses outside the chunk);
  * an index repeated within a chunk is counted once per entry, as every
- * received entry enters the scatter-mean.
+ * received entry enters the scatter-mean.  The payloads are read only and may
+ * be shared between replicas, but none may overlap theta (DEMO_EINVAL).
  */
 int demo_decode_update(float* theta, int64_t n, int chunk, int k, float lr, int mode, int R,
                        const float* const* vals, const uint8_t* const* idx,
@@ -216,6 +219,8 @@ int demo_step_wire(float* theta, int64_t n, int chunk, int k, float beta, float 
  * Random scheme hashes shard chunk indices, so blocks draw the same positions
  * as a single call.  The call only enqueues work; on return the compute stream
  * holds the whole step.  Events are taken from a pool created by demo_init.
+ * Every send and receive buffer is written, so each must be apart from theta,
+ * every g[r] and m[r] and every other payload buffer (DEMO_EINVAL).
  */
 int demo_step_pipelined(float* theta, int64_t n, int chunk, int k, float beta, float lr, int mode, int sign, int R,
                         const void* const* g, int grad_dtype, float* const* m, int diloco_period, uint64_t seed,

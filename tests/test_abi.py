@@ -113,6 +113,11 @@ def test_encode_argument_checks(L):
     assert encode_call(L, g=p(0x10004)) == EALIGN
     assert encode_call(L, vals=p(0x30008)) == EALIGN
     assert encode_call(L, m=p(0x10000)) == EINVAL  # m overlaps g
+    # the payload is written: n = 64, k = 4 gives 32 value bytes and 8 index bytes
+    assert encode_call(L, vals=p(0x20010)) == EINVAL  # values inside m
+    assert encode_call(L, vals=p(0x10000 + 240)) == EINVAL  # values overlap the end of g
+    assert encode_call(L, idx=p(0x30010)) == EINVAL  # indices inside the values
+    assert encode_call(L, idx=p(0x30020)) in (ENOTINIT, ENODEV)  # indices right after the values
     # valid arguments reach the device check
     assert encode_call(L) in (ENOTINIT, ENODEV)
     assert encode_call(L, mode=1, idx=None) in (ENOTINIT, ENODEV)
@@ -142,6 +147,33 @@ def test_decode_argument_checks(L):
     bad = (ctypes.c_void_p * 2)(0x30000, 0x40001)
     assert L.demo_decode_update(th, 64, 32, 4, 0.1, 1, 2, bad, None, 8, 0, 0, None) == EALIGN
     assert L.demo_decode_update(th, 64, 32, 4, 0.1, 0, 2, vals, idx, 8, 0, 0, None) in (ENOTINIT, ENODEV)
+    # theta (256 bytes at 0x70000) is written while the payloads are read
+    inside = (ctypes.c_void_p * 2)(0x30000, 0x70040)
+    assert L.demo_decode_update(th, 64, 32, 4, 0.1, 0, 2, inside, idx, 8, 0, 0, None) == EINVAL
+    idx_in = (ctypes.c_void_p * 2)(0x50000, 0x700f0)
+    assert L.demo_decode_update(th, 64, 32, 4, 0.1, 0, 2, vals, idx_in, 8, 0, 0, None) == EINVAL
+    shared = (ctypes.c_void_p * 2)(0x30000, 0x30000)  # read-only payloads may be shared
+    assert L.demo_decode_update(th, 64, 32, 4, 0.1, 0, 2, shared, idx, 8, 0, 0, None) in (ENOTINIT, ENODEV)
+
+
+def pipelined_call(L, sv, si, rv, ri, R=2):
+    g = (ctypes.c_void_p * R)(*[0x100000 * (r + 1) for r in range(R)])
+    m = (ctypes.c_void_p * R)(*[0x1000000 * (r + 1) for r in range(R)])
+    arr = lambda xs: (ctypes.c_void_p * R)(*xs)
+    return L.demo_step_pipelined(p(0x500000000), 64, 32, 4, 0.9, 0.1, 0, 1, R, g, 0, m, 8, 0, 0, 0, arr(sv), arr(si),
+                                 arr(rv), arr(ri), 2, None, None)
+
+
+def test_pipelined_buffer_checks(L):
+    sv, si = [0x30000, 0x31000], [0x32000, 0x33000]
+    rv, ri = [0x34000, 0x35000], [0x36000, 0x37000]
+    assert pipelined_call(L, sv, si, rv, ri) in (ENOTINIT, ENODEV)
+    assert pipelined_call(L, sv, si, sv, ri) == EINVAL  # receive values are the send values
+    assert pipelined_call(L, sv, si, [0x34000, 0x34010], ri) == EINVAL  # two replicas' receive values overlap
+    assert pipelined_call(L, sv, [0x32000, 0x31010], rv, ri) == EINVAL  # indices inside another replica's values
+    assert pipelined_call(L, sv, si, [0x500000040, 0x35000], ri) == EINVAL  # receive values inside theta
+    assert pipelined_call(L, sv, si, rv, [0x36000, 0x1000000]) == EINVAL  # receive indices inside m[0]
+    assert pipelined_call(L, [0x100000, 0x31000], si, rv, ri) == EINVAL  # send values inside g[0]
 
 
 def test_validate_payload_host(L):
