@@ -42,9 +42,13 @@ notes of the repository):
 
 Parity status: every function here is pinned by the CPU tests
 (``tests/test_oracle_pins.py``) against closed forms, a library DCT, brute
-force and published splitmix64 outputs, except the composed multi-step
-trajectory, which is "parity unpinned" beyond those per-step pins: the pages
-print no worked example.
+force and published splitmix64 outputs.  The composed multi-step trajectory is
+pinned where mathematics fixes it: with the sign off and beta = 1 every scheme
+conserves beta m + g = m' + q, so theta after T steps follows from the end
+momenta alone (DeMo with one replica; Random, Striding and DiLoCo with several),
+and Striding under a constant gradient has a closed form for any beta.  Signed
+trajectories (sign(q) sent, q fed back) have no such invariant and no worked
+example on the pages: beyond the per-step pins they are "parity unpinned".
 """
 
 import math

@@ -238,6 +238,57 @@ def pin_diloco_closed_form():
         theta, m = th2, m2
 
 
+def pin_conservation_multistep():
+    # Sign off, beta = 1: every step splits beta m + g exactly into the new momentum and the
+    # component q that is sent (the chunk transform is orthonormal, so DeMo's q in the
+    # parameter domain is the inverse transform of the kept coefficients).  Random, Striding
+    # and DiLoCo replicas all send the same slots, so Q is the plain mean of the replicas' q
+    # (DeMo is taken with one replica).  Summed over T steps the momenta telescope:
+    #     theta_T = theta_0 - lr / R * sum_r (m_r,0 + sum_t g_r,t - m_r,T).
+    r = rng(11)
+    n = 6 * C
+    lr, T = 0.25, 7
+    for mode, k, R in ((ref.MODE_DEMO, 4, 1), (ref.MODE_DEMO, 1, 1), (ref.MODE_RANDOM, 3, 3),
+                       (ref.MODE_STRIDE, 4, 2), (ref.MODE_DILOCO, 1, 2)):
+        theta0 = r.standard_normal(n)
+        m0 = [r.standard_normal(n) for _ in range(R)]
+        theta, ms = theta0.copy(), [m.copy() for m in m0]
+        gsum = [np.zeros(n) for _ in range(R)]
+        for t in range(T):
+            gs = [r.standard_normal(n) for _ in range(R)]
+            theta, ms, _ = ref.step(theta, ms, gs, beta=1.0, lr=lr, k=k, mode=mode, sign=False, seed=3,
+                                    step_idx=t, period=3)
+            for q in range(R):
+                gsum[q] += gs[q]
+        want = theta0 - lr / R * sum(m0[q] + gsum[q] - ms[q] for q in range(R))
+        assert np.abs(theta - want).max() < 1e-12 * (1.0 + np.abs(want).max()), mode
+
+
+def pin_stride_constant_gradient():
+    # Striding with a constant gradient g: position p of a chunk is sent on the steps t with
+    # t = p (mod s), s = 32 / k, carrying everything accumulated since its last send: the
+    # first send (t = p mod s) carries g (1 - b^(t+1)) / (1 - b), each later one
+    # g (1 - b^s) / (1 - b); after T steps m holds what accumulated since the last send.
+    beta, lr, T = 0.75, 0.5, 11
+    b = float(np.float32(beta))
+    for k in (1, 4, 8):
+        s = C // k
+        g = np.tile(np.linspace(-1.0, 2.0, C), 3)
+        theta, m = np.zeros(g.size), np.zeros(g.size)
+        for t in range(T):
+            theta, (m,), _ = ref.step(theta, [m], [g], beta=beta, lr=lr, k=k, mode=ref.MODE_STRIDE, sign=False,
+                                      step_idx=t)
+        geo = lambda L: (1.0 - b ** L) / (1.0 - b)  # 1 + b + ... + b^(L-1)
+        p = np.tile(np.arange(C), 3)
+        first = p % s
+        sends = np.where(first < T, (T - 1 - first) // s + 1, 0)
+        sent = np.where(sends > 0, geo(first + 1) + (sends - 1) * geo(s), 0.0)
+        last = first + (sends - 1) * s
+        left = np.where(sends > 0, T - 1 - last, T)
+        assert np.abs(theta - (-float(np.float32(lr)) * g * sent)).max() < 1e-12
+        assert np.abs(m - g * geo(left)).max() < 1e-12
+
+
 def pin_payload_bytes():
     n = 1 << 20
     for k in (1, 2, 4, 8):
@@ -255,6 +306,7 @@ ALL_PINS = [
     pin_topk_bruteforce, pin_k32_zero_residual, pin_parseval_and_projection, pin_sgd_reduction,
     pin_replica_mean_identical, pin_scatter_mean_hand_example, pin_sign_values, pin_splitmix64_published,
     pin_random_positions, pin_stride_coverage, pin_diloco_closed_form, pin_payload_bytes,
+    pin_conservation_multistep, pin_stride_constant_gradient,
 ]
 
 
@@ -362,6 +414,32 @@ def test_mutant_stride_without_offset(monkeypatch):
 def test_mutant_dropped_beta(monkeypatch):
     monkeypatch.setattr(ref, "f32", lambda x: 1.0 if x == 0.9 else float(np.float32(x)))
     assert _fails([pin_diloco_closed_form])
+
+
+def test_mutant_forward_transform_in_decode(monkeypatch):
+    orig = ref.decode_update
+
+    def bad(theta, vals_list, pos_list, lr, mode, wire=0):
+        new_theta, Q, Y, cnt = orig(theta, vals_list, pos_list, lr, mode, wire)
+        if mode == ref.MODE_DEMO:  # DCT-II where the inverse (DCT-III) belongs
+            Q = Y @ ref._D.T
+            new_theta = np.asarray(theta) - ref.f32(lr) * Q.reshape(-1)
+        return new_theta, Q, Y, cnt
+
+    monkeypatch.setattr(ref, "decode_update", bad)
+    assert _fails([pin_conservation_multistep])
+
+
+def test_mutant_momentum_not_carried(monkeypatch):
+    orig = ref.step
+
+    def bad(theta, ms, gs, **kw):
+        th, _, info = orig(theta, ms, gs, **kw)
+        return th, [np.asarray(m, dtype=np.float64).copy() for m in ms], info  # the old m returned
+
+    monkeypatch.setattr(ref, "step", bad)
+    assert _fails([pin_conservation_multistep])
+    assert _fails([pin_stride_constant_gradient])
 
 
 def test_mutant_wrong_hash_constant(monkeypatch):
