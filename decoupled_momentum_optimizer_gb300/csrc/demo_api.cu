@@ -134,11 +134,39 @@ unsigned int stride_mask(int o, int ns, int k) {
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? DEMO_OK : DEMO_ECUDA; }
 
+// DiLoCo between syncs: only the momenta move, m_r <- beta m_r + g_r, an elementwise pass
+// with no tiles (the tile kernels would compute the same FMA per element).
+template <int MAXR>
+int run_momentum(DeviceState* st, int64_t n, float beta, int R, const void* const* g, int grad_dtype,
+                 float* const* m, cudaStream_t stream) {
+  MomentumParams<MAXR> p;
+  std::memset(&p, 0, sizeof(p));
+  for (int r = 0; r < R; ++r) {
+    p.g[r] = g[r];
+    p.m[r] = m[r];
+  }
+  p.n4 = n / 4;
+  p.R = R;
+  p.beta = beta;
+  const long long want = (p.n4 + 255) / 256;
+  const int grid = static_cast<int>(want < 8LL * st->sms ? want : 8LL * st->sms);
+  const bool bf16 = grad_dtype == DEMO_GRAD_BF16;
+  cudaError_t e;
+  if constexpr (MAXR == kSmallReplicas) {
+    e = launch_momentum_small(p, bf16, grid, stream);
+  } else {
+    e = launch_momentum_large(p, bf16, grid, stream);
+  }
+  return to_status(e);
+}
+
 template <int MAXR>
 int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float lr, int mode, int sign, int R,
              const void* const* g, int grad_dtype, float* const* m, int diloco_period, uint64_t seed, uint64_t step,
              int wire, cudaStream_t stream) {
   static_assert(sizeof(StepParams<MAXR>) < 32000, "kernel parameter block too large");
+  if (mode == DEMO_MODE_DILOCO && !diloco_sync(step, diloco_period))
+    return run_momentum<MAXR>(st, n, beta, R, g, grad_dtype, m, stream);
   StepParams<MAXR> p;
   std::memset(&p, 0, sizeof(p));
   const int64_t nc = n / DEMO_CHUNK;
@@ -297,6 +325,11 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
 int run_encode(DeviceState* st, const void* g, int grad_dtype, float* m, int64_t n, int k, float beta, int mode,
                int sign, bool sends, uint64_t seed, uint64_t step, int wire, void* vals, void* idx, int64_t chunk0,
                cudaStream_t stream) {
+  if (mode == DEMO_MODE_DILOCO && !sends) {
+    const void* gs[1] = {g};
+    float* ms[1] = {m};
+    return run_momentum<kSmallReplicas>(st, n, beta, 1, gs, grad_dtype, ms, stream);
+  }
   EncodeParams p;
   std::memset(&p, 0, sizeof(p));
   const int64_t nc = n / DEMO_CHUNK;

@@ -70,6 +70,62 @@ __global__ void __launch_bounds__(kDenseThreads) dense_decode_kernel(const __gri
   }
 }
 
+// DiLoCo between syncs ("2. Replication Schemes" table: the momentum accumulates locally and
+// nothing is sent; Algorithm 1 step 3 alone): m_r <- beta m_r + g_r, one FMA per element as
+// the tile kernels compute it, so the result is bit-identical to theirs.  Every replica's
+// loads for a group of four parameters (in batches of four replicas) are issued before any
+// store, so the compiler need not order them against stores that might alias.
+__device__ __forceinline__ float4 grad4(const void* g, long long i, bool bf16) {
+  if (!bf16) return reinterpret_cast<const float4*>(g)[i];
+  const uint2 h = reinterpret_cast<const uint2*>(g)[i];
+  return make_float4(__uint_as_float(h.x << 16), __uint_as_float(h.x & 0xffff0000u), __uint_as_float(h.y << 16),
+                     __uint_as_float(h.y & 0xffff0000u));
+}
+
+template <int MAXR, bool BF16>
+__global__ void __launch_bounds__(kDenseThreads) momentum_kernel(const __grid_constant__ MomentumParams<MAXR> p) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.n4; i += stride) {
+    for (int r0 = 0; r0 < p.R; r0 += 4) {
+      float4 g[4], m[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        if (r0 + b < p.R) {
+          g[b] = grad4(p.g[r0 + b], i, BF16);
+          m[b] = reinterpret_cast<const float4*>(p.m[r0 + b])[i];
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        if (r0 + b < p.R) {
+          float4 x;
+          x.x = __fmaf_rn(p.beta, m[b].x, g[b].x);
+          x.y = __fmaf_rn(p.beta, m[b].y, g[b].y);
+          x.z = __fmaf_rn(p.beta, m[b].z, g[b].z);
+          x.w = __fmaf_rn(p.beta, m[b].w, g[b].w);
+          reinterpret_cast<float4*>(p.m[r0 + b])[i] = x;
+        }
+      }
+    }
+  }
+}
+
+cudaError_t launch_momentum_small(const MomentumParams<kSmallReplicas>& p, bool bf16, int grid, cudaStream_t st) {
+  if (bf16)
+    momentum_kernel<kSmallReplicas, true><<<grid, kDenseThreads, 0, st>>>(p);
+  else
+    momentum_kernel<kSmallReplicas, false><<<grid, kDenseThreads, 0, st>>>(p);
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_momentum_large(const MomentumParams<kMaxReplicas>& p, bool bf16, int grid, cudaStream_t st) {
+  if (bf16)
+    momentum_kernel<kMaxReplicas, true><<<grid, kDenseThreads, 0, st>>>(p);
+  else
+    momentum_kernel<kMaxReplicas, false><<<grid, kDenseThreads, 0, st>>>(p);
+  return cudaPeekAtLastError();
+}
+
 cudaError_t launch_dense_small(const DenseParams<kSmallReplicas>& p, int grid, cudaStream_t st) {
   dense_decode_kernel<kSmallReplicas><<<grid, kDenseThreads, 0, st>>>(p);
   return cudaPeekAtLastError();

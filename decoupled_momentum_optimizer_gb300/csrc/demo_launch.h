@@ -69,6 +69,19 @@ struct DenseParams {
 cudaError_t launch_dense_small(const DenseParams<kSmallReplicas>& p, int grid, cudaStream_t st);
 cudaError_t launch_dense_large(const DenseParams<kMaxReplicas>& p, int grid, cudaStream_t st);
 
+// Momentum only (DiLoCo between syncs): m_r <- beta m_r + g_r for every replica.
+template <int MAXR>
+struct MomentumParams {
+  const void* g[MAXR];  // float32 or bfloat16 [n]
+  float* m[MAXR];       // float32 [n]
+  long long n4;         // n / 4
+  int R;
+  float beta;
+};
+
+cudaError_t launch_momentum_small(const MomentumParams<kSmallReplicas>& p, bool bf16, int grid, cudaStream_t st);
+cudaError_t launch_momentum_large(const MomentumParams<kMaxReplicas>& p, bool bf16, int grid, cudaStream_t st);
+
 // Decoupled AdamW (elementwise, grid-stride over groups of four parameters).
 struct AdamWParams {
   float* theta;

@@ -5,7 +5,8 @@ large parameter block), the encode for 6, 8 and 11 (DeMo also for k = 1, 2, 4, 8
 at compile time), and the decode for four (warps, staging) shapes (DeMo also for
 k = 1, 2, 4, 8); the host picks among them by mode, k, R, gradient dtype
 and wire format (DeMo payloads too large for every shape are staged a group
-of replicas per item).  Each case below lands on a different branch of that choice
+of replicas per item).  DiLoCo steps between syncs go to an elementwise momentum
+kernel and sync steps' decode to an elementwise dense decode.  Each case below lands on a different branch of that choice
 (noted beside it) and runs the teacher-forced harness of tests/parity.py for
 two steps: split and fused bit-identical, payloads, momentum and Q against the
 oracle.  The shard has three full 32-chunk tiles and a ragged one of five chunks,
@@ -34,7 +35,9 @@ def _init():
 CASES = [
     ("stride", 4, 2, False, "f32", "fused 6 warps; encode 11; decode 11 warps"),
     ("stride", 2, 6, True, "f32", "fused 6 warps, large block; encode bf16 6; decode 11"),
-    ("diloco", 1, 2, False, "f32", "fused 6 (sync) and 8 (off-sync); encode 8; decode direct"),
+    ("diloco", 1, 2, False, "f32", "fused 6 (sync); off-sync steps: momentum kernel; encode 8; dense decode"),
+    ("diloco", 1, 5, True, "f32", "momentum kernel, bf16 gradients, replicas in batches of four (4 + 1)"),
+    ("diloco", 1, 17, False, "f32", "momentum kernel and fused step with the large parameter block"),
     ("diloco", 1, 2, True, "bf16", "encode bf16 6; 16-bit DiLoCo payload"),
     ("random", 2, 2, False, "f32", "fused 6 (k <= R + 1); encode 8"),
     ("random", 8, 2, False, "f32", "fused 8; decode 11, every replica staged"),
