@@ -51,7 +51,18 @@ def parse_args():
                    help="time only this path on the workload (R encodes + one decode, or the Decoupled AdamW step) "
                         "and print its time; for profiling those kernels")
     p.add_argument("--wire", default="f32", help="payload wire format of --only split")
-    return p.parse_args()
+    p.add_argument("--diloco-period", type=int, default=1,
+                   help="DiLoCo sync period of the timed steps: 1 (default) makes every step a sync step, a "
+                        "period longer than warm-up + steps times only the steps between syncs (momentum only)")
+    a = p.parse_args()
+    if a.diloco_period < 1 or 1 < a.diloco_period <= a.warmup + a.steps:
+        p.error("--diloco-period must be 1 or longer than --warmup + --steps (one kind of step per run)")
+    return a
+
+
+def diloco_syncs(args):
+    """Whether the run's DiLoCo steps are sync steps (all of them) or not (none)."""
+    return args.diloco_period == 1
 
 
 # ----------------------------------------------------------------------------
@@ -230,7 +241,7 @@ for t in range(max_steps + 1):  # step 0 is an untimed warm-up
     gs = [rng.standard_normal(n).astype(np.float32).astype(np.float64) * 1e-3 for _ in range(R)]
     ts = time.perf_counter()
     th, ms, _ = ref.step(th, ms, gs, beta=0.999, lr=1e-3, k=k, mode=ref.__dict__["MODE_" + mode.upper()],
-                         sign=sign, step_idx=t)
+                         sign=sign, step_idx=t, period=1 if mode == "diloco" else 8)
     if t > 0:
         el += time.perf_counter() - ts
         steps += 1
@@ -299,12 +310,14 @@ def host_cpu():
 # Reference arm: the CPU oracle, rank 0 only
 # ----------------------------------------------------------------------------
 
-def run_config(wl, R, mode, k, sign, world):
+def run_config(wl, R, mode, k, sign, world, sync=True):
     """The JSON line's `config`: the workload one GPU's step covers (both arms print the same)."""
-    step_bytes = algorithmic_bytes(wl.n, R, 2 if wl.g_dtype == "bf16" else 4, mode)
+    step_bytes = algorithmic_bytes(wl.n, R, 2 if wl.g_dtype == "bf16" else 4, mode, sync=sync)
     flush = step_bytes < 2 * L2_BYTES
     return {"workload": f"{wl.name}: {wl.n} params, R={R} resident replicas, {mode} k={k}/32, "
-                        f"sign={'on' if sign else 'off'}, grads {wl.g_dtype}",
+                        f"sign={'on' if sign else 'off'}, grads {wl.g_dtype}"
+                        + ((", every step a sync step" if sync else ", steps between syncs (momentum only)")
+                           if mode == "diloco" else ""),
             "n": wl.n, "R": R, "mode": mode, "k": k, "sign": bool(sign), "grad_dtype": wl.g_dtype,
             "parallelism": f"one shard per GPU x {world}",
             "l2": "L2 flushed (256 MB write) between steps" if flush else
@@ -330,7 +343,7 @@ def run_reference(args):
         gs = [rng.standard_normal(n).astype(np.float32).astype(np.float64) * wl.g_std for _ in range(R)]
         t0 = time.perf_counter()
         th, ms, _ = ref.step(th, ms, gs, beta=wl.beta, lr=wl.lr, k=k, mode=ref.__dict__["MODE_" + mode.upper()],
-                             sign=sign, step_idx=t)
+                             sign=sign, step_idx=t, period=args.diloco_period)
         if t >= args.warmup:
             times.append(time.perf_counter() - t0)
     per = sum(times) / len(times)
@@ -341,7 +354,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": run_config(wl, R, mode, k, sign, args.gpus),
+        "config": run_config(wl, R, mode, k, sign, args.gpus, mode != "diloco" or diloco_syncs(args)),
         "cpu_baseline": {"value": value, "unit": "params/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -543,7 +556,7 @@ def split_bytes(n, R, grad_bytes, mode, k, sync=True, wire="f32"):
     return R * (n * (grad_bytes + 8) + P) + (R * P + theta if theta else 0)
 
 
-def time_e2e(dm, case, mode, k, sign, seed, steps, dev):
+def time_e2e(dm, case, mode, k, sign, seed, steps, dev, diloco_period=8):
     """End to end through the public API: every step copies its R gradients from pinned host memory
     and reads theta back to pinned host memory.  The copies of step t+2's gradients overlap steps t and
     t+1; theta is snapshotted on the device (double-buffered) so that its read-back overlaps the next step."""
@@ -577,7 +590,7 @@ def time_e2e(dm, case, mode, k, sign, seed, steps, dev):
         for t in range(K):
             main.wait_event(e_in[t])
             dm.step(case.theta, dev_g[t % 2], case.ms, k=k, beta=wl.beta, lr=wl.lr, mode=mode, sign=sign,
-                    seed=seed, step=t0 + t, stream=main)
+                    seed=seed, step=t0 + t, diloco_period=diloco_period, stream=main)
             if t >= 2:
                 main.wait_event(e_out[t - 2])  # the snapshot buffer has been read back
             snaps[t % 2].copy_(case.theta)
@@ -634,14 +647,16 @@ def main():
     dm.init(local)
     dev = torch.device("cuda", local)
     case = Case(wl, R, dev, n_sets=3)  # three pre-drawn gradient sets per replica, cycled
-    step_bytes = algorithmic_bytes(n, R, case.grad_bytes, mode)
+    sync = mode != "diloco" or diloco_syncs(args)
+    step_bytes = algorithmic_bytes(n, R, case.grad_bytes, mode, sync=sync)
     stream = torch.cuda.current_stream()
     seed = shard_seed(0, rank)  # each GPU steps its own shard with its own index seed
 
+    period = args.diloco_period if mode == "diloco" else 8
     sampler = ClockSampler(local)
     barrier()
     step_ms, kernel_ms, _ = time_fused(dm, case, mode, k, sign, seed, args.steps, args.warmup, stream,
-                                           sampler=sampler)
+                                       sampler=sampler, diloco_period=period)
     barrier()
     if world > 1:
         tt = torch.tensor([step_ms, kernel_ms], device=dev)
@@ -652,7 +667,7 @@ def main():
     if not args.no_e2e:
         Ke = max(3, min(args.steps, 10))
         barrier()
-        e_ms, hb, db = time_e2e(dm, case, mode, k, sign, seed, Ke, dev)
+        e_ms, hb, db = time_e2e(dm, case, mode, k, sign, seed, Ke, dev, diloco_period=period)
         if world > 1:
             tt = torch.tensor([e_ms], device=dev)
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -672,7 +687,8 @@ def main():
     peak, peak_kind = measured_peaks()
     achieved = step_bytes / (kernel_ms * 1e-3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-            "traffic": ncu_traffic(args.workload, mode, k, R), "kernel": "demo::step_kernel",
+            "traffic": ncu_traffic(args.workload, mode, k, R),
+            "kernel": "demo::step_kernel" if sync else "demo::momentum_kernel",
             "algorithmic_bytes_per_launch": step_bytes,
             "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
             else "fallback 6.8 TB/s"}
@@ -689,7 +705,7 @@ def main():
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": run_config(wl, R, mode, k, sign, world),
+        "config": run_config(wl, R, mode, k, sign, world, sync),
         "achieved_gbs": achieved,
         "hbm_frac_of_peak": achieved / peak,
         "roofline": roof,
@@ -755,10 +771,11 @@ def run_only(args):
     case = Case(wl, R, torch.device("cuda", 0), n_sets=2)
     stream = torch.cuda.current_stream()
     if args.only == "split":
-        # DiLoCo: period 1, so that every timed step is a sync step (the one with a payload)
+        # DiLoCo: one kind of step per run (--diloco-period)
         ms = time_split(dm, case, mode, k, sign, 0, args.steps, args.warmup, stream, wire=args.wire,
-                        diloco_period=1 if mode == "diloco" else 8)
-        nbytes = split_bytes(case.n, R, case.grad_bytes, mode, k, wire=args.wire)
+                        diloco_period=args.diloco_period if mode == "diloco" else 8)
+        nbytes = split_bytes(case.n, R, case.grad_bytes, mode, k, wire=args.wire,
+                             sync=mode != "diloco" or diloco_syncs(args))
     else:
         ms = time_adamw(dm, case, args.steps, args.warmup, stream)
         nbytes = case.n * (R * (case.grad_bytes + 16) + 8)
@@ -789,13 +806,14 @@ def run_sweep(args):
             cache[key] = Case(wl, R, dev, n_sets=1 if wl.n >= (1 << 24) else 3)
         case = cache[key]
         n = case.n
-        # DiLoCo: period 8; "diloco" times the off-sync steps, "diloco-sync" the sync step
+        # DiLoCo: "diloco" times the steps between syncs, "diloco-sync" the sync steps; the
+        # period makes every warm-up and timed step of the row of that one kind (1: every step
+        # syncs; longer than the run: none does)
         real_mode = "diloco" if mode.startswith("diloco") else mode
         sync = mode == "diloco-sync"
-        period = 8
-        step0 = 7 if sync else 0
+        period = 1 if sync else 1 << 30
         rec = {"workload": name, "n": n, "mode": mode, "k": k, "sign": sign, "R": R, "grad_dtype": case.wl.g_dtype}
-        steps, warmup = (args.steps, args.warmup) if not real_mode == "diloco" else (1, 0)
+        steps, warmup = args.steps, args.warmup
         if "graph" in paths:
             # the split path on a small shard: R + 1 calls eagerly (host-bound) and as one replayed graph
             em = time_split(dm, case, real_mode, k, sign, 0, 10 * steps, warmup, stream)
@@ -847,27 +865,12 @@ def run_sweep(args):
                       f"{r2['split_gbs']:7.0f} GB/s  payload {r2['payload_bytes_per_replica'] / 1e6:8.2f} MB/replica",
                       flush=True)
             continue
-        if real_mode == "diloco":
-            # one step at a time so that every timed step is (or is not) a sync step
-            ms_list, l_list = [], []
-            for rep in range(6):
-                t0 = step0 + 8 * rep
-                s_ms, l_ms, _ = time_fused(dm, case, real_mode, k, sign, 0, 1, 0, stream, step0=t0,
-                                           diloco_period=period)
-                ms_list.append(s_ms)
-                l_list.append(l_ms)
-            step_ms, launch_ms = statistics.median(ms_list[1:]), statistics.median(l_list[1:])
-        else:
-            step_ms, launch_ms, _ = time_fused(dm, case, real_mode, k, sign, 0, steps, warmup, stream)
+        step_ms, launch_ms, _ = time_fused(dm, case, real_mode, k, sign, 0, steps, warmup, stream, diloco_period=period)
         fb = algorithmic_bytes(n, R, case.grad_bytes, real_mode, sync=sync or real_mode != "diloco")
         rec.update(fused_ms=step_ms, fused_params_per_s=n / (step_ms * 1e-3), fused_bytes=fb,
                    fused_gbs=fb / (launch_ms * 1e-3) / 1e9, fused_frac=fb / (launch_ms * 1e-3) / 1e9 / peak)
         if "split" in paths:
-            if real_mode == "diloco":
-                sm = statistics.median([time_split(dm, case, real_mode, k, sign, 0, 1, 0, stream,
-                                                   diloco_period=period, step0=step0 + 8 * rep) for rep in range(4)])
-            else:
-                sm = time_split(dm, case, real_mode, k, sign, 0, steps, warmup, stream)
+            sm = time_split(dm, case, real_mode, k, sign, 0, steps, warmup, stream, diloco_period=period)
             sb = split_bytes(n, R, case.grad_bytes, real_mode, k, sync=sync or real_mode != "diloco")
             rec.update(split_ms=sm, split_params_per_s=n / (sm * 1e-3), split_bytes=sb,
                        split_gbs=sb / (sm * 1e-3) / 1e9, split_frac=sb / (sm * 1e-3) / 1e9 / peak)

@@ -55,6 +55,20 @@ def test_reference_arm_other_ranks_do_no_work():
     assert r.returncode == 0 and r.stdout.strip() == ""
 
 
+def test_diloco_runs_time_one_kind_of_step():
+    r = run_bench("--impl", "reference", "--mode", "diloco", "--k", "1", "--diloco-period", "4", "--steps", "2",
+                  "--warmup", "3")
+    assert r.returncode != 0 and "--diloco-period" in r.stderr  # a period that mixes sync and non-sync steps
+    for period, words, gain in (("1", "every step a sync step", 32), ("100", "steps between syncs", 24)):
+        r = run_bench("--impl", "reference", "--mode", "diloco", "--k", "1", "--diloco-period", period, "--steps", "2",
+                      "--warmup", "3")
+        assert r.returncode == 0, r.stderr[-2000:]
+        d = json.loads(r.stdout)
+        assert words in d["config"]["workload"]
+        # the config's L2 note counts the step's bytes: R (4 + 8) per parameter, plus 8 for theta on a sync step
+        assert f"{gain * 222903552 / 1e9:.2f} GB per step" in d["config"]["l2"]
+
+
 def test_gpu_arm_fails_loudly_without_a_gpu():
     import torch
 
