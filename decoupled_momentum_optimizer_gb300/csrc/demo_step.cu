@@ -245,7 +245,9 @@ __global__ void __launch_bounds__(WARPS * 32, 1) step_kernel(const __grid_consta
 // Striding and DiLoCo sync items are a multiply-add per element; Random adds
 // k hashes per chunk once per tile, i.e. shared by R + 1 items; DeMo adds the
 // transforms and k - 1 top-k rounds per replica, and from k = 7 on it needs
-// all eleven warps to keep HBM busy.
+// all eleven warps to keep HBM busy.  (DiLoCo steps between syncs are sent to
+// the elementwise momentum kernel by the host; their rule here is kept for the
+// kernel's own generality.)
 int step_warps(int mode, int k, bool bf16, int R, bool sync) {
   if (mode == kModeStride) return kStepWarpsLight;
   if (mode == kModeDiloco) return sync ? kStepWarpsLight : kStepWarpsMid;
