@@ -1,6 +1,7 @@
 // C ABI of the DeMo shard step: argument checks, TMA tensor maps, launches.
 // The operations and their sources are described in include/demo.h.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -23,11 +24,15 @@ constexpr int64_t kMaxN = int64_t(1) << 35;  // keeps every row coordinate withi
 constexpr int kMaxBlocks = 64;  // blocks of the pipelined step
 
 struct DeviceState {
-  bool ready = false;
+  std::atomic<bool> ready{false};  // set last by demo_init (release), read by every call (acquire)
   int sms = 0;
   unsigned int* fault = nullptr;
   cudaEvent_t ev_enc[kMaxBlocks];  // block b encoded (compute stream)
   cudaEvent_t ev_xch[kMaxBlocks];  // block b exchanged (communication stream)
+  // Held while one pipelined call enqueues its work: the event pool is shared, and a
+  // wait takes the event's last record at the time it is enqueued, so calls from
+  // several host threads stay correct when their enqueue sequences do not interleave.
+  std::mutex pipeline_mu;
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -72,7 +77,7 @@ int current_state(DeviceState** out) {
     cudaGetLastError();
     return DEMO_ENOTINIT;
   }
-  if (dev < 0 || dev >= kMaxDevices || !g_dev[dev].ready) return DEMO_ENOTINIT;
+  if (dev < 0 || dev >= kMaxDevices || !g_dev[dev].ready.load(std::memory_order_acquire)) return DEMO_ENOTINIT;
   *out = &g_dev[dev];
   return DEMO_OK;
 }
@@ -410,7 +415,7 @@ int demo_init(int device) {
   if (major != 10 || minor != 3) return DEMO_ENODEV;
   if (cudaSetDevice(device) != cudaSuccess) return DEMO_ECUDA;
   DeviceState& st = g_dev[device];
-  if (st.ready) return DEMO_OK;
+  if (st.ready.load(std::memory_order_acquire)) return DEMO_OK;
   if (!g_encode) {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -437,7 +442,7 @@ int demo_init(int device) {
   }
   st.sms = sms;
   st.fault = static_cast<unsigned int*>(fault);
-  st.ready = true;
+  st.ready.store(true, std::memory_order_release);
   return DEMO_OK;
 }
 
@@ -669,6 +674,7 @@ int demo_step_pipelined(float* theta, int64_t n, int chunk, int k, float beta, f
   if (s != DEMO_OK) return s;
   cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
   cudaStream_t xs = static_cast<cudaStream_t>(comm_stream);
+  std::lock_guard<std::mutex> enqueue(st->pipeline_mu);
 
   // blocks of whole 32-chunk tiles, so every wire format's payload splits at block boundaries
   const int64_t nc = n / DEMO_CHUNK;

@@ -50,6 +50,10 @@
  *     combined in the fixed order r = 0..R-1 (no floating-point atomics).
  *   - Non-finite inputs produce unspecified values, never out-of-bounds
  *     accesses.
+ *   - Calls may come from several host threads once demo_init has returned
+ *     for the device.  demo_step_pipelined enqueues each call's work under a
+ *     per-device lock (it shares a pool of events); the kernels of calls that
+ *     overlap on the GPU are ordered only by the caller's streams.
  *   - demo_encode(_wire), demo_decode_update(_wire), demo_step(_wire),
  *     demo_step_pipelined and demo_adamw_step make only kernel launches, event
  *     records and waits and asynchronous device copies on the given streams, so

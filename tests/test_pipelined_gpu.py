@@ -71,3 +71,56 @@ def test_pipelined_argument_errors():
         dm.step_pipelined(th, [g], [m], send, send, k=4, beta=0.9, lr=0.1, blocks=65)
     with pytest.raises(dm.DemoError):
         dm.step_pipelined(th, [g], [m], None, None, k=4, beta=0.9, lr=0.1, blocks=2)
+
+
+def test_pipelined_from_two_host_threads():
+    """Two host threads step their own shards through demo_step_pipelined at the same time, each
+    on its own pair of streams (the binding releases the interpreter lock during the call, so the
+    two enqueue sequences overlap on the host).  The library serialises each call's use of its
+    event pool; every shard must end bit-identical to the same steps taken by the fused path."""
+    import threading
+
+    n, R, k, steps = RAGGED, 2, 4, 12
+    kw = dict(k=k, beta=0.99, lr=1e-2, mode="demo", sign=True, seed=0, wire="f32")
+    results, errors = {}, []
+
+    def state(tid):
+        theta = cuda_normal(n, 2e-2, 100 + tid)
+        ms = [cuda_normal(n, 1e-2, 200 + 10 * tid + r) for r in range(R)]
+        gsets = [[cuda_normal(n, 1e-3, 300 + 100 * tid + 10 * t + r) for r in range(R)] for t in range(steps)]
+        return theta, ms, gsets
+
+    states = [state(tid) for tid in range(2)]
+    torch.cuda.synchronize()
+
+    def worker(tid):
+        try:
+            theta, ms, gsets = states[tid]
+            theta, ms = theta.clone(), [m.clone() for m in ms]
+            cs, xs = torch.cuda.Stream(), torch.cuda.Stream()
+            send = [dm.payload_buffers("demo", n, k) for _ in range(R)]
+            recv = [dm.payload_buffers("demo", n, k) for _ in range(R)]
+            torch.cuda.synchronize()
+            for t in range(steps):
+                dm.step_pipelined(theta, gsets[t], ms, send, recv, step=t, blocks=7, stream=cs, comm_stream=xs, **kw)
+            cs.synchronize()
+            results[tid] = (theta, ms)
+        except Exception as e:  # reported on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(tid,)) for tid in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for tid in range(2):
+        theta, ms, gsets = states[tid]
+        theta, ms = theta.clone(), [m.clone() for m in ms]
+        for t in range(steps):
+            dm.step(theta, gsets[t], ms, step=t, **kw)
+        torch.cuda.synchronize()
+        assert same_bits(results[tid][0], theta)
+        for a, b in zip(results[tid][1], ms):
+            assert same_bits(a, b)
