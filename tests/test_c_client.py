@@ -19,14 +19,16 @@ EINVAL, ENODEV, ENOTINIT = -1, -3, -5
 
 
 @pytest.fixture(scope="module")
-def client_output(tmp_path_factory):
+def client_output():
     cc = shutil.which("gcc") or shutil.which("cc")
     if cc is None:
         pytest.skip("no C compiler")
     from decoupled_momentum_optimizer_gb300 import build
 
     pkg = os.path.dirname(build.build())
-    exe = str(tmp_path_factory.mktemp("cabi") / "abi_client")
+    out_dir = os.path.join(ROOT, "_build")  # git-ignored build folder inside the repository
+    os.makedirs(out_dir, exist_ok=True)
+    exe = os.path.join(out_dir, "abi_client")
     cmd = [cc, "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), SRC,
            "-o", exe, "-L", pkg, "-ldemo_gb300", "-Wl,-rpath," + pkg]
     r = subprocess.run(cmd, capture_output=True, text=True)
