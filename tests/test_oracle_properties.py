@@ -13,7 +13,10 @@ including exact ties, zeros, signed zeros and extreme magnitudes:
   the same for the same (seed, step, chunk), a prefix for a smaller k;
 * scatter-mean: every slot's mean times its count gives back the sum of what
   was sent to it, and slots nobody sent stay zero;
-* the ternary bit-plane format round-trips.
+* the ternary bit-plane format round-trips;
+* conservation over several steps (sign off, beta = 1; DeMo with one replica,
+  the other schemes with several): theta_T = theta_0 - lr / R * sum_r
+  (m_r,0 + sum_t g_r,t - m_r,T).
 """
 
 import numpy as np
@@ -106,3 +109,28 @@ def test_ternary_format_round_trips(data, nc, k, demo):
     assert np.array_equal(v2, vals)
     if demo:
         assert np.array_equal(i2, idx)
+
+
+@settings(max_examples=60, deadline=None)
+@given(mode=st.sampled_from([ref.MODE_DEMO, ref.MODE_RANDOM, ref.MODE_STRIDE, ref.MODE_DILOCO]),
+       R=st.integers(1, 4), kexp=st.integers(0, 5), T=st.integers(1, 6), nc=st.integers(1, 5),
+       period=st.integers(1, 4), seed=st.integers(0, 2 ** 64 - 1), data_seed=st.integers(0, 2 ** 32 - 1))
+def test_conservation_over_steps(mode, R, kexp, T, nc, period, seed, data_seed):
+    if mode == ref.MODE_DEMO:
+        R = 1  # DeMo replicas may keep different slots: the mean is then per slot, not of the whole q
+    k = 1 << kexp  # a divisor of 32, valid for every scheme
+    r = np.random.default_rng(data_seed)
+    n = nc * C
+    lr = 0.125
+    theta0 = r.standard_normal(n)
+    m0 = [r.standard_normal(n) for _ in range(R)]
+    theta, ms = theta0.copy(), [m.copy() for m in m0]
+    gsum = [np.zeros(n) for _ in range(R)]
+    for t in range(T):
+        gs = [r.standard_normal(n) for _ in range(R)]
+        theta, ms, _ = ref.step(theta, ms, gs, beta=1.0, lr=lr, k=k, mode=mode, sign=False, seed=seed, step_idx=t,
+                                period=period)
+        for q in range(R):
+            gsum[q] += gs[q]
+    want = theta0 - lr / R * sum(m0[q] + gsum[q] - ms[q] for q in range(R))
+    assert np.abs(theta - want).max() <= 1e-12 * (1.0 + np.abs(want).max())
