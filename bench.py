@@ -385,7 +385,8 @@ class Case:
 
 def time_fused(dm, case, mode, k, sign, seed, steps, warmup, stream, per_launch=True, sampler=None,
                step0=0, diloco_period=8):
-    """Mean step and mean launch time (ms) of demo_step over ``steps`` timed steps."""
+    """Mean step and mean launch time (ms) of demo_step over ``steps`` timed steps, and the
+    per-launch statistics (median, min, max) with whether L2 was flushed between steps."""
     import torch
 
     wl = case.wl
@@ -413,9 +414,11 @@ def time_fused(dm, case, mode, k, sign, seed, steps, warmup, stream, per_launch=
             ev[i][1].record(stream)
         b.record(stream)
         torch.cuda.synchronize()
-    launch = sum(x.elapsed_time(y) for x, y in ev) / steps
+    times = [x.elapsed_time(y) for x, y in ev]
+    launch = sum(times) / steps
     step = launch if flush else a.elapsed_time(b) / steps
-    return step, launch, flush
+    return step, launch, {"l2_flush": flush, "median": statistics.median(times), "min": min(times),
+                          "max": max(times)}
 
 
 class _Null:
@@ -655,8 +658,8 @@ def main():
     period = args.diloco_period if mode == "diloco" else 8
     sampler = ClockSampler(local)
     barrier()
-    step_ms, kernel_ms, _ = time_fused(dm, case, mode, k, sign, seed, args.steps, args.warmup, stream,
-                                       sampler=sampler, diloco_period=period)
+    step_ms, kernel_ms, lstats = time_fused(dm, case, mode, k, sign, seed, args.steps, args.warmup, stream,
+                                            sampler=sampler, diloco_period=period)
     barrier()
     if world > 1:
         tt = torch.tensor([step_ms, kernel_ms], device=dev)
@@ -708,6 +711,8 @@ def main():
         "config": run_config(wl, R, mode, k, sign, world, sync),
         "achieved_gbs": achieved,
         "hbm_frac_of_peak": achieved / peak,
+        "launch_ms": {"mean": kernel_ms, "median": lstats["median"], "min": lstats["min"], "max": lstats["max"],
+                      "note": "CUDA events around each timed launch; mean is the max over ranks, the rest rank 0's"},
         "roofline": roof,
         "gpu_launches": args.steps,
         "clocks": sampler.summary(),
@@ -865,8 +870,10 @@ def run_sweep(args):
                       f"{r2['split_gbs']:7.0f} GB/s  payload {r2['payload_bytes_per_replica'] / 1e6:8.2f} MB/replica",
                       flush=True)
             continue
-        step_ms, launch_ms, _ = time_fused(dm, case, real_mode, k, sign, 0, steps, warmup, stream, diloco_period=period)
+        step_ms, launch_ms, lst = time_fused(dm, case, real_mode, k, sign, 0, steps, warmup, stream,
+                                             diloco_period=period)
         fb = algorithmic_bytes(n, R, case.grad_bytes, real_mode, sync=sync or real_mode != "diloco")
+        rec.update(fused_launch_ms_median=lst["median"], fused_launch_ms_min=lst["min"])
         rec.update(fused_ms=step_ms, fused_params_per_s=n / (step_ms * 1e-3), fused_bytes=fb,
                    fused_gbs=fb / (launch_ms * 1e-3) / 1e9, fused_frac=fb / (launch_ms * 1e-3) / 1e9 / peak)
         if "split" in paths:
