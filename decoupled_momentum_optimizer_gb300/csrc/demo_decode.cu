@@ -4,7 +4,7 @@
 //
 // "DeToNATION: Decoupled Torch Network-Aware Training on Interlinked Online
 // Nodes" (Paper-Notes, AAAI 2026), method section, "1. FlexDeMo" Algorithm 1
-// steps 6-7 (the synchronised Q_t), "2. Replication Schemes" table.
+// (synchronisation and the parameter update with Q_t), "2. Replication Schemes" table.
 //
 // Per warp, theta tiles of 32 chunks stream through a two-slot TMA ring.  With
 // each theta tile the leading replicas' payload spans for the same 32 chunks

@@ -2,7 +2,7 @@
 //
 // "DeToNATION: Decoupled Torch Network-Aware Training on Interlinked Online
 // Nodes" (Paper-Notes, AAAI 2026), "2. Replication Schemes" table (DiLoCo: full
-// synchronisation every n steps) and "1. FlexDeMo" Algorithm 1 step 7.
+// synchronisation every n steps) and "1. FlexDeMo" Algorithm 1 (the parameter update).
 //
 // On a sync step every replica sends its whole momentum, so Q = Y and the update is
 // elementwise.  A grid-stride loop over groups of four parameters reads every
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(kDenseThreads) dense_decode_kernel(const __gri
 }
 
 // DiLoCo between syncs ("2. Replication Schemes" table: the momentum accumulates locally and
-// nothing is sent; Algorithm 1 step 3 alone): m_r <- beta m_r + g_r, one FMA per element as
+// nothing is sent; Algorithm 1's momentum accumulation alone): m_r <- beta m_r + g_r, one FMA per element as
 // the tile kernels compute it, so the result is bit-identical to theirs.  Every replica's
 // loads for a group of four parameters (in batches of four replicas) are issued before any
 // store, so the compiler need not order them against stores that might alias.

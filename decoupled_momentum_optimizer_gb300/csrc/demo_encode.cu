@@ -1,9 +1,11 @@
-// Split-path encode: one replica's Algorithm 1 steps 3-5 and its payload (the
+// Split-path encode: one replica's momentum accumulation, extraction and error
+// feedback (Algorithm 1) and its payload (the
 // buffer the real system would hand to the inter-node all_gather / all-reduce).
 //
 // "DeToNATION: Decoupled Torch Network-Aware Training on Interlinked Online
 // Nodes" (Paper-Notes, AAAI 2026), method section, "1. FlexDeMo" Algorithm 1
-// steps 3-5, "2. Replication Schemes" table, "3. Sign function" subsection.
+// (accumulation, extraction, removal), "2. Replication Schemes" table, "3. Sign
+// function" subsection.
 //
 // Same warp/tile organisation as the fused step: per warp, tiles of 32 chunks
 // stream through a two-slot TMA ring; each lane encodes its chunk in registers;

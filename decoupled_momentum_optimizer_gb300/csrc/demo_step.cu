@@ -4,7 +4,8 @@
 //
 // "DeToNATION: Decoupled Torch Network-Aware Training on Interlinked Online
 // Nodes" (Paper-Notes, AAAI 2026), method section, "1. FlexDeMo", Algorithm 1
-// steps 3-7, with the replication group R simulated by R resident replicas.
+// (momentum accumulation through the parameter update), with the replication
+// group R simulated by R resident replicas.
 //
 // Per warp, a tile is 32 chunks (one per lane) and is visited as R + 1 items:
 // item r < R streams g_r and m_r through TMA into a two-slot ring, computes the

@@ -5,14 +5,15 @@
  * for ONE flat float32 parameter shard and R replicas of it ("DeToNATION:
  * Decoupled Torch Network-Aware Training on Interlinked Online Nodes",
  * Paper-Notes AAAI 2026, section on the method, "1. FlexDeMo" Algorithm 1,
- * steps 3-7; "DeMo: Decoupled Momentum Optimization", abstract):
+ * from the momentum accumulation to the parameter update; "DeMo: Decoupled
+ * Momentum Optimization", abstract):
  *
- *   per replica r:  m_r <- beta m_r + g_r                       (step 3)
- *                   split m_r into 32-element chunks; select     (step 4)
- *                   q_r = the selected component; m_r <- m_r - q_r (step 5)
+ *   per replica r:  m_r <- beta m_r + g_r                 (momentum accumulation)
+ *                   split m_r into 32-element chunks; select        (extraction)
+ *                   q_r = the selected component; m_r <- m_r - q_r     (removal)
  *                   payload_r = q_r's values (ternary sign if asked)
- *   all replicas:   Y = per-slot mean of the payloads (scatter-mean), (step 6)
- *                   Q = inverse transform of Y,  theta <- theta - lr Q (step 7)
+ *   all replicas:   Y = per-slot mean of the payloads (scatter-mean)      (sync)
+ *                   Q = inverse transform of Y, theta <- theta - lr Q   (update)
  *
  * Selection ("replication scheme", same page, "2. Replication Schemes" table):
  *   DEMO_MODE_DEMO    orthonormal DCT-II of the chunk, keep the k coefficients
@@ -29,7 +30,8 @@
  *                     divide 32.  Payload: k values in j order.  Q = Y.
  *   DEMO_MODE_DILOCO  on steps with (step+1) mod diloco_period == 0 the whole
  *                     momentum is sent (32 values per chunk) and m is zeroed;
- *                     on other steps only step 3 runs and theta is untouched.
+ *                     on other steps only the momentum accumulates and theta
+ *                     is untouched.
  * The sign flag replaces every sent value by sign(v) in {-1, 0, +1} (same page,
  * "3. Sign function" subsection); m always subtracts the unsigned q.
  * The mean of a slot divides by the number of replicas that sent that slot.
@@ -143,7 +145,8 @@ size_t demo_payload_bytes(int mode, int64_t n, int chunk, int k, uint64_t step,
                           int diloco_period, size_t* idx_bytes);
 
 /*
- * demo_encode -- one replica's steps 3-5 plus its payload (the send buffer).
+ * demo_encode -- one replica's accumulation, extraction and removal, plus its
+ * payload (the send buffer).
  *   g       device, n elements of grad_dtype (read only)
  *   m       device float32 [n], momentum, updated in place to beta m + g - q
  *   vals    device float32: [n/32][k] (DeMo, Random, Striding) or [n] (DiLoCo
@@ -161,7 +164,8 @@ int demo_encode(const void* g, int grad_dtype, float* m, int64_t n, int chunk, i
                 uint64_t step, float* vals, uint8_t* idx, void* stream);
 
 /*
- * demo_decode_update -- step 6 (scatter-mean of R payloads) and step 7.
+ * demo_decode_update -- the synchronisation (scatter-mean of R payloads) and the
+ * parameter update.
  *   theta   device float32 [n], updated in place to theta - lr Q
  *   R       1..64 payloads, vals[r] / idx[r] laid out as demo_encode writes
  *           them (idx only for DeMo; pass NULL otherwise)

@@ -10,10 +10,10 @@ Sources (cited by page title and section):
 
 * "DeToNATION: Decoupled Torch Network-Aware Training on Interlinked Online
   Nodes" (Paper-Notes, AAAI 2026), section "方法详解", subsection "1. FlexDeMo
-  优化器", Algorithm 1 -- the per-shard step:
-  step 3 momentum accumulate, step 4 extract fast components, step 5 subtract
-  them from the momentum, step 6 synchronise q in the replication group R,
-  step 7 parameter update with the synchronised Q.
+  优化器", Algorithm 1 -- the per-shard step: momentum accumulation,
+  extraction of the fast components, their removal from the momentum,
+  synchronisation of q in the replication group R, and the parameter update
+  with the synchronised Q.
 * Same page, subsection "2. 复制方案 (Replication Schemes)", scheme table --
   DeMo (DCT-II, indices sent), Random (shared seed, no indices), Striding
   (equally spaced, no indices), DiLoCo (full sync every n steps).
@@ -199,7 +199,7 @@ def _ternary_sign(v):
 
 
 def encode(m, g, beta, k, mode, sign, seed=0, step=0, period=8, chunk_ids=None):
-    """Algorithm 1 steps 3-5 for one replica, plus the payload of step 6.
+    """Algorithm 1's accumulation, extraction and removal for one replica, plus its payload.
 
     m, g: float64 arrays of length n (n a multiple of 32); g holds the exact
     float32 / bfloat16 gradient values.  Returns a dict with
@@ -222,14 +222,14 @@ def encode(m, g, beta, k, mode, sign, seed=0, step=0, period=8, chunk_ids=None):
     if chunk_ids is None:
         chunk_ids = np.arange(nc, dtype=np.int64)
 
-    # Step 3: momentum accumulate, m <- beta m + Delta.
+    # Momentum accumulation: m <- beta m + Delta.
     x = (f32(beta) * m + g).reshape(nc, CHUNK)
 
     q = np.zeros_like(x)
     out = {"X": None, "idx": None, "near_tie": np.zeros(nc, dtype=bool)}
 
     if mode == MODE_DEMO:
-        # Step 4: DCT-II of every chunk, keep the top-k by magnitude.
+        # Extraction: DCT-II of every chunk, keep the top-k by magnitude.
         X = x @ _D.T  # X[c, u] = sum_i D[u, i] x[c, i]
         kept, order = topk_select(X, k)
         mag = np.abs(X)
@@ -272,7 +272,7 @@ def encode(m, g, beta, k, mode, sign, seed=0, step=0, period=8, chunk_ids=None):
     if vals is not None and sign:
         vals = _ternary_sign(vals)
 
-    # Step 5: m <- m - q (the unsigned extracted component).
+    # Removal from the momentum: m <- m - q (the unsigned extracted component).
     out["m"] = (x - q).reshape(n)
     out["q"] = q
     out["vals"] = vals
@@ -304,7 +304,7 @@ def scatter_mean(vals_list, pos_list, nc):
 
 
 def decode_update(theta, vals_list, pos_list, lr, mode, wire=0):
-    """Algorithm 1 step 6 (combine) and step 7 (theta <- theta - lr Q).
+    """Algorithm 1's synchronisation (combine) and parameter update (theta <- theta - lr Q).
 
     DeMo: Q = D^T Y (inverse DCT of the scatter-mean); the other schemes send
     values in the parameter domain, so Q = Y.  ``wire`` rounds the received

@@ -5,7 +5,8 @@ and the sent component q (the chunk transform is orthonormal, so for DeMo the
 parameter-domain q is the inverse transform of the kept coefficients), and the
 replicas of Random, Striding and DiLoCo send the same slots, so Q is the plain
 mean of the replicas' q (DeMo is taken with one replica).  Over T steps the
-momenta telescope ("DeToNATION" notes, FlexDeMo Algorithm 1, steps 3-7):
+momenta telescope ("DeToNATION" notes, FlexDeMo Algorithm 1, from the momentum
+accumulation to the parameter update):
 
     theta_T = theta_0 - lr / R * sum_r (m_r,0 + sum_t g_r,t - m_r,T).
 

@@ -7,7 +7,7 @@ including exact ties, zeros, signed zeros and extreme magnitudes:
 * top-k ("DeMo: Decoupled Momentum Optimization", abstract): k distinct slots in
   ascending order, and every kept slot beats every dropped one under the key
   (|X_u| larger, or equal with the lower index), checked pairwise;
-* error feedback (FlexDeMo Algorithm 1 steps 4-5): the transform of the new
+* error feedback (FlexDeMo Algorithm 1, extraction and removal): the transform of the new
   momentum is the old coefficients with the kept slots cleared;
 * Random positions ("2. Replication Schemes"): k distinct slots in [0, 32),
   the same for the same (seed, step, chunk), a prefix for a smaller k;
