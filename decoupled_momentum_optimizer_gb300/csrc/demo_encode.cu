@@ -300,7 +300,9 @@ int encode_warps(int mode, int k, int wire, bool bf16, int* kv) {
     if (bf16) return k == 1 ? kStepWarpsMid : kStepWarps;
     return k <= 6 ? kStepWarpsMid : kStepWarps;
   }
-  if (mode == kModeRandom) return bf16 ? kStepWarps : kStepWarpsMid;
+  // Random with float32 gradients: k <= 2 draws per chunk are light enough for six warps
+  // (1-3% faster than eight on 2^26-2^28 shards and the ViT-B shard); k = 8 wants eight.
+  if (mode == kModeRandom) return bf16 ? kStepWarps : (k <= 2 ? kStepWarpsLight : kStepWarpsMid);
   if (mode == kModeStride) return bf16 ? kStepWarpsLight : kStepWarps;
   return bf16 ? kStepWarpsLight : kStepWarpsMid;
 }

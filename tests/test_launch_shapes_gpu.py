@@ -39,7 +39,8 @@ CASES = [
     ("diloco", 1, 5, True, "f32", "momentum kernel, bf16 gradients, replicas in batches of four (4 + 1)"),
     ("diloco", 1, 17, False, "f32", "momentum kernel and fused step with the large parameter block"),
     ("diloco", 1, 2, True, "bf16", "encode bf16 6; 16-bit DiLoCo payload"),
-    ("random", 2, 2, False, "f32", "fused 6 (k <= R + 1); encode 8"),
+    ("random", 2, 2, False, "f32", "fused 6 (k <= R + 1); encode 6 (k <= 2)"),
+    ("random", 3, 2, False, "f32", "encode 8 (k > 2)"),
     ("random", 8, 2, False, "f32", "fused 8; decode 11, every replica staged"),
     ("random", 8, 2, True, "f32", "encode bf16 11"),
     ("random", 8, 5, False, "f32", "fused 8, large block; decode 8 warps / 6 KB"),
