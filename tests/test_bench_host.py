@@ -133,3 +133,26 @@ def test_clock_reasons_decoded(bench):
     assert s["reasons"] == ["sw_power_cap"] and s["sm_mhz"] == 2066 and s["samples"] == 4
     cs.samples = [(1500, 0x8 | 0x40)]
     assert cs.summary()["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+
+
+def test_profile_commands_still_parse(bench, monkeypatch):
+    """Every bench command a committed profile summary gives still parses with the current bench.py,
+    names a known workload, and runs committed files only."""
+    import glob
+    import shlex
+
+    from decoupled_momentum_optimizer_gb300 import workloads as W
+
+    found = 0
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        text = open(path).read().replace("\\\n", " ")
+        for line in text.splitlines():
+            if "python bench.py" not in line:
+                continue
+            words = shlex.split(line.split("python bench.py", 1)[1])
+            monkeypatch.setattr(sys, "argv", ["bench.py"] + words)
+            args = bench.parse_args()
+            W.workload(args.workload)
+            assert "_work" not in line, path
+            found += 1
+    assert found >= 8
