@@ -38,8 +38,10 @@
  *
  * Conventions shared by every entry point:
  *   - Pointers named as device pointers are caller-owned device memory of the
- *     current device, 16-byte aligned, not aliasing one another.  Pointer
- *     ARRAYS (g, m, vals, idx) are host arrays of R device pointers.
+ *     current device, 16-byte aligned.  A buffer a call writes may overlap no
+ *     other buffer of the call (DEMO_EINVAL); buffers it only reads may be
+ *     shared (one gradient for several replicas, one payload for several).
+ *     Pointer ARRAYS (g, m, vals, idx) are host arrays of R device pointers.
  *   - n is the shard length, a positive multiple of 32; chunk must be 32.
  *   - Calls enqueue on `stream` (a cudaStream_t; NULL = legacy default stream)
  *     and return without synchronising.  The library allocates no memory in
