@@ -8,7 +8,7 @@ import torch
 import decoupled_momentum_optimizer_gb300 as dm
 import oracle.demo_ref as ref
 
-from parity import C, chunk_close, f64
+from parity import chunk_close, f64
 
 pytestmark = pytest.mark.gpu
 
