@@ -245,3 +245,19 @@ def test_binding_refuses_cpu_tensors():
     for call in calls:
         with pytest.raises(ValueError, match="no CPU path"):
             call()
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    """Without the built library every entry point raises: there is no fallback."""
+    import torch
+
+    import decoupled_momentum_optimizer_gb300 as dm
+
+    monkeypatch.setattr(dm, "_lib", None)
+    monkeypatch.setattr(dm, "LIB_PATH", os.path.join(ROOT, "_build", "no_such_library.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        dm.lib()
+    with pytest.raises(RuntimeError, match="missing"):
+        dm.payload_bytes("demo", 64, 4)
+    with pytest.raises(RuntimeError, match="missing"):
+        dm.validate_payload(torch.zeros(8, dtype=torch.uint8), 64, 4)
