@@ -156,3 +156,28 @@ def test_profile_commands_still_parse(bench, monkeypatch):
             assert "_work" not in line, path
             found += 1
     assert found >= 8
+
+
+def test_sweep_cases_are_valid(bench):
+    """Every configuration the sweep measures names a known workload and a valid scheme, k and
+    path, so a sweep on the GPU never stops at a malformed case."""
+    from decoupled_momentum_optimizer_gb300 import workloads as W
+
+    cases = bench.sweep_cases()
+    assert len(cases) > 50
+    for name, mode, k, sign, R, paths in cases:
+        wl = W.workload(name)
+        assert 1 <= R <= 64 and wl.n % 32 == 0
+        base = "diloco" if mode.startswith("diloco") else mode
+        assert base in ("demo", "random", "stride", "diloco", "adamw")
+        if base in ("demo", "random", "stride"):
+            assert 1 <= k <= 32
+        if base == "stride":
+            assert 32 % k == 0
+        for p in paths:
+            kind = p.split(":")[0]
+            assert kind in ("fused", "split", "pipe", "adamw", "graph"), p
+            if kind in ("split", "pipe") and ":" in p:
+                assert p.split(":")[1] in ("f32", "ternary", "bf16", "f16"), p
+                if p.split(":")[1] == "ternary":
+                    assert sign, p  # the ternary format carries signed values only
