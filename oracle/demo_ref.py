@@ -43,12 +43,15 @@ notes of the repository):
 Parity status: every function here is pinned by the CPU tests
 (``tests/test_oracle_pins.py``) against closed forms, a library DCT, brute
 force and published splitmix64 outputs.  The composed multi-step trajectory is
-pinned where mathematics fixes it: with the sign off and beta = 1 every scheme
+pinned where mathematics fixes it.  Sign off: with beta = 1 every scheme
 conserves beta m + g = m' + q, so theta after T steps follows from the end
-momenta alone (DeMo with one replica; Random, Striding and DiLoCo with several),
-and Striding under a constant gradient has a closed form for any beta.  Signed
-trajectories (sign(q) sent, q fed back) have no such invariant and no worked
-example on the pages: beyond the per-step pins they are "parity unpinned".
+momenta alone, and Striding under a constant gradient has a closed form for any
+beta.  Sign on: a DeMo chunk that is one cosine of the basis keeps exactly that
+coefficient with k = 1, drains to zero momentum every step and moves theta by
+the mean of the replicas' signs times that basis vector; under a constant
+gradient every Striding, Random or DiLoCo send carries the sign of the gradient
+(an accumulation of it), so theta moves by the mean sign once per send and the
+momentum holds the geometric sum since the last send.
 """
 
 import math
@@ -393,18 +396,33 @@ WIRE_F16 = 3
 
 
 def round_bf16(x):
-    """float64 -> nearest bfloat16 (ties to even), returned as float64."""
+    """float64 -> nearest bfloat16 (ties to even), returned as float64.
+
+    bfloat16 keeps 8 significant bits and float32's exponent range: a normal
+    value in [2^(e-1), 2^e) is a multiple of 2^(e-8), and below 2^-126 the
+    spacing is the subnormal step 2^-133.  The value is rounded once, from its
+    full float64 value, to the nearest multiple of that spacing (half to even);
+    results of 2^128 or more overflow to infinity.  Scaling by a power of two is
+    exact in float64, so np.round sees the exact quotient.
+    """
     x = np.asarray(x, dtype=np.float64)
-    f = x.astype(np.float32)  # exact for the values this is used on (float32 payloads)
-    b = f.view(np.uint32).astype(np.uint64)
-    lsb = (b >> 16) & 1
-    r = ((b + 0x7FFF + lsb) >> 16) << 16
-    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+    out = x.copy()
+    fin = np.isfinite(x) & (x != 0.0)
+    _, e = np.frexp(x[fin])  # |x| in [2^(e-1), 2^e)
+    q = np.ldexp(1.0, np.maximum(e - 8, -133))
+    r = np.round(x[fin] / q) * q
+    r[np.abs(r) >= 2.0 ** 128] = np.inf * np.sign(r[np.abs(r) >= 2.0 ** 128])
+    out[fin] = r
+    return out
 
 
 def round_f16(x):
-    """float64 -> nearest float16 (ties to even), returned as float64."""
-    return np.asarray(x, dtype=np.float64).astype(np.float16).astype(np.float64)
+    """float64 -> nearest float16 (ties to even), returned as float64.
+
+    numpy converts float64 to float16 in one rounding, from the full value.
+    """
+    with np.errstate(over="ignore"):  # beyond the largest float16 the result is an infinity
+        return np.asarray(x, dtype=np.float64).astype(np.float16).astype(np.float64)
 
 
 def wire_round(vals, wire):

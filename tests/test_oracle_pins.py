@@ -289,6 +289,82 @@ def pin_stride_constant_gradient():
         assert np.abs(m - g * geo(left)).max() < 1e-12
 
 
+def _basis_row(u):
+    """Row u of the orthonormal DCT-II basis, written out from its definition."""
+    a = math.sqrt((1.0 if u == 0 else 2.0) / C)
+    return np.array([a * math.cos(math.pi * (2 * i + 1) * u / (2 * C)) for i in range(C)])
+
+
+def pin_signed_demo_basis_chunks():
+    # Sign on, k = 1, every gradient chunk a multiple of ONE basis cosine u0 (its own per chunk):
+    # the chunk's only nonzero coefficient is u0, so top-1 keeps u0 and the removal leaves m = 0
+    # (for any beta); the replica sends sign(a) at u0, the mean over replicas is the mean of the
+    # signs, and Q is that mean times basis row u0.  Over T steps, per chunk c:
+    #     theta_T = theta_0 - lr * sum_t mean_r sign(a_{r,t,c}) * row(u0_c),   m_r = 0 throughout.
+    # Three replicas with independent amplitudes make the mean of signs take the values
+    # {+-1, +-1/3}, which a sign taken after the mean (or no sign) would not give.
+    r = rng(31)
+    u0 = [0, 1, 5, 17, 31, 0, 8]
+    nc, R, T = len(u0), 3, 6
+    n = nc * C
+    rows = [_basis_row(u) for u in u0]
+    cosv = [np.array([math.cos(math.pi * (2 * i + 1) * u / (2 * C)) for i in range(C)]) for u in u0]
+    for beta in (0.5, 0.999):
+        theta0 = r.standard_normal(n)
+        theta, ms = theta0.copy(), [np.zeros(n) for _ in range(R)]
+        want = theta0.copy()
+        lr = 0.25
+        for t in range(T):
+            a = r.standard_normal((R, nc))
+            gs = [np.concatenate([a[q, c] * cosv[c] for c in range(nc)]) for q in range(R)]
+            theta, ms, info = ref.step(theta, ms, gs, beta=beta, lr=lr, k=1, mode=ref.MODE_DEMO, sign=True,
+                                       step_idx=t)
+            for c in range(nc):
+                want[c * C:(c + 1) * C] -= float(np.float32(lr)) * np.sign(a[:, c]).mean() * rows[c]
+                for q in range(R):
+                    assert list(info["encodes"][q]["idx"][c]) == [u0[c]]
+            for q in range(R):
+                assert np.abs(ms[q]).max() < 1e-12 * np.abs(a).max()
+        assert np.abs(theta - want).max() < 1e-12
+
+
+def pin_signed_constant_gradient():
+    # Sign on, a constant gradient w_r * g per replica (w = 1, 0.5, -2): a send at position p
+    # carries w_r g_p times 1 + b + ... + b^(L-1) (L steps accumulated since its last send), whose
+    # sign is sign(w_r g_p); every replica sends the same positions, so each send moves theta by
+    # lr * mean_r sign(w_r) * sign(g_p) = lr * sign(g_p) / 3, and m_r holds w_r g_p times the
+    # geometric sum of the steps since the last send.  Positions per step: Striding o + s j with
+    # o = t mod s, s = 32 / k; Random the shared-seed draws; DiLoCo all 32 on sync steps.
+    beta, lr, T = 0.75, 0.5, 13
+    b = float(np.float32(beta))
+    w = [1.0, 0.5, -2.0]
+    geo = lambda L: (1.0 - b ** L) / (1.0 - b)
+    g = np.concatenate([np.linspace(-1.0, 2.0, C), np.linspace(3.0, -0.5, C), -np.linspace(0.1, 1.0, C)])
+    nc = g.size // C
+    for mode, k in ((ref.MODE_STRIDE, 1), (ref.MODE_STRIDE, 4), (ref.MODE_STRIDE, 8), (ref.MODE_RANDOM, 3),
+                    (ref.MODE_DILOCO, 1)):
+        theta, ms = np.zeros(g.size), [np.zeros(g.size) for _ in w]
+        sends = np.zeros(g.size)
+        last = np.full(g.size, -1)
+        for t in range(T):
+            theta, ms, _ = ref.step(theta, ms, [wq * g for wq in w], beta=beta, lr=lr, k=k, mode=mode, sign=True,
+                                    seed=5, step_idx=t, period=4)
+            for c in range(nc):
+                if mode == ref.MODE_STRIDE:
+                    pos = [(t % (C // k)) + (C // k) * j for j in range(k)]
+                elif mode == ref.MODE_RANDOM:
+                    pos = ref.random_positions(5, t, c, k)
+                else:
+                    pos = list(range(C)) if (t + 1) % 4 == 0 else []
+                for p in pos:
+                    sends[c * C + p] += 1
+                    last[c * C + p] = t
+        assert np.abs(theta - (-float(np.float32(lr)) * sends * np.sign(g) / 3.0)).max() < 1e-12, mode
+        left = T - 1 - last  # steps accumulated since the last send (all T when never sent)
+        for wq, m in zip(w, ms):
+            assert np.abs(m - wq * g * geo(left)).max() < 1e-12, mode
+
+
 def pin_payload_bytes():
     n = 1 << 20
     for k in (1, 2, 4, 8):
@@ -306,7 +382,8 @@ ALL_PINS = [
     pin_topk_bruteforce, pin_k32_zero_residual, pin_parseval_and_projection, pin_sgd_reduction,
     pin_replica_mean_identical, pin_scatter_mean_hand_example, pin_sign_values, pin_splitmix64_published,
     pin_random_positions, pin_stride_coverage, pin_diloco_closed_form, pin_payload_bytes,
-    pin_conservation_multistep, pin_stride_constant_gradient,
+    pin_conservation_multistep, pin_stride_constant_gradient, pin_signed_demo_basis_chunks,
+    pin_signed_constant_gradient,
 ]
 
 
@@ -391,6 +468,43 @@ def test_mutant_signed_feedback(monkeypatch):
 
     monkeypatch.setattr(ref, "encode", bad)
     assert _fails([pin_parseval_and_projection])
+    assert _fails([pin_signed_demo_basis_chunks])
+
+
+def test_mutant_signed_feedback_in_positional_schemes(monkeypatch):
+    # Striding / Random / DiLoCo: the removal leaves x - sign(x) at the sent positions instead of 0
+    orig = ref.encode
+
+    def bad(m, g, beta, k, mode, sign, **kw):
+        out = orig(m, g, beta, k, mode, sign, **kw)
+        if sign and mode != ref.MODE_DEMO and out["pos"] is not None:
+            x = (ref.f32(beta) * np.asarray(m) + np.asarray(g)).reshape(-1, C)
+            mm = out["m"].reshape(-1, C).copy()
+            rows = np.arange(x.shape[0])[:, None]
+            mm[rows, out["pos"]] = x[rows, out["pos"]] - np.sign(x[rows, out["pos"]])
+            out["m"] = mm.reshape(-1)
+        return out
+
+    monkeypatch.setattr(ref, "encode", bad)
+    assert _fails([pin_signed_constant_gradient])
+
+
+def test_mutant_sign_after_the_mean(monkeypatch):
+    # the replicas send unsigned values and the receiver takes the sign of their mean
+    orig = ref.step
+
+    def bad(theta, ms, gs, *, sign, lr, mode, **kw):
+        th, m2, info = orig(theta, ms, gs, sign=False, lr=lr, mode=mode, **kw)
+        if sign:
+            Y = np.sign(info["Y"])
+            Q = Y @ ref._D if mode == ref.MODE_DEMO else Y
+            th = np.asarray(theta, dtype=np.float64) - ref.f32(lr) * Q.reshape(-1)
+        return th, m2, info
+
+    monkeypatch.setattr(ref, "step", bad)
+    assert _fails([pin_signed_demo_basis_chunks])
+    assert _fails([pin_signed_constant_gradient])
+    assert not _fails([pin_conservation_multistep, pin_stride_constant_gradient])  # unsigned pins cannot see it
 
 
 def test_mutant_no_removal_in_fisher_yates(monkeypatch):
@@ -428,6 +542,7 @@ def test_mutant_forward_transform_in_decode(monkeypatch):
 
     monkeypatch.setattr(ref, "decode_update", bad)
     assert _fails([pin_conservation_multistep])
+    assert _fails([pin_signed_demo_basis_chunks])
 
 
 def test_mutant_momentum_not_carried(monkeypatch):
@@ -440,6 +555,7 @@ def test_mutant_momentum_not_carried(monkeypatch):
     monkeypatch.setattr(ref, "step", bad)
     assert _fails([pin_conservation_multistep])
     assert _fails([pin_stride_constant_gradient])
+    assert _fails([pin_signed_constant_gradient])
 
 
 def test_mutant_wrong_hash_constant(monkeypatch):
@@ -529,6 +645,58 @@ def test_16bit_rounding_matches_torch():
     th = torch.tensor(x, dtype=torch.float32).to(torch.float16).to(torch.float64).numpy()
     assert np.array_equal(ref.round_bf16(x), tb)
     assert np.array_equal(ref.round_f16(x), th)
+
+
+def _nearest_in_table(x, table_bits, as_float):
+    """Brute force: the nearest finite value of a 16-bit format to each float64 x, ties to the
+    pattern with an even last bit; values beyond the largest finite one by half a step or more
+    become infinities.  ``table_bits`` holds every bit pattern of the format."""
+    vals = as_float(table_bits)
+    fin = np.isfinite(vals)
+    bits, vals = table_bits[fin], vals[fin]
+    order = np.lexsort((bits, vals))  # -0 and +0 share a value: the sort keeps both
+    bits, vals = bits[order], vals[order]
+    top = vals.max()
+    step_top = top - vals[vals < top].max()
+    out = np.empty_like(x)
+    for i, v in enumerate(x):
+        if abs(v) >= top + step_top / 2:
+            out[i] = math.copysign(math.inf, v)
+            continue
+        d = np.abs(vals - v)
+        best = d.min()
+        cand = np.flatnonzero(d == best)
+        even = [c for c in cand if bits[c] % 2 == 0]
+        pick = even[0] if even else cand[0]
+        out[i] = vals[pick]
+        if out[i] == 0.0:
+            out[i] = math.copysign(0.0, v)
+    return out
+
+
+def test_16bit_rounding_from_float64_by_brute_force():
+    # The oracle rounds a float64 payload value to bf16 / fp16 in ONE rounding.  Rounding it to
+    # float32 first would differ wherever the float32 value lands on a 16-bit midpoint: x =
+    # 1 + 2^-8 + 2^-30 is above the bf16 midpoint between 1 and 1 + 2^-7 (so it rounds up), but
+    # float32 drops the 2^-30 and the midpoint then rounds to the even 1.0.
+    import torch
+
+    pats = np.arange(1 << 16, dtype=np.uint32)
+    bf = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    hf = lambda b: b.astype(np.uint16).view(np.float16).astype(np.float64)
+    r = rng(23)
+    x = np.concatenate([r.standard_normal(300) * s for s in (1e-40, 1e-3, 1.0, 1e4)])
+    mids = [1 + 2 ** -8, 1 + 2 ** -8 + 2 ** -30, 1 + 2 ** -8 - 2 ** -30, 1 + 3 * 2 ** -8, -(1 + 2 ** -8 + 2 ** -30),
+            1 + 2 ** -11, 1 + 2 ** -11 + 2 ** -40, 1 + 2 ** -11 - 2 ** -40, 2.0 ** -134, 2.0 ** -134 * 1.0000001,
+            2.0 ** -25, 2.0 ** -25 * 1.0000001, 65504.0, 65519.99, 65520.0, 3.3895313892515355e38, 3.4e38, 0.0, -0.0]
+    x = np.concatenate([x, mids])
+    with np.errstate(invalid="ignore"):  # the tables hold NaN patterns, dropped by _nearest_in_table
+        assert np.array_equal(ref.round_bf16(x), _nearest_in_table(x, pats, bf))
+        assert np.array_equal(ref.round_f16(x), _nearest_in_table(x, pats, hf))
+    assert ref.round_bf16(np.array([1 + 2 ** -8 + 2 ** -30]))[0] == 1 + 2 ** -7
+    # the double-rounding route (float32 first, then bf16, as torch converts) gives 1.0 there
+    assert torch.tensor([1 + 2 ** -8 + 2 ** -30], dtype=torch.float64).float().to(torch.bfloat16).item() == 1.0
+    assert np.isnan(ref.round_bf16(np.array([np.nan]))[0])
 
 
 def test_ternary_wire_step_equals_signed_f32_step():
