@@ -17,7 +17,13 @@ For each step the harness
   own Q to TOL relative to the mean of the summands' magnitudes (a mean of
   nearly opposite values cancels float32 rounding up); m to TOL
   relative to the larger of that and the chunk's momentum before the
-  subtraction (k = 32 cancels it to rounding noise), and the theta update to within one float32 rounding of theta - lr Q.
+  subtraction (k = 32 cancels it to rounding noise), and the theta update to
+  within one float32 rounding of theta - lr Q.
+
+Paths whose payloads stay inside the library (the pipelined step and its
+no-allocation variant) are checked with ``oracle_step`` + ``check_outcome``:
+the same m, Q and theta checks, with Q read by running the path once more on a
+zero theta with lr = -1.
 """
 
 import numpy as np
@@ -96,6 +102,41 @@ def gpu_fused(theta, ms, gs, *, k, beta, lr, mode, sign, seed, step, period, wir
     return th2, ms2
 
 
+def gpu_pipelined(theta, gs, ms, *, k, beta, lr, mode, sign, seed, step, period, wire, blocks, comm, static=False):
+    """One demo_step_pipelined call (payload buffers made here) or, with ``static``, one call of its
+    no-allocation variant, updating theta and ms in place."""
+    kw = dict(k=k, beta=beta, lr=lr, mode=mode, sign=sign, seed=seed, step=step, diloco_period=period, wire=wire,
+              blocks=blocks, comm_stream=comm)
+    if static:
+        dm.step_pipelined_static(theta, gs, ms, **kw)
+        return
+    n = theta.numel()
+    send = [dm.payload_buffers(mode, n, k, step=step, diloco_period=period, wire=wire) for _ in ms]
+    recv = [dm.payload_buffers(mode, n, k, step=step, diloco_period=period, wire=wire) for _ in ms]
+    dm.step_pipelined(theta, gs, ms, send if send[0][0] is not None else None,
+                      recv if recv[0][0] is not None else None, **kw)
+
+
+def check_pipelined_step(theta, ms, gs, *, k, beta, lr, mode, sign, seed, step, period, wire, blocks, comm,
+                         static=False):
+    """One teacher-forced pipelined step against the oracle: the step runs on a copy of the state
+    with a zero theta and lr = -1 (which leaves theta = Q exactly) and on the state itself, which
+    it updates in place; then m, Q and theta are compared with the oracle's step from the same
+    start (check_outcome)."""
+    rows, el_t, th0, m0, g0, info = oracle_step(theta, ms, gs, k=k, beta=beta, lr=lr, mode=mode, sign=sign,
+                                                seed=seed, step=step, period=period, wire=wire)
+    kw = dict(k=k, beta=beta, mode=mode, sign=sign, seed=seed, step=step, period=period, wire=wire, blocks=blocks,
+              comm=comm, static=static)
+    Q = torch.zeros_like(theta)
+    gpu_pipelined(Q, gs, [m.clone() for m in ms], lr=-1.0, **kw)
+    gpu_pipelined(theta, gs, ms, lr=lr, **kw)
+    torch.cuda.synchronize()
+    pick = lambda t: f64(t.index_select(0, el_t))
+    check_outcome(info, m0, g0, th0, [pick(m) for m in ms], pick(Q), pick(theta), beta=beta, lr=lr, sign=sign,
+                  wire=wire)
+    return int(info["near_tie"].sum())
+
+
 def host_payload(vals, idx, *, wire, mode, nc, k, rows):
     """The GPU's payload decoded on the host: (values [rows][kv] float64, indices [rows][k] or None)."""
     kv = C if mode == "diloco" else k
@@ -119,6 +160,53 @@ def same_bits(a, b):
     return torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
+def check_outcome(info, m0, g0, th0, m_gpu, Q_gpu, th_gpu, *, beta, lr, sign, wire="f32", excl=None, tol=TOL):
+    """The GPU's new momenta, Q and theta of one step against the oracle's step ``info`` from the
+    same start (all float64 arrays over the same chunks; chunks flagged in ``excl`` are skipped).
+
+    m to TOL relative to the larger of the new m and the momentum before the subtraction;
+    Q to TOL (plus one rounding unit of a 16-bit wire format when unsigned) relative to the
+    mean of the summands' magnitudes; theta within one float32 rounding of theta - lr Q_gpu.
+    """
+    R = len(m0)
+    nrows = th0.size // C
+    if excl is None:
+        excl = info["near_tie"].copy()
+    wrel, wabs = WIRE_REL[wire], WIRE_ABS[wire]
+    for r in range(R):
+        x = ref.f32(beta) * m0[r] + g0[r]  # the momentum before the subtraction of q
+        mg = m_gpu[r].reshape(nrows, C)
+        bad, worst = chunk_close(mg, info["encodes"][r]["m"], tol, excl, scale=x)
+        assert not bad.any(), f"m[{r}] differs in {bad.sum()} chunks (worst {worst:.3g})"
+    # the mean of R replicas can cancel, so the error scale is the mean of |values|
+    Yabs, _ = ref.scatter_mean([None if e["vals"] is None else np.abs(e["vals"]) for e in info["encodes"]],
+                               [e["pos"] for e in info["encodes"]], nrows)
+    if wabs and not sign:  # the fp16 floor is absolute: compare it against the summand scale
+        Yabs = np.maximum(Yabs, wabs / max(tol + wrel, 1e-30))
+    bad, worst = chunk_close(Q_gpu, info["Q"], tol + (0.0 if sign else wrel), excl, scale=Yabs)
+    assert not bad.any(), f"Q differs in {bad.sum()} chunks (worst {worst:.3g})"
+    # theta' = theta - lr Q with one float32 rounding (checked to one ulp)
+    want = (th0 - ref.f32(lr) * Q_gpu).astype(np.float32)
+    got = th_gpu.astype(np.float32)
+    ulp = np.spacing(np.maximum(np.abs(want), np.abs(got)).astype(np.float32))
+    assert (np.abs(got.astype(np.float64) - want.astype(np.float64)) <= ulp).all(), "theta update is not theta - lr Q"
+
+
+def oracle_step(theta, ms, gs, *, k, beta, lr, mode, sign, seed=0, step=0, period=8, rows=None, wire="f32"):
+    """The oracle's step on ``rows`` (default all chunks) of the GPU tensors' current values.
+
+    Returns (rows, element index tensor, th0, m0, g0, info) with the inputs as float64 arrays."""
+    nc = theta.numel() // C
+    rows = np.arange(nc) if rows is None else np.asarray(rows, dtype=np.int64)
+    el = (rows[:, None] * C + np.arange(C)[None, :]).reshape(-1)
+    el_t = torch.from_numpy(el).to(theta.device)
+    pick = lambda t: f64(t.index_select(0, el_t))
+    th0, m0, g0 = pick(theta), [pick(m) for m in ms], [pick(g) for g in gs]
+    _, _, info = ref.step(th0, m0, g0, beta=beta, lr=lr, k=k, mode=ref.__dict__["MODE_" + mode.upper()], sign=sign,
+                          seed=seed, step_idx=step, period=period, chunk_ids=rows, wire=dm.WIRES[wire])
+    return rows, el_t, th0, m0, g0, info
+
+
 def check_step(theta, ms, gs, *, k, beta, lr, mode, sign, seed=0, step=0, period=8, rows=None, tol=TOL,
                stats=None, wire="f32"):
     """One teacher-forced step (see module docstring); returns the fused path's new (theta, ms)."""
@@ -134,21 +222,12 @@ def check_step(theta, ms, gs, *, k, beta, lr, mode, sign, seed=0, step=0, period
     for r in range(R):
         assert same_bits(ms_f[r], ms_s[r]), f"fused and split m[{r}] differ"
 
-    if rows is None:
-        rows = np.arange(nc)
-    rows = np.asarray(rows, dtype=np.int64)
-    el = (rows[:, None] * C + np.arange(C)[None, :]).reshape(-1)
-    el_t = torch.from_numpy(el).to(theta.device)
+    rows, el_t, th0, m0, g0, info = oracle_step(theta, ms, gs, k=k, beta=beta, lr=lr, mode=mode, sign=sign,
+                                                seed=seed, step=step, period=period, rows=rows, wire=wire)
 
     def pick(t):
         return f64(t.index_select(0, el_t))
 
-    th0 = pick(theta)
-    m0 = [pick(m) for m in ms]
-    g0 = [pick(g) for g in gs]
-    th1, m1, info = ref.step(th0, m0, g0, beta=beta, lr=lr, k=k, mode=ref.__dict__["MODE_" + mode.upper()],
-                             sign=sign, seed=seed, step_idx=step, period=period, chunk_ids=rows,
-                             wire=dm.WIRES[wire])
     wrel, wabs = WIRE_REL[wire], WIRE_ABS[wire]
     excl = info["near_tie"].copy()
     nrows = len(rows)
@@ -189,10 +268,6 @@ def check_step(theta, ms, gs, *, k, beta, lr, mode, sign, seed=0, step=0, period
                 ov = enc["vals"]
                 err = np.abs(gv - ov) <= wrel * np.abs(ov) + wabs + tol * np.abs(ov).max(1, keepdims=True)
                 assert err.all(), "DiLoCo payload differs"
-        x = ref.f32(beta) * m0[r] + g0[r]  # the momentum before the subtraction of q
-        bad, worst = chunk_close(mg, m1[r], tol, excl, scale=x)
-        assert not bad.any(), f"m[{r}] differs in {bad.sum()} chunks (worst {worst:.3g})"
-
     Qg = pick(Q)
     # decode alone: the oracle's scatter-mean and inverse transform of the GPU's own payloads
     gpu_vals, gpu_pos = [], []
@@ -206,19 +281,8 @@ def check_step(theta, ms, gs, *, k, beta, lr, mode, sign, seed=0, step=0, period
                                     ref.__dict__["MODE_" + mode.upper()])
     bad, worst = chunk_close(Qg, Qd, tol)
     assert not bad.any(), f"decode of the GPU payloads: Q differs in {bad.sum()} chunks (worst {worst:.3g})"
-    # end to end: the mean of R replicas can cancel, so the error scale is the mean of |values|
-    Yabs, _ = ref.scatter_mean([None if e["vals"] is None else np.abs(e["vals"]) for e in info["encodes"]],
-                               [e["pos"] for e in info["encodes"]], nrows)
-    if wabs and not sign:  # the fp16 floor is absolute: compare it against the summand scale
-        Yabs = np.maximum(Yabs, wabs / max(tol + wrel, 1e-30))
-    bad, worst = chunk_close(Qg, info["Q"], tol + (0.0 if sign else wrel), excl, scale=Yabs)
-    assert not bad.any(), f"Q differs in {bad.sum()} chunks (worst {worst:.3g})"
-
-    # theta' = theta - lr Q with one float32 rounding (checked to one ulp)
-    want = (th0 - ref.f32(lr) * Qg).astype(np.float32)
-    got = pick(th_f).astype(np.float32)
-    ulp = np.spacing(np.maximum(np.abs(want), np.abs(got)).astype(np.float32))
-    assert (np.abs(got.astype(np.float64) - want.astype(np.float64)) <= ulp).all(), "theta update is not theta - lr Q"
+    check_outcome(info, m0, g0, th0, [pick(m) for m in ms_f], Qg, pick(th_f), beta=beta, lr=lr, sign=sign,
+                  wire=wire, excl=excl, tol=tol)
 
     if stats is not None:
         stats.setdefault("near_tie", 0)

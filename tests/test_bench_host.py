@@ -46,7 +46,7 @@ def test_reference_arm_prints_one_contract_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     cfg = d["config"]
-    assert cfg["n"] == 222903552 and cfg["R"] == 2 and cfg["mode"] == "demo" and cfg["k"] == 4 and cfg["sign"]
+    assert cfg["n"] == 1 << 30 and cfg["R"] == 2 and cfg["mode"] == "demo" and cfg["k"] == 4 and cfg["sign"]
 
 
 def test_reference_arm_other_ranks_do_no_work():
@@ -66,7 +66,7 @@ def test_diloco_runs_time_one_kind_of_step():
         d = json.loads(r.stdout)
         assert words in d["config"]["workload"]
         # the config's L2 note counts the step's bytes: R (4 + 8) per parameter, plus 8 for theta on a sync step
-        assert f"{gain * 222903552 / 1e9:.2f} GB per step" in d["config"]["l2"]
+        assert f"{gain * (1 << 30) / 1e9:.2f} GB per step" in d["config"]["l2"]
 
 
 def test_gpu_arm_fails_loudly_without_a_gpu():

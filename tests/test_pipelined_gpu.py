@@ -1,17 +1,19 @@
 """The split path with its exchange overlapped on a second stream
-(demo_step_pipelined) is bit-identical to the fused step for every scheme,
-wire format and block count."""
+(demo_step_pipelined): teacher-forced against the float64 oracle for every
+scheme and wire format with 1, 3 and 64 blocks (ragged last blocks included),
+and bit-identical to the fused step."""
 
 import pytest
 import torch
 
 import decoupled_momentum_optimizer_gb300 as dm
 
-from parity import same_bits
+from parity import check_pipelined_step, same_bits
 
 pytestmark = pytest.mark.gpu
 
 RAGGED = 32 * (31 * 32 + 8)
+N64 = 32 * (63 * 32 + 5)  # 63 full tiles and a 64th of 5 chunks: 64 blocks are one tile each
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -57,6 +59,34 @@ def test_pipelined_equals_fused(mode, k, sign, R, wire, blocks):
         assert same_bits(th_f, th_p)
         for a, b in zip(ms_f, ms_p):
             assert same_bits(a, b)
+
+
+# mode, k, sign, R, wire, blocks, n, steps (two in a row; DiLoCo with period 8: off-sync, then sync)
+ORACLE_CASES = [
+    ("demo", 4, True, 2, "f32", 1, RAGGED, (0, 1)),
+    ("demo", 4, True, 3, "ternary", 64, N64, (0, 1)),
+    ("demo", 2, False, 2, "bf16", 3, RAGGED, (0, 1)),
+    ("demo", 8, False, 2, "f16", 64, N64, (0, 1)),
+    ("demo", 1, True, 5, "f32", 3, RAGGED, (0, 1)),  # R = 5: the kernels' large parameter block
+    ("random", 8, True, 2, "ternary", 3, RAGGED, (0, 1)),
+    ("random", 1, False, 3, "f32", 64, N64, (0, 1)),
+    ("stride", 4, True, 2, "bf16", 1, RAGGED, (2, 3)),
+    ("diloco", 1, False, 2, "f32", 3, RAGGED, (6, 7)),
+    ("diloco", 1, True, 3, "ternary", 64, N64, (6, 7)),
+]
+
+
+@pytest.mark.parametrize("mode,k,sign,R,wire,blocks,n,steps", ORACLE_CASES, ids=lambda v: str(v))
+def test_pipelined_matches_oracle(mode, k, sign, R, wire, blocks, n, steps):
+    comm = torch.cuda.Stream()
+    theta = cuda_normal(n, 2e-2, 1)
+    ms = [cuda_normal(n, 1e-2, 10 + r) for r in range(R)]
+    ties = 0
+    for step in steps:
+        gs = [cuda_normal(n, 1e-3, 20 + 3 * r + step) for r in range(R)]
+        ties += check_pipelined_step(theta, ms, gs, k=k, beta=0.99, lr=1e-2, mode=mode, sign=sign, seed=3,
+                                     step=step, period=8, wire=wire, blocks=blocks, comm=comm)
+    assert ties <= 0.01 * (n // 32) * len(steps)
 
 
 def test_pipelined_argument_errors():

@@ -15,6 +15,8 @@ import torch
 
 import decoupled_momentum_optimizer_gb300 as dm
 
+from parity import check_pipelined_step
+
 pytestmark = pytest.mark.gpu
 
 ENOSPACE = -6
@@ -46,6 +48,31 @@ def test_static_scratch_matches_pipelined_on_two_calls(mode, k, sign, wire):
         assert torch.equal(theta_a, theta_b)
         for a, b in zip(ms_a, ms_b):
             assert torch.equal(a, b)
+    assert dm.device_fault() == 0
+
+
+# mode, k, sign, R, wire, steps (two in a row; DiLoCo with period 8: no payload, then a full one)
+ORACLE_CASES = [
+    ("demo", 4, True, 3, "f32", (0, 1)),
+    ("demo", 2, False, 4, "bf16", (0, 1)),
+    ("random", 8, True, 3, "ternary", (0, 1)),
+    ("stride", 2, True, 5, "f16", (1, 2)),
+    ("diloco", 1, False, 3, "f32", (6, 7)),
+    ("diloco", 1, True, 2, "ternary", (6, 7)),
+]
+
+
+@pytest.mark.parametrize("mode,k,sign,R,wire,steps", ORACLE_CASES, ids=lambda v: str(v))
+def test_static_scratch_matches_oracle(mode, k, sign, R, wire, steps):
+    dm.init(0)
+    n = 32 * (45 * 32 + 17)  # a ragged last tile
+    comm = torch.cuda.Stream()
+    theta = cuda_normal(n, 2e-2, 5)
+    ms = [cuda_normal(n, 1e-2, 30 + r) for r in range(R)]
+    for step in steps:
+        gs = [cuda_normal(n, 1e-3, 40 + 7 * r + step) for r in range(R)]
+        check_pipelined_step(theta, ms, gs, k=k, beta=0.99, lr=1e-2, mode=mode, sign=sign, seed=11, step=step,
+                             period=8, wire=wire, blocks=5, comm=comm, static=True)
     assert dm.device_fault() == 0
 
 
