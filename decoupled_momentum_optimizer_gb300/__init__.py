@@ -58,6 +58,7 @@ _SIGS = {
                                                   ctypes.c_int, _c_vp, _c_vp]),
     "demo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "demo_device_fault": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint)]),
+    "demo_test_stall_next_launch": (ctypes.c_int, [ctypes.c_longlong]),
 }
 
 _lib = None
@@ -358,3 +359,10 @@ def device_fault():
     code = ctypes.c_uint(0)
     _check(lib().demo_device_fault(ctypes.byref(code)), "demo_device_fault")
     return code.value
+
+
+def test_stall_next_launch(item=0):
+    """demo_test_stall_next_launch: the next tile-kernel launch on the current device makes the
+    load of its first warp's item ``item`` never complete, so that warp's bounded wait gives up
+    and sets the fault word (read by device_fault).  For tests of the failure path."""
+    _check(lib().demo_test_stall_next_launch(item), "demo_test_stall_next_launch")

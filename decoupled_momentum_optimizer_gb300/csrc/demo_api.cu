@@ -33,6 +33,9 @@ struct DeviceState {
   // wait takes the event's last record at the time it is enqueued, so calls from
   // several host threads stay correct when their enqueue sequences do not interleave.
   std::mutex pipeline_mu;
+  // Test hook of the kernels' bounded waits (demo_test_stall_next_launch): 1 + the item whose
+  // load the next tile-kernel launch makes stall, 0 = none; taken (and cleared) by that launch.
+  std::atomic<long long> stall_at{0};
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -197,6 +200,7 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
   fill_rcp(p);
   p.wire = wire;
   p.fault = st->fault;
+  p.stall_at = st->stall_at.exchange(0);
   const int warps = shard_warps(step_warps(mode, p.k, bf16, R, p.sync != 0), p.ntiles, st);
   const int grid = grid_for(p.ntiles, st, warps);
   cudaError_t e;
@@ -313,6 +317,7 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
   fill_rcp(p);
   p.wire = wire;
   p.fault = st->fault;
+  p.stall_at = st->stall_at.exchange(0);
   const int warps = stage_payloads(p, mode, k, wire, R);
   const int grid = grid_for(p.ntiles, st, warps);
   const bool kv_ok = mode == DEMO_MODE_DEMO && wire != DEMO_WIRE_TERNARY && (k == 1 || k == 2 || k == 4 || k == 8);
@@ -354,6 +359,7 @@ int run_encode(DeviceState* st, const void* g, int grad_dtype, float* m, int64_t
   p.stride_mask = (mode == DEMO_MODE_STRIDE) ? stride_mask(p.stride_o, p.stride_ns, k) : 0u;
   p.beta = beta;
   p.fault = st->fault;
+  p.stall_at = st->stall_at.exchange(0);
   int kv = 0;
   const int warps = shard_warps(encode_warps(mode, p.k, wire, bf16, &kv), p.ntiles, st);
   return to_status(launch_encode(p, mode, bf16, warps, kv, grid_for(p.ntiles, st, warps), stream));
@@ -887,6 +893,14 @@ int demo_adamw_step(float* theta, int64_t n, float beta1, float beta2, float eps
   const int64_t want = (p.n4 + 255) / 256;
   const int grid = static_cast<int>(want < 8LL * st->sms ? want : 8LL * st->sms);
   return to_status(launch_adamw(p, grad_dtype == DEMO_GRAD_BF16, grid, static_cast<cudaStream_t>(stream)));
+}
+
+int demo_test_stall_next_launch(long long item) {
+  DeviceState* st = nullptr;
+  const int s = current_state(&st);
+  if (s != DEMO_OK) return s;
+  st->stall_at.store(item >= 0 ? item + 1 : 0);
+  return DEMO_OK;
 }
 
 int demo_device_fault(unsigned int* code) {

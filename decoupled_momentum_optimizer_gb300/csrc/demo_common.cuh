@@ -94,6 +94,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Test hook of the give-up path above: when stall_at = 1 + i (0 = off), the load of item i of
+// global warp 0 announces kStallBytes more than it delivers, so its barrier never completes
+// and the warp's bounded wait runs out, exactly as for a copy that never lands.  Every copy
+// still lands; the warp reports the fault, waits (bounded) for its copies and returns.
+constexpr uint32_t kStallBytes = 16;
+__device__ __forceinline__ uint32_t stall_extra(long long stall_at, long long gw, long long item) {
+  return (stall_at != 0 && gw == 0 && item + 1 == stall_at) ? kStallBytes : 0u;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

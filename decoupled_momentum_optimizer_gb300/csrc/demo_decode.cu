@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
 
   const uint32_t span = p.vspan + p.ispan;  // staged bytes per replica
   // Items are loaded strictly in order: the loads keep their own (tile, item) cursor.
-  long long ld_t = gw;
+  long long ld_t = gw, ld_item = 0;
   int ld_g = 0, ld_slot = 0;
   auto issue = [&]() {
     if (ld_t >= p.ntiles) return;
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
     int r0, r1;
     staged_range(ld_t, ld_g, r0, r1);
     uint64_t* bar = &bars[ld_slot];
-    mbar_expect_tx(bar, (last ? kTileBytesF32 : 0) + (r1 - r0) * span);
+    mbar_expect_tx(bar, (last ? kTileBytesF32 : 0) + (r1 - r0) * span + stall_extra(p.stall_at, gw, ld_item++));
     if (last) tma_load_2d(ws.tbuf[ld_slot], &p.theta, bar, 0, static_cast<int>(ld_t * 32));
     for (int r = r0; r < r1; ++r) {
       unsigned char* d = ws.stage[ld_slot] + (r - r0) * span;

@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_cons
     if (item >= nitems) return;
     const int s = static_cast<int>(item & 1);
     const int y = static_cast<int>((gw + item * TW) * 32);
-    mbar_expect_tx(&bars[s], (BF16 ? kTileBytesBF16 : kTileBytesF32) + kTileBytesF32);
+    mbar_expect_tx(&bars[s], (BF16 ? kTileBytesBF16 : kTileBytesF32) + kTileBytesF32 + stall_extra(p.stall_at, gw, item));
     tma_load_2d(ws.gbuf[s], &p.g, &bars[s], 0, y);
     tma_load_2d(ws.mbuf[s], &p.m, &bars[s], 0, y);
   };

@@ -20,6 +20,7 @@ struct EncodeParams {
   float beta;
   unsigned long long hbase;
   unsigned int* fault;
+  long long stall_at;  // test hook of the bounded waits (see stall_extra), 0 = off
 };
 
 template <int MAXR>
@@ -45,6 +46,7 @@ struct DecodeParams {
   unsigned long long hbase;
   float rcp_tab[kMaxReplicas + 1];
   unsigned int* fault;
+  long long stall_at;  // test hook of the bounded waits (see stall_extra), 0 = off
 };
 
 // Decode CTA shapes: warps per SM and the shared-memory staging per slot for the

@@ -30,6 +30,7 @@ struct StepParams {
   float rcp_tab[kMaxReplicas + 1];  // float32(1/c), entry 0 = 0
   int wire;                         // payload wire format the on-chip values are rounded to
   unsigned int* fault;
+  long long stall_at;  // test hook of the bounded waits: 1 + the item whose load stalls (warp 0), 0 = off
 };
 
 // Launchers (one per translation unit; the other kernels' are in demo_launch.h).

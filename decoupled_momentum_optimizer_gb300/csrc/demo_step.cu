@@ -71,18 +71,19 @@ __global__ void __launch_bounds__(WARPS * 32, 1) step_kernel(const __grid_consta
 
   // Items are loaded strictly in order, so the loads keep their own (tile, kind)
   // cursor instead of dividing item numbers by the items per tile.
-  long long ld_t = gw;
+  long long ld_t = gw, ld_item = 0;
   int ld_kind = 0, ld_slot = 0;
   auto issue = [&]() {
     if (ld_t >= p.ntiles) return;
     const int y = static_cast<int>(ld_t * 32);
     uint64_t* bar = &bars[ld_slot];
+    const uint32_t extra = stall_extra(p.stall_at, gw, ld_item++);
     if (ld_kind < p.R) {
-      mbar_expect_tx(bar, (BF16 ? kTileBytesBF16 : kTileBytesF32) + kTileBytesF32);
+      mbar_expect_tx(bar, (BF16 ? kTileBytesBF16 : kTileBytesF32) + kTileBytesF32 + extra);
       tma_load_2d(ws.gbuf[ld_slot], &p.g[ld_kind], bar, 0, y);
       tma_load_2d(ws.mbuf[ld_slot], &p.m[ld_kind], bar, 0, y);
     } else {
-      mbar_expect_tx(bar, kTileBytesF32);
+      mbar_expect_tx(bar, kTileBytesF32 + extra);
       tma_load_2d(ws.gbuf[ld_slot], &p.theta, bar, 0, y);
     }
     ld_slot ^= 1;

@@ -304,6 +304,23 @@ const char* demo_status_string(int status);
  */
 int demo_device_fault(unsigned int* code);
 
+/*
+ * demo_test_stall_next_launch -- test hook for the failure path of the kernels'
+ * device-side waits (failure detection without a GPU fault); the pages have no
+ * counterpart.  The next launch of a tile kernel on the current device (the one
+ * demo_step, demo_encode or demo_decode_update runs, or their _wire / pipelined
+ * variants; not the elementwise DiLoCo and AdamW kernels) makes its first warp
+ * announce 16 bytes more than the load of that warp's item `item` (0-based)
+ * delivers.  That load's barrier then never completes: the warp's bounded wait
+ * gives up after its limit (2 s), the warp sets bit 1 of the fault word, waits
+ * (again bounded) for the copies it has in flight and returns, leaving its
+ * remaining tiles unprocessed.  Every copy still lands, nothing faults or hangs,
+ * and the context stays usable.  A negative item cancels a pending request; a
+ * request stays pending until a tile kernel launches.  Returns DEMO_OK or
+ * DEMO_ENOTINIT.
+ */
+int demo_test_stall_next_launch(long long item);
+
 #ifdef __cplusplus
 }
 #endif
