@@ -100,21 +100,33 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t nc, bool bf16) {
   return r == CUDA_SUCCESS;
 }
 
-int grid_for(int64_t ntiles, const DeviceState* st, int warps_per_cta = kStepWarps) {
-  const int64_t want = (ntiles + warps_per_cta - 1) / warps_per_cta;
-  return static_cast<int>(want < st->sms ? want : st->sms);
-}
+// Launch shape of a tile kernel: the build (`inst` warps: its shared-memory layout and
+// register budget), the warps that run per CTA (`active`) and the grid.
+struct TileShape {
+  int inst, active, grid;
+};
 
-// A small shard is latency-bound rather than HBM-bound: each warp walks its tiles one
-// after another, so the time follows the largest number of tiles any warp takes.  Where
-// six warps per CTA would give some warps a second tile and the shard fits two waves of
-// eight-warp CTAs, eight warps per CTA are taken instead (measured 15-28% faster at
-// 2^20 parameters in every mode; even at 2^22; six stay ahead on larger shards).
-int shard_warps(int warps, int64_t ntiles, const DeviceState* st) {
-  if (warps != kStepWarpsLight) return warps;
-  const int64_t light = static_cast<int64_t>(st->sms) * kStepWarpsLight;
-  const int64_t mid = static_cast<int64_t>(st->sms) * kStepWarpsMid;
-  return (ntiles > light && ntiles <= 2 * mid) ? kStepWarpsMid : warps;
+// Most tiles per warp for which a shard counts as small (see tile_shape).
+constexpr int64_t kLatencyTilesPerWarp = 3;
+
+// Large shards stream HBM: one CTA of `warps` warps per SM, the fewest warps that cover
+// the compute per item (chosen per mode), so that fewer requests are in flight once HBM is
+// saturated.  A small shard is a few tiles per warp, and its time is the longest chain of
+// tiles any warp walks (each tile is R + 1 dependent items).  There every SM gets a CTA and
+// each warp m = ceil(ntiles / (SMs * inst)) tiles, with the fewest warps per CTA that reach
+// m: they share the SM's issue slots with the fewest other warps.  Any warp count up to the
+// build's fits its registers, so `inst` is the widest build (11 warps for the fused step
+// and the encode; the decode keeps the build its payload staging needs).
+TileShape tile_shape(int warps, int widest, int64_t ntiles, const DeviceState* st) {
+  const int64_t S = st->sms;
+  const int64_t m = (ntiles + S * widest - 1) / (S * widest);
+  if (m <= kLatencyTilesPerWarp) {
+    const int active = static_cast<int>((ntiles + m * S - 1) / (m * S));
+    const int64_t grid = (ntiles + active - 1) / active;
+    return {widest, active, static_cast<int>(grid < S ? grid : S)};
+  }
+  const int64_t want = (ntiles + warps - 1) / warps;
+  return {warps, warps, static_cast<int>(want < S ? want : S)};
 }
 
 template <class P>
@@ -201,13 +213,12 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
   p.wire = wire;
   p.fault = st->fault;
   p.stall_at = st->stall_at.exchange(0);
-  const int warps = shard_warps(step_warps(mode, p.k, bf16, R, p.sync != 0), p.ntiles, st);
-  const int grid = grid_for(p.ntiles, st, warps);
+  const TileShape sh = tile_shape(step_warps(mode, p.k, bf16, R, p.sync != 0), kStepWarps, p.ntiles, st);
   cudaError_t e;
   if constexpr (MAXR == kSmallReplicas) {
-    e = launch_step_small(p, mode, bf16, warps, grid, stream);
+    e = launch_step_small(p, mode, bf16, sh.inst, sh.active, sh.grid, stream);
   } else {
-    e = launch_step_large(p, mode, bf16, warps, grid, stream);
+    e = launch_step_large(p, mode, bf16, sh.inst, sh.active, sh.grid, stream);
   }
   return to_status(e);
 }
@@ -319,14 +330,14 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
   p.fault = st->fault;
   p.stall_at = st->stall_at.exchange(0);
   const int warps = stage_payloads(p, mode, k, wire, R);
-  const int grid = grid_for(p.ntiles, st, warps);
+  const TileShape sh = tile_shape(warps, warps, p.ntiles, st);
   const bool kv_ok = mode == DEMO_MODE_DEMO && wire != DEMO_WIRE_TERNARY && (k == 1 || k == 2 || k == 4 || k == 8);
   const int kv = kv_ok ? k : 0;
   cudaError_t e;
   if constexpr (MAXR == kSmallReplicas) {
-    e = launch_decode_small(p, mode, warps, kv, grid, stream);
+    e = launch_decode_small(p, mode, sh.inst, kv, sh.active, sh.grid, stream);
   } else {
-    e = launch_decode_large(p, mode, warps, kv, grid, stream);
+    e = launch_decode_large(p, mode, sh.inst, kv, sh.active, sh.grid, stream);
   }
   return to_status(e);
 }
@@ -361,8 +372,8 @@ int run_encode(DeviceState* st, const void* g, int grad_dtype, float* m, int64_t
   p.fault = st->fault;
   p.stall_at = st->stall_at.exchange(0);
   int kv = 0;
-  const int warps = shard_warps(encode_warps(mode, p.k, wire, bf16, &kv), p.ntiles, st);
-  return to_status(launch_encode(p, mode, bf16, warps, kv, grid_for(p.ntiles, st, warps), stream));
+  const TileShape sh = tile_shape(encode_warps(mode, p.k, wire, bf16, &kv), kStepWarps, p.ntiles, st);
+  return to_status(launch_encode(p, mode, bf16, sh.inst, kv, sh.active, sh.grid, stream));
 }
 
 // Byte offset of the payload of the block starting at chunk c0 (tile t0 = c0 / 32) in a wire-format buffer.

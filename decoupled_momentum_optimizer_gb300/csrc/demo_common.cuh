@@ -139,6 +139,19 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Programmatic dependent launch.  A tile kernel launched with programmatic stream
+// serialisation may start while the previous kernel of its stream is still running:
+// griddep_launch_dependents lets the next kernel's CTAs start their prologue on the SMs
+// this grid frees, and griddep_wait blocks until the previous grid has completed and its
+// memory operations are visible.  Each tile kernel waits before its first global-memory
+// access, so every read and write stays ordered after the previous kernel, and since every
+// kernel in the chain waits, after all earlier ones.  Without the launch attribute both are
+// no-ops.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ----------------------------------------------------------------------------
 // Swizzled row access.  TMA's 128-byte swizzle stores 16-byte unit j of row r
 // at unit j ^ (r & 7) (tile base 1024-byte aligned); the 64-byte swizzle of a

@@ -202,11 +202,16 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
   WarpSmem& ws = reinterpret_cast<WarpSmem*>(base)[warp];
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + WARPS * sizeof(WarpSmem)) + 2 * warp;
   float* rcp = reinterpret_cast<float*>(base + WARPS * sizeof(WarpSmem) + WARPS * 16);
-  if (threadIdx.x <= kMaxReplicas) rcp[threadIdx.x] = p.rcp_tab[threadIdx.x];
+  griddep_launch_dependents();
+  for (int i = threadIdx.x; i <= kMaxReplicas; i += blockDim.x) rcp[i] = p.rcp_tab[i];
+  if (threadIdx.x == 0) prefetch_tmap(&p.theta);
   __syncthreads();
 
-  const long long gw = static_cast<long long>(blockIdx.x) * WARPS + warp;
-  const long long TW = static_cast<long long>(gridDim.x) * WARPS;
+  // The launch may run fewer warps than the shared-memory layout holds: warps are counted
+  // from the block size.
+  const int nw = static_cast<int>(blockDim.x >> 5);
+  const long long gw = static_cast<long long>(blockIdx.x) * nw + warp;
+  const long long TW = static_cast<long long>(gridDim.x) * nw;
   if (gw >= p.ntiles) return;
   const long long ntw = (p.ntiles - 1 - gw) / TW + 1;  // tiles of this warp
   // Items: one per tile, or (DeMo, group > 0) one per group of replicas on full tiles.
@@ -262,6 +267,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
       ld_t += TW;
     }
   };
+  griddep_wait();  // the payloads the previous kernels wrote are visible from here on
   if (lane == 0) {
     issue();
     issue();
@@ -417,12 +423,18 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
 }
 
 template <int MAXR, int WARPS>
-static cudaError_t launch_decode_w(const DecodeParams<MAXR>& p, int mode, int kv, int grid, cudaStream_t st) {
+static cudaError_t launch_decode_w(const DecodeParams<MAXR>& p, int mode, int kv, int active, int grid,
+                                   cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(WARPS * 32);
+  cfg.blockDim = dim3(active * 32);
   cfg.dynamicSmemBytes = dec_smem(WARPS);
   cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   switch (mode) {
     case kModeDemo:
       switch (kv) {
@@ -439,23 +451,24 @@ static cudaError_t launch_decode_w(const DecodeParams<MAXR>& p, int mode, int kv
 }
 
 template <int MAXR>
-static cudaError_t launch_decode_t(const DecodeParams<MAXR>& p, int mode, int warps, int kv, int grid,
+static cudaError_t launch_decode_t(const DecodeParams<MAXR>& p, int mode, int warps, int kv, int active, int grid,
                                    cudaStream_t st) {
-  if (warps == 11) return launch_decode_w<MAXR, 11>(p, mode, kv, grid, st);
-  if (warps == 10) return launch_decode_w<MAXR, 10>(p, mode, kv, grid, st);
-  if (warps == 9) return launch_decode_w<MAXR, 9>(p, mode, kv, grid, st);
-  if (warps == 8) return launch_decode_w<MAXR, 8>(p, mode, kv, grid, st);
+  if (active < 1 || active > warps) return cudaErrorInvalidValue;
+  if (warps == 11) return launch_decode_w<MAXR, 11>(p, mode, kv, active, grid, st);
+  if (warps == 10) return launch_decode_w<MAXR, 10>(p, mode, kv, active, grid, st);
+  if (warps == 9) return launch_decode_w<MAXR, 9>(p, mode, kv, active, grid, st);
+  if (warps == 8) return launch_decode_w<MAXR, 8>(p, mode, kv, active, grid, st);
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int kv, int grid,
-                                cudaStream_t st) {
-  return launch_decode_t(p, mode, warps, kv, grid, st);
+cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int kv, int active,
+                                int grid, cudaStream_t st) {
+  return launch_decode_t(p, mode, warps, kv, active, grid, st);
 }
 
-cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int kv, int grid,
-                                cudaStream_t st) {
-  return launch_decode_t(p, mode, warps, kv, grid, st);
+cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int kv, int active,
+                                int grid, cudaStream_t st) {
+  return launch_decode_t(p, mode, warps, kv, active, grid, st);
 }
 
 template <class K>

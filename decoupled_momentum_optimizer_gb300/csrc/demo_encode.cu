@@ -160,18 +160,25 @@ __global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_cons
   const int lane = threadIdx.x & 31;
   EncWarpSmem& ws = reinterpret_cast<EncWarpSmem*>(base)[warp];
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + WARPS * sizeof(EncWarpSmem)) + 2 * warp;
+  griddep_launch_dependents();
 
-  const long long gw = static_cast<long long>(blockIdx.x) * WARPS + warp;
-  const long long TW = static_cast<long long>(gridDim.x) * WARPS;
+  // The launch may run fewer warps than the shared-memory layout holds: warps are counted
+  // from the block size.
+  const int nw = static_cast<int>(blockDim.x >> 5);
+  const long long gw = static_cast<long long>(blockIdx.x) * nw + warp;
+  const long long TW = static_cast<long long>(gridDim.x) * nw;
   if (gw >= p.ntiles) return;
   const long long nitems = (p.ntiles - 1 - gw) / TW + 1;
 
   if (lane == 0) {
+    prefetch_tmap(&p.g);
+    prefetch_tmap(&p.m);
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
     fence_mbar_init();
   }
   __syncwarp();
+  griddep_wait();  // the previous kernel's writes (m, an earlier payload's readers) are done
 
   auto issue = [&](long long item) {
     if (item >= nitems) return;
@@ -319,12 +326,18 @@ static cudaError_t launch_encode_demo(const cudaLaunchConfig_t& cfg, const Encod
 }
 
 template <int WARPS>
-static cudaError_t launch_encode_w(const EncodeParams& p, int mode, bool bf16, int kv, int grid, cudaStream_t st) {
+static cudaError_t launch_encode_w(const EncodeParams& p, int mode, bool bf16, int kv, int active, int grid,
+                                   cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(WARPS * 32);
+  cfg.blockDim = dim3(active * 32);
   cfg.dynamicSmemBytes = enc_smem(WARPS);
   cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (mode == kModeDemo)
     return bf16 ? launch_encode_demo<WARPS, true>(cfg, p, kv) : launch_encode_demo<WARPS, false>(cfg, p, kv);
 #define DEMO_LAUNCH(M, B) \
@@ -339,11 +352,12 @@ static cudaError_t launch_encode_w(const EncodeParams& p, int mode, bool bf16, i
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps, int kv, int grid,
+cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps, int kv, int active, int grid,
                           cudaStream_t st) {
-  if (warps == kStepWarpsLight) return launch_encode_w<kStepWarpsLight>(p, mode, bf16, kv, grid, st);
-  if (warps == kStepWarpsMid) return launch_encode_w<kStepWarpsMid>(p, mode, bf16, kv, grid, st);
-  if (warps == kStepWarps) return launch_encode_w<kStepWarps>(p, mode, bf16, kv, grid, st);
+  if (active < 1 || active > warps) return cudaErrorInvalidValue;
+  if (warps == kStepWarpsLight) return launch_encode_w<kStepWarpsLight>(p, mode, bf16, kv, active, grid, st);
+  if (warps == kStepWarpsMid) return launch_encode_w<kStepWarpsMid>(p, mode, bf16, kv, active, grid, st);
+  if (warps == kStepWarps) return launch_encode_w<kStepWarps>(p, mode, bf16, kv, active, grid, st);
   return cudaErrorInvalidValue;
 }
 

@@ -104,14 +104,16 @@ cudaError_t launch_adamw(const AdamWParams& p, bool bf16, int grid, cudaStream_t
 int encode_warps(int mode, int k, int wire, bool bf16, int* kv);
 // kv: DeMo's k when the encode is specialised for it (1, 2, 4 or 8 with a float32 or
 // 16-bit format), else 0.
-cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps, int kv, int grid,
+// `warps` picks the build (shared-memory layout, register budget); `active` warps (1..warps)
+// run in each CTA.
+cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps, int kv, int active, int grid,
                           cudaStream_t st);
 // kv: DeMo's k when the decode is specialised for it (1, 2, 4 or 8 with a float32 or
 // 16-bit format), else 0.
-cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int kv, int grid,
-                                cudaStream_t st);
-cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int kv, int grid,
-                                cudaStream_t st);
+cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int kv, int active,
+                                int grid, cudaStream_t st);
+cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int kv, int active,
+                                int grid, cudaStream_t st);
 
 // Set the dynamic shared-memory limit of every encode and decode kernel instantiation.
 cudaError_t prepare_encode_kernels();

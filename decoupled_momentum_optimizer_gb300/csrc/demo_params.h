@@ -46,10 +46,12 @@ constexpr int kStepWarps = 11;
 constexpr int kStepWarpsMid = 8;
 constexpr int kStepWarpsLight = 6;
 int step_warps(int mode, int k, bool bf16, int R, bool sync);
-cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, bool bf16, int warps, int grid,
-                              cudaStream_t st);
-cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int warps, int grid,
-                              cudaStream_t st);
+// `warps` picks the build (its shared-memory layout and register budget); `active` warps
+// (1..warps) run in each CTA.
+cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, bool bf16, int warps, int active,
+                              int grid, cudaStream_t st);
+cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int warps, int active,
+                              int grid, cudaStream_t st);
 
 // Set the dynamic shared-memory limit of every step kernel instantiation.
 cudaError_t prepare_step_kernels();

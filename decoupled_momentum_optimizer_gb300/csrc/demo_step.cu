@@ -47,11 +47,17 @@ __global__ void __launch_bounds__(WARPS * 32, 1) step_kernel(const __grid_consta
   StepWarpSmem& ws = reinterpret_cast<StepWarpSmem*>(base)[warp];
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + WARPS * sizeof(StepWarpSmem)) + 2 * warp;
   float* rcp = reinterpret_cast<float*>(base + WARPS * sizeof(StepWarpSmem) + WARPS * 16);
-  if (threadIdx.x <= kMaxReplicas) rcp[threadIdx.x] = p.rcp_tab[threadIdx.x];
+  griddep_launch_dependents();
+  for (int i = threadIdx.x; i <= kMaxReplicas; i += blockDim.x) rcp[i] = p.rcp_tab[i];
+  for (int i = threadIdx.x; i <= 2 * p.R; i += blockDim.x)
+    prefetch_tmap(i == 0 ? &p.theta : (i <= p.R ? &p.g[i - 1] : &p.m[i - 1 - p.R]));
   __syncthreads();
 
-  const long long gw = static_cast<long long>(blockIdx.x) * WARPS + warp;
-  const long long TW = static_cast<long long>(gridDim.x) * WARPS;
+  // The launch may run fewer warps than the shared-memory layout holds (WARPS is the most
+  // the build's registers allow): warps are counted from the block size.
+  const int nw = static_cast<int>(blockDim.x >> 5);
+  const long long gw = static_cast<long long>(blockIdx.x) * nw + warp;
+  const long long TW = static_cast<long long>(gridDim.x) * nw;
   if (gw >= p.ntiles) return;
   const long long ntw = (p.ntiles - 1 - gw) / TW + 1;
   const bool theta_item = !(MODE == kModeDiloco && !p.sync);
@@ -92,6 +98,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) step_kernel(const __grid_consta
       ld_t += TW;
     }
   };
+  griddep_wait();  // the previous kernel's writes (m, theta) are visible from here on
   if (lane == 0) {
     issue();
     issue();
@@ -259,12 +266,18 @@ int step_warps(int mode, int k, bool bf16, int R, bool sync) {
 }
 
 template <int MAXR, int WARPS>
-static cudaError_t launch_step_w(const StepParams<MAXR>& p, int mode, bool bf16, int grid, cudaStream_t st) {
+static cudaError_t launch_step_w(const StepParams<MAXR>& p, int mode, bool bf16, int active, int grid,
+                                 cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(WARPS * 32);
+  cfg.blockDim = dim3(active * 32);
   cfg.dynamicSmemBytes = step_smem(WARPS);
   cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
 #define DEMO_LAUNCH(M, B) \
   if (mode == M && bf16 == B) return cudaLaunchKernelEx(&cfg, step_kernel<M, B, MAXR, WARPS>, p);
   DEMO_LAUNCH(kModeDemo, false)
@@ -280,22 +293,23 @@ static cudaError_t launch_step_w(const StepParams<MAXR>& p, int mode, bool bf16,
 }
 
 template <int MAXR>
-static cudaError_t launch_step_t(const StepParams<MAXR>& p, int mode, bool bf16, int warps, int grid,
+static cudaError_t launch_step_t(const StepParams<MAXR>& p, int mode, bool bf16, int warps, int active, int grid,
                                  cudaStream_t st) {
-  if (warps == kStepWarpsLight) return launch_step_w<MAXR, kStepWarpsLight>(p, mode, bf16, grid, st);
-  if (warps == kStepWarpsMid) return launch_step_w<MAXR, kStepWarpsMid>(p, mode, bf16, grid, st);
-  if (warps == kStepWarps) return launch_step_w<MAXR, kStepWarps>(p, mode, bf16, grid, st);
+  if (active < 1 || active > warps) return cudaErrorInvalidValue;
+  if (warps == kStepWarpsLight) return launch_step_w<MAXR, kStepWarpsLight>(p, mode, bf16, active, grid, st);
+  if (warps == kStepWarpsMid) return launch_step_w<MAXR, kStepWarpsMid>(p, mode, bf16, active, grid, st);
+  if (warps == kStepWarps) return launch_step_w<MAXR, kStepWarps>(p, mode, bf16, active, grid, st);
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, bool bf16, int warps, int grid,
-                              cudaStream_t st) {
-  return launch_step_t(p, mode, bf16, warps, grid, st);
+cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, bool bf16, int warps, int active,
+                              int grid, cudaStream_t st) {
+  return launch_step_t(p, mode, bf16, warps, active, grid, st);
 }
 
-cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int warps, int grid,
-                              cudaStream_t st) {
-  return launch_step_t(p, mode, bf16, warps, grid, st);
+cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int warps, int active,
+                              int grid, cudaStream_t st) {
+  return launch_step_t(p, mode, bf16, warps, active, grid, st);
 }
 
 template <int MAXR, int WARPS>
