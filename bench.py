@@ -52,6 +52,8 @@ def parse_args():
                         "than L2, with its own clock record (0: skip)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--sweep", default=None, help="measure every configuration of the results table into this JSONL file")
+    p.add_argument("--sweep-match", default=None,
+                   help="with --sweep: only the configurations whose 'workload mode k R' label matches this regex")
     p.add_argument("--only", choices=["split", "adamw"], default=None,
                    help="time only this path on the workload (R encodes + one decode, or the Decoupled AdamW step) "
                         "and print its time; for profiling those kernels")
@@ -774,19 +776,25 @@ def sweep_cases():
     # Decoupled AdamW (moments local, directions averaged densely)
     for name in ("t5_base", "olmo2_1b_half", f"flat{1 << 28}"):
         out.append((name, "adamw", 0, False, 2, ("adamw",)))
-    for e in (20, 22, 24, 26, 28, 30):
-        for k in (1, 2, 4, 8):
-            out.append((f"flat{1 << e}", "demo", k, True, 2, ("fused",) if e != 26 else ("fused", "split")))
-    for R in (1, 8, 64):
-        out.append((f"flat{1 << 26}", "demo", 4, True, R, ("fused", "split")))
-    out.append((f"flat{1 << 30}", "demo", 4, True, 8, ("fused",)))
+    # the 65,536-parameter shard (DeMo k=4, sign, R=2): fused and split
+    out.append(("flat64k", "demo", 4, True, 2, ("fused", "split")))
+    # the flat size sweep: 2^20..2^30 parameters x k in {1, 2, 4, 8} x R in {1, 2, 8, 64} (R = 64 up
+    # to 2^26) x every scheme, sign on; DiLoCo (k does not apply) as steps between syncs and as
+    # sync steps; the split path beside the fused step at 2^26
+    for e in range(20, 31):
+        for R in (1, 2, 8, 64):
+            if R == 64 and e > 26:
+                continue
+            paths = ("fused", "split") if e == 26 else ("fused",)
+            for mode in ("demo", "random", "stride"):
+                for k in (1, 2, 4, 8):
+                    out.append((f"flat{1 << e}", mode, k, True, R, paths))
+            for kind in ("diloco", "diloco-sync"):
+                out.append((f"flat{1 << e}", kind, 1, True, R, paths))
     # the split path on small shards, eager against a CUDA graph replay
-    for e in (20, 22, 24):
-        out.append((f"flat{1 << e}", "demo", 4, True, 2, ("graph",)))
-        out.append((f"flat{1 << e}", "random", 8, True, 2, ("graph",)))
-    for e in (24, 26, 28):
-        for mode, k in (("random", 1), ("random", 8), ("stride", 4), ("diloco", 1), ("diloco-sync", 1)):
-            out.append((f"flat{1 << e}", mode, k, True, 2, ("fused", "split") if e == 26 else ("fused",)))
+    for e in (16, 20, 22, 24):
+        out.append((f"flat{1 << e}" if e != 16 else "flat64k", "demo", 4, True, 2, ("graph",)))
+        out.append((f"flat{1 << e}" if e != 16 else "flat64k", "random", 8, True, 2, ("graph",)))
     return out
 
 
@@ -827,7 +835,12 @@ def run_sweep(args):
     peak, _ = measured_peaks()
     cache = {}
     f = open(args.sweep, "w")
+    import re
+
+    match = re.compile(args.sweep_match) if args.sweep_match else None
     for name, mode, k, sign, R, paths in sweep_cases():
+        if match is not None and not match.search(f"{name} {mode} {k} {R}"):
+            continue
         key = (name, R)
         if key not in cache:
             cache.clear()
@@ -915,7 +928,7 @@ def run_sweep(args):
     # the float64 oracle on the host cores, on whole shards: the 65,536-parameter shard for its
     # five steps and a 2^20 shard for three, with one BLAS thread and with every core
     ncpu = os.cpu_count() or 1
-    for name, nc, steps in (("flat64k", 2048, 5), ("flat1048576", 32768, 3)):
+    for name, nc, steps in (() if match is not None else (("flat64k", 2048, 5), ("flat1048576", 32768, 3))):
         for threads in sorted({1, ncpu}):
             d, err = oracle_time("demo", 4, True, 2, nc, 1e9, threads, max_steps=steps)
             rec = {"oracle": True, "workload": name, "n": nc * 32, "mode": "demo", "k": 4, "sign": True, "R": 2,

@@ -353,26 +353,58 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
 #pragma unroll
       for (int i = 0; i < 32; ++i) qs[i * 32 + lane] = 0.0f;
       const long long tile = row0 >> 5;
-      if (ns == p.R && p.k <= 8) {
-        // Every replica staged and k <= 8: sum the replicas' k values per draw
-        // (replicas in order; one vector load per replica when the format allows),
-        // then place each sum at its draw's position, with the draws unrolled.
+      if (p.k <= 8) {
+        // k <= 8: sum the replicas' k values per draw (replicas in order: the staged ones from
+        // shared memory, then the others from global memory, four replicas' loads in flight
+        // at a time; one vector load per replica where the format allows), then place each
+        // sum at its draw's position, with the draws unrolled.
         float sum[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) sum[j] = 0.0f;
         const bool vec = p.wire != kWireTernary && vector_kd(p.k);
-        for (int r = 0; r < p.R; ++r) {
-          const unsigned char* sv = ws.stage[s] + r * span;
-          float pv[8];
+        auto load_one = [&](const void* base, long long cc, long long tl, float (&pv)[8]) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) pv[j] = 0.0f;
           if (vec) {
             uint32_t ilo, ihi;
-            load_payload(sv, nullptr, p.wire, lane, p.k, pv, ilo, ihi);
+            load_payload(base, nullptr, p.wire, cc, p.k, pv, ilo, ihi);
           } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              if (j < p.k) pv[j] = payload_value(sv, p.wire, lane, 0, lane, p.k, j);
+              if (j < p.k) pv[j] = payload_value(base, p.wire, cc, tl, lane, p.k, j);
+          }
+        };
+        for (int r = 0; r < ns; ++r) {
+          float pv[8];
+          load_one(ws.stage[s] + r * span, lane, 0, pv);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) sum[j] += pv[j];
+        }
+        const bool reads = valid || p.wire == kWireTernary;  // rows past the end read nothing
+        int r = ns;
+        for (; r + 4 <= p.R; r += 4) {
+          float pv[4][8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (reads) {
+              load_one(p.vals[r + q], c, tile, pv[q]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) pv[q][j] = 0.0f;
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sum[j] += pv[q][j];
+        }
+        for (; r < p.R; ++r) {
+          float pv[8];
+          if (reads) {
+            load_one(p.vals[r], c, tile, pv);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) pv[j] = 0.0f;
           }
 #pragma unroll
           for (int j = 0; j < 8; ++j) sum[j] += pv[j];
@@ -428,7 +460,7 @@ static cudaError_t launch_decode_w(const DecodeParams<MAXR>& p, int mode, int kv
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(active * 32);
-  cfg.dynamicSmemBytes = dec_smem(WARPS);
+  cfg.dynamicSmemBytes = persistent_smem(dec_smem(WARPS));
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -478,7 +510,7 @@ static cudaError_t set_smem(K kernel, int bytes) {
 
 template <int MAXR, int WARPS>
 static cudaError_t prepare_w() {
-  const int bytes = static_cast<int>(dec_smem(WARPS));
+  const int bytes = static_cast<int>(persistent_smem(dec_smem(WARPS)));
   cudaError_t e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, 0>, bytes);
   if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, 1>, bytes);
   if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, 2>, bytes);

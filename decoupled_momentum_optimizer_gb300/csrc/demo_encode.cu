@@ -331,7 +331,7 @@ static cudaError_t launch_encode_w(const EncodeParams& p, int mode, bool bf16, i
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(active * 32);
-  cfg.dynamicSmemBytes = enc_smem(WARPS);
+  cfg.dynamicSmemBytes = persistent_smem(enc_smem(WARPS));
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -367,7 +367,7 @@ static cudaError_t prepare_encode_w() {
 #define DEMO_ATTR(M, B, KV)                                                                             \
   if (e == cudaSuccess)                                                                                 \
     e = cudaFuncSetAttribute(encode_kernel<M, B, WARPS, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                             static_cast<int>(enc_smem(WARPS)));
+                             static_cast<int>(persistent_smem(enc_smem(WARPS))));
   DEMO_ATTR(kModeDemo, false, 0)
   DEMO_ATTR(kModeDemo, false, 1)
   DEMO_ATTR(kModeDemo, false, 2)

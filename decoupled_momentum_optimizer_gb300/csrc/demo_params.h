@@ -53,6 +53,14 @@ cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, boo
 cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int warps, int active,
                               int grid, cudaStream_t st);
 
+// The tile kernels are persistent: each assumes one CTA per SM (its grid is at most one CTA
+// per SM and its warps walk their tiles statically).  A CTA that asks for more than half of
+// an SM's shared memory (228 KB) can never share the SM with another CTA of the same kernel
+// -- not even when a programmatically dependent launch places its CTAs while the previous
+// kernel still holds some SMs -- so every launch asks for at least this much.
+constexpr size_t kOneCtaPerSmSmem = 116 * 1024;
+constexpr size_t persistent_smem(size_t bytes) { return bytes > kOneCtaPerSmSmem ? bytes : kOneCtaPerSmSmem; }
+
 // Set the dynamic shared-memory limit of every step kernel instantiation.
 cudaError_t prepare_step_kernels();
 

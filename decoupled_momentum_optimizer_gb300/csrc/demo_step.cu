@@ -271,7 +271,7 @@ static cudaError_t launch_step_w(const StepParams<MAXR>& p, int mode, bool bf16,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(active * 32);
-  cfg.dynamicSmemBytes = step_smem(WARPS);
+  cfg.dynamicSmemBytes = persistent_smem(step_smem(WARPS));
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -318,7 +318,7 @@ static cudaError_t prepare_w() {
 #define DEMO_ATTR(M, B)                                                                                  \
   if (e == cudaSuccess)                                                                                  \
     e = cudaFuncSetAttribute(step_kernel<M, B, MAXR, WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                             static_cast<int>(step_smem(WARPS)));
+                             static_cast<int>(persistent_smem(step_smem(WARPS))));
   DEMO_ATTR(kModeDemo, false)
   DEMO_ATTR(kModeDemo, true)
   DEMO_ATTR(kModeRandom, false)
