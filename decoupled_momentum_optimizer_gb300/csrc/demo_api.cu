@@ -331,8 +331,10 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
   p.stall_at = st->stall_at.exchange(0);
   const int warps = stage_payloads(p, mode, k, wire, R);
   const TileShape sh = tile_shape(warps, warps, p.ntiles, st);
-  const bool kv_ok = mode == DEMO_MODE_DEMO && wire != DEMO_WIRE_TERNARY && (k == 1 || k == 2 || k == 4 || k == 8);
-  const int kv = kv_ok ? k : 0;
+  // DeMo with k in {1, 2, 4, 8} runs the decode compiled for its k: kv = k for the float32 and
+  // 16-bit formats, kv = -k for the ternary one
+  const bool kv_ok = mode == DEMO_MODE_DEMO && (k == 1 || k == 2 || k == 4 || k == 8);
+  const int kv = kv_ok ? (wire == DEMO_WIRE_TERNARY ? -k : k) : 0;
   cudaError_t e;
   if constexpr (MAXR == kSmallReplicas) {
     e = launch_decode_small(p, mode, sh.inst, kv, sh.active, sh.grid, stream);

@@ -190,6 +190,98 @@ __device__ __forceinline__ void demo_accumulate(SumCount* acc, int lane, const v
   }
 }
 
+// One replica's entries for this lane's chunk, read and decoded, for a k known at
+// compile time: KV < 0 is -k for the ternary format (KV > 0, k for a float32 or 16-bit
+// format, is also readable this way, but demo_accumulate serves those: reading ahead
+// measured 1-2% slower there).  For the ternary format every entry takes seven bit-plane
+// words, and reading the next replica's entries before adding this replica's lets those
+// loads overlap the shared-memory updates (the updates themselves stay in replica order).
+template <int KV>
+struct DemoEntries {
+  static constexpr int K = KV < 0 ? -KV : KV;
+  float pv[K];
+  int uu[K];
+};
+
+template <int KV>
+__device__ __forceinline__ void demo_read(DemoEntries<KV>& e, const void* vals, const void* idx, int wire,
+                                          long long c, long long tile, int lane) {
+  constexpr int K = DemoEntries<KV>::K;
+  if constexpr (KV < 0) {
+    // the tile's bit-planes: value words [K][2] (nonzero, negative), index words [K][5]; this
+    // lane's chunk is bit `lane` of each word
+    const uint32_t* vw = static_cast<const uint32_t*>(vals) + tile * K * 2;
+    const uint32_t* iw = static_cast<const uint32_t*>(idx) + tile * K * 5;
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      const uint2 w = reinterpret_cast<const uint2*>(vw)[j];
+      const uint32_t nz = (w.x >> lane) & 1u, ng = (w.y >> lane) & 1u;
+      e.pv[j] = nz ? (ng ? -1.0f : 1.0f) : 0.0f;
+      int u = 0;
+#pragma unroll
+      for (int b = 0; b < 5; ++b) u |= static_cast<int>((iw[5 * j + b] >> lane) & 1u) << b;
+      e.uu[j] = u;
+    }
+  } else {
+    float pv[8];
+    uint32_t ilo, ihi;
+    load_payload(vals, idx, wire, c, K, pv, ilo, ihi);
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      e.pv[j] = pv[j];
+      e.uu[j] = ((j < 4 ? ilo >> (8 * j) : ihi >> (8 * (j - 4)))) & 31;
+    }
+  }
+}
+
+template <int KV>
+__device__ __forceinline__ void demo_add(SumCount* acc, int lane, const DemoEntries<KV>& e) {
+  constexpr int K = DemoEntries<KV>::K;
+  bool ascending = false;
+  if constexpr (K > 1) {
+    ascending = true;
+#pragma unroll
+    for (int j = 1; j < K; ++j) ascending = ascending && e.uu[j] > e.uu[j - 1];
+  }
+  if (ascending) {
+    // A valid payload lists distinct slots in ascending order: read all k slots, then update
+    // and write them, instead of a chain of k dependent updates.
+    SumCount a[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) a[j] = acc[e.uu[j] * 32 + lane];
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      a[j].sum += e.pv[j];
+      a[j].cnt += 1u;
+    }
+#pragma unroll
+    for (int j = 0; j < K; ++j) acc[e.uu[j] * 32 + lane] = a[j];
+  } else {
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      SumCount a = acc[e.uu[j] * 32 + lane];
+      a.sum += e.pv[j];
+      a.cnt += 1u;
+      acc[e.uu[j] * 32 + lane] = a;
+    }
+  }
+}
+
+// Replicas [r_begin, r_end) added in order, each replica's entries read before the previous
+// replica's are added.  `at(r, e)` reads replica r's entries; `adds`: this lane's chunk exists.
+template <int KV, class At>
+__device__ __forceinline__ void demo_add_replicas(SumCount* acc, int lane, int r_begin, int r_end, bool adds, At&& at) {
+  if (r_begin >= r_end) return;
+  DemoEntries<KV> cur;
+  at(r_begin, cur);
+  for (int r = r_begin; r < r_end; ++r) {
+    DemoEntries<KV> nxt = cur;
+    if (r + 1 < r_end) at(r + 1, nxt);
+    if (adds) demo_add<KV>(acc, lane, cur);
+    cur = nxt;
+  }
+}
+
 template <int MODE, int MAXR, int WARPS, int KV>
 __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_constant__ DecodeParams<MAXR> p) {
   using WarpSmem = DecWarpSmem<dec_stage_bytes(WARPS)>;
@@ -298,9 +390,16 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
     }
 
     if constexpr (MODE == kModeDemo) {
-      for (int r = r0; r < ns; ++r) {
-        const unsigned char* sv = ws.stage[s] + (r - r0) * span;
-        demo_accumulate<KV>(ws.acc, lane, sv, sv + p.vspan, p.wire, p.k, lane, 0, true, true);
+      if constexpr (KV < 0) {
+        demo_add_replicas<KV>(ws.acc, lane, r0, ns, true, [&](int r, DemoEntries<KV>& e) {
+          const unsigned char* sv = ws.stage[s] + (r - r0) * span;
+          demo_read<KV>(e, sv, sv + p.vspan, p.wire, lane, 0, lane);
+        });
+      } else {
+        for (int r = r0; r < ns; ++r) {
+          const unsigned char* sv = ws.stage[s] + (r - r0) * span;
+          demo_accumulate<KV>(ws.acc, lane, sv, sv + p.vspan, p.wire, p.k, lane, 0, true, true);
+        }
       }
     }
     if (!last) {
@@ -319,8 +418,15 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
     if constexpr (MODE == kModeDemo) {
       const long long tile = row0 >> 5;
       const bool reads = valid || p.wire == kWireTernary;
-      for (int r = ns; r < p.R; ++r)
-        demo_accumulate<KV>(ws.acc, lane, p.vals[r], p.idx[r], p.wire, p.k, c, tile, valid, reads);
+      if constexpr (KV < 0) {
+        // the ternary words belong to the whole tile and every lane reads them
+        demo_add_replicas<KV>(ws.acc, lane, ns, p.R, valid, [&](int r, DemoEntries<KV>& e) {
+          if (reads) demo_read<KV>(e, p.vals[r], p.idx[r], p.wire, c, tile, lane);
+        });
+      } else {
+        for (int r = ns; r < p.R; ++r)
+          demo_accumulate<KV>(ws.acc, lane, p.vals[r], p.idx[r], p.wire, p.k, c, tile, valid, reads);
+      }
       if (p.R * p.k > kMaxReplicas) {
         // Valid payloads count at most R entries per slot; a malformed one (an index
         // repeated within a chunk) can count more than the reciprocal table covers.
@@ -474,6 +580,10 @@ static cudaError_t launch_decode_w(const DecodeParams<MAXR>& p, int mode, int kv
         case 2: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS, 2>, p);
         case 4: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS, 4>, p);
         case 8: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS, 8>, p);
+        case -1: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS, -1>, p);
+        case -2: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS, -2>, p);
+        case -4: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS, -4>, p);
+        case -8: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS, -8>, p);
         default: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS, 0>, p);
       }
     case kModeRandom: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeRandom, MAXR, WARPS, 0>, p);
@@ -516,6 +626,10 @@ static cudaError_t prepare_w() {
   if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, 2>, bytes);
   if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, 4>, bytes);
   if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, 8>, bytes);
+  if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, -1>, bytes);
+  if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, -2>, bytes);
+  if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, -4>, bytes);
+  if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, -8>, bytes);
   if (e == cudaSuccess) e = set_smem(decode_kernel<kModeRandom, MAXR, WARPS, 0>, bytes);
   if (e == cudaSuccess) e = set_smem(decode_kernel<kModeStride, MAXR, WARPS, 0>, bytes);
   return e;

@@ -109,7 +109,7 @@ int encode_warps(int mode, int k, int wire, bool bf16, int* kv);
 cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps, int kv, int active, int grid,
                           cudaStream_t st);
 // kv: DeMo's k when the decode is specialised for it (1, 2, 4 or 8 with a float32 or
-// 16-bit format), else 0.
+// 16-bit format; -1, -2, -4 or -8 for those k with the ternary format), else 0.
 cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int kv, int active,
                                 int grid, cudaStream_t st);
 cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int kv, int active,
