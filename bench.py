@@ -57,7 +57,11 @@ def parse_args():
     p.add_argument("--only", choices=["split", "adamw"], default=None,
                    help="time only this path on the workload (R encodes + one decode, or the Decoupled AdamW step) "
                         "and print its time; for profiling those kernels")
-    p.add_argument("--wire", default="f32", help="payload wire format of --only split")
+    p.add_argument("--wire", default="f32", help="payload wire format of --only split and --exchange")
+    p.add_argument("--exchange", action="store_true",
+                   help="one replica per GPU: every rank steps its own replica of the workload's shard and the "
+                        "payloads are exchanged by the process group (NCCL; R = the number of ranks); prints the "
+                        "rank-0 line with the max-over-ranks step time")
     p.add_argument("--diloco-period", type=int, default=1,
                    help="DiLoCo sync period of the timed steps: 1 (default) makes every step a sync step, a "
                         "period longer than warm-up + steps times only the steps between syncs (momentum only)")
@@ -655,6 +659,8 @@ def main():
         return run_sweep(args)
     if args.only:
         return run_only(args)
+    if args.exchange:
+        return run_exchange(args)
 
     import torch
     import torch.distributed as dist
@@ -773,6 +779,77 @@ def main():
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# One replica per GPU: the payloads exchanged by the process group
+# ----------------------------------------------------------------------------
+
+def run_exchange(args):
+    """Every rank holds one replica of the workload's shard (R = world size) and steps it through
+    ReplicaExchange: the library's encode, an NCCL all_gather (DeMo) or all-reduce (the other
+    schemes with float32 values) of the wire-format payloads, the library's decode.  Without
+    torchrun it runs as a one-rank group.  Prints rank 0's JSON line (max-over-ranks step time)."""
+    import torch
+    import torch.distributed as dist
+
+    import decoupled_momentum_optimizer_gb300 as dm
+    from decoupled_momentum_optimizer_gb300 import workloads as W
+    from decoupled_momentum_optimizer_gb300.exchange import ReplicaExchange
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    else:
+        dist.init_process_group("nccl", rank=0, world_size=1, store=dist.HashStore(), device_id=dev)
+    dm.init(local)
+    wl, mode, k, sign, _ = workload_settings(args)
+    n = wl.n
+    period = args.diloco_period if mode == "diloco" else 8
+    ex = ReplicaExchange(n, k, mode, wire=args.wire, diloco_period=period)
+    theta = W.make_theta0(wl, dev)
+    m = torch.zeros(n, device=dev)
+    stream = W.GradStream(wl, rank, dev)  # this rank's replica draws its own gradients
+    ring = [stream.next() for _ in range(3)]
+    main = torch.cuda.current_stream()
+
+    def one(t):
+        ex.step(theta, ring[t % len(ring)], m, beta=wl.beta, lr=wl.lr, sign=sign, seed=0, step=t)
+
+    for t in range(args.warmup):
+        one(t)
+    torch.cuda.synchronize()
+    dist.barrier()
+    grad_bytes = ring[0].element_size()
+    step_bytes = n * (grad_bytes + 8) + (8 * n if (mode != "diloco" or diloco_syncs(args)) else 0)
+    ms = _timed_steps(lambda i: one(args.warmup + i), args.steps, main, step_bytes < 2 * L2_BYTES, dev)
+    dist.barrier()
+    tt = torch.tensor([ms], device=dev)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    ms = tt.item()
+    tx, rx = ex.bytes_per_step(period - 1 if mode == "diloco" else 0)
+    fault = dm.device_fault()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": world * n / (ms * 1e-3), "unit": "params/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{wl.name}: {n} params, one replica per GPU (R = {world}), {mode} k={k}/32, "
+                                   f"sign={'on' if sign else 'off'}, grads {wl.g_dtype}, payloads exchanged by "
+                                   f"{ex.collective} ({args.wire})",
+                       "n": n, "R": world, "mode": mode, "k": k, "sign": bool(sign), "wire": args.wire,
+                       "collective": ex.collective, "payload_bytes_sent": tx, "payload_bytes_received": rx,
+                       "parallelism": f"one replica per GPU x {world}",
+                       "note": "value counts every rank's replica: world x n params per step"},
+            "device_fault": fault,
+        }
+        print(json.dumps(line), flush=True)
+    dist.destroy_process_group()
     return 0
 
 
