@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB_NAME = "libdemo_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = ["demo_api.cu", "demo_step.cu", "demo_encode.cu", "demo_decode.cu", "demo_dense.cu", "demo_adamw.cu"]
+SOURCES = ["demo_api.cu", "demo_step.cu", "demo_encode.cu", "demo_decode.cu", "demo_decode_lanes.cu",
+           "demo_decode_groups.cu", "demo_dense.cu", "demo_adamw.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

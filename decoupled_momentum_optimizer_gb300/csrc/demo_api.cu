@@ -223,21 +223,30 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
   return to_status(e);
 }
 
-// Which replicas' payloads the decode kernel stages through shared memory, and
-// the CTA shape that goes with it (returns its warp count).  The spans of one
-// 32-chunk tile must be 16-byte multiples (so every tile's span starts 16-byte
-// aligned in a 16-byte aligned buffer).  The shape with the most warps whose
-// staging holds every replica is taken (measured faster than staging only some
-// with more warps).  When none holds them all, DeMo stages the replicas a group
-// at a time (the decode visits each full tile as one item per group), and the
-// other schemes stage the leading replicas that fit 2 KB and read the others
-// directly (in the real system they receive one all-reduced payload, not R).
-// DiLoCo payloads (4 KB of float32 per tile and replica) are always read directly.
+// Which replicas' payloads the decode kernel stages through shared memory, the CTA shape
+// that goes with it (returns its warp count) and the kernel flavour.  The spans of one
+// 32-chunk tile must be 16-byte multiples (so every tile's span starts 16-byte aligned in a
+// 16-byte aligned buffer).  The shape with the most warps whose staging holds every
+// replica is taken (measured faster than staging only some with more warps).  When none
+// holds them all (the receiver of an all_gather over many replicas), the replicas are
+// staged a group at a time (the decode visits each full tile as one item per group; Random
+// and Striding for k <= 8 only), or, for DeMo with k in {1, 2, 4, 8} and long spans, read
+// directly.  DiLoCo payloads (4 KB of float32 per tile and replica) are always read
+// directly.
+// How the spans move (measured on 2^24 and 2^26 shards with 8 to 64 replicas): with more
+// than four replicas, lane copies for spans up to 320 bytes (192 in the 11-warp shape), bulk
+// copies for longer ones; DeMo payloads with k in {1, 2, 4, 8} that no shape holds whole are
+// read directly, F replicas at a time, from 256-byte spans on, and staged in groups below.
+constexpr size_t kLaneCopyMaxSpan = 320;
+constexpr size_t kLaneCopyMaxSpanWide = 192;
+constexpr size_t kDirectMinSpan = 256;
+
 template <class P>
-int stage_payloads(P& p, int mode, int k, int wire, int R) {
+int stage_payloads(P& p, int mode, int k, int wire, int R, int* flavor) {
   p.nstaged = 0;
   p.group = 0;
   p.vspan = p.ispan = 0;
+  *flavor = kFlavPlain;
   if (mode == DEMO_MODE_DILOCO) return kDecShapes[0];
   const bool demo = mode == DEMO_MODE_DEMO;
   size_t vs, is;
@@ -248,6 +257,8 @@ int stage_payloads(P& p, int mode, int k, int wire, int R) {
     vs = 32 * static_cast<size_t>(k) * (wire == DEMO_WIRE_F32 ? 4 : 2);
     is = demo ? 32 * static_cast<size_t>(k) : 0;    // uint8 [chunk][k]
   }
+  const bool kv_path = demo && (k == 1 || k == 2 || k == 4 || k == 8);
+  const bool ternary = wire == DEMO_WIRE_TERNARY;
   const size_t span = vs + is;
   const size_t small = static_cast<size_t>(dec_stage_bytes(kDecShapes[0]));
   if (vs % 16 || is % 16 || span > small) return kDecShapes[0];
@@ -263,16 +274,25 @@ int stage_payloads(P& p, int mode, int k, int wire, int R) {
         break;
       }
     }
-    // DeMo payloads that no shape holds whole (the receiver of an all_gather over many
-    // replicas): stage them a group at a time, one item per group, with the largest
-    // staging area (8 warps, 6 KB), so that each item moves as much as it can.
-    if (ns < R && demo) {
-      warps = kDecShapes[3];
-      p.group = static_cast<int>(static_cast<size_t>(dec_stage_bytes(warps)) / span);
-      ns = 0;
+    if (ns < R) {
+      // Payloads that no shape holds whole (the receiver of an all_gather over many
+      // replicas): stage them a group at a time, one item per group, with the largest
+      // staging area (8 warps, 6 KB), so that each item moves as much as it can.  Random
+      // and Striding keep per-draw sums across the items for k <= 8 only.
+      const bool direct = kv_path && !ternary && span >= kDirectMinSpan;
+      if (direct) {
+        ns = 0;
+      } else if (demo || k <= 8) {
+        warps = kDecShapes[3];
+        p.group = static_cast<int>(static_cast<size_t>(dec_stage_bytes(warps)) / span);
+        ns = 0;
+      }
     }
   }
   p.nstaged = ns;
+  const bool lane_copy = R > kSmallReplicas && (ns > 0 || p.group > 0) &&
+                         span <= (warps == kDecShapes[0] ? kLaneCopyMaxSpanWide : kLaneCopyMaxSpan);
+  *flavor = (p.group > 0 ? kFlavGroups : kFlavPlain) | (lane_copy ? kFlavLaneCopy : kFlavPlain);
   p.vspan = static_cast<unsigned int>(vs);
   p.ispan = static_cast<unsigned int>(is);
   return warps;
@@ -329,7 +349,8 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
   p.wire = wire;
   p.fault = st->fault;
   p.stall_at = st->stall_at.exchange(0);
-  const int warps = stage_payloads(p, mode, k, wire, R);
+  int flavor;
+  const int warps = stage_payloads(p, mode, k, wire, R, &flavor);
   const TileShape sh = tile_shape(warps, warps, p.ntiles, st);
   // DeMo with k in {1, 2, 4, 8} runs the decode compiled for its k: kv = k for the float32 and
   // 16-bit formats, kv = -k for the ternary one
@@ -339,7 +360,7 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
   if constexpr (MAXR == kSmallReplicas) {
     e = launch_decode_small(p, mode, sh.inst, kv, sh.active, sh.grid, stream);
   } else {
-    e = launch_decode_large(p, mode, sh.inst, kv, sh.active, sh.grid, stream);
+    e = launch_decode_large(p, mode, sh.inst, kv, flavor, sh.active, sh.grid, stream);
   }
   return to_status(e);
 }

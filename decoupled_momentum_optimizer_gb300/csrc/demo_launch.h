@@ -38,9 +38,9 @@ struct DecodeParams {
   // with the theta tile; the others, and a ragged last tile, are read directly.
   int nstaged;
   unsigned int vspan, ispan;
-  // DeMo with more replicas than a staging area holds: each full tile is visited as
-  // ceil(R / group) items, item i staging replicas [i * group, (i + 1) * group) and the
-  // last one also the theta tile; 0 = one item per tile.
+  // More replicas than a staging area holds: each full tile is visited as ceil(R / group)
+  // items, item i staging replicas [i * group, (i + 1) * group) and the last one also the
+  // theta tile; 0 = one item per tile.
   int group;
   float lr, rcpR;
   unsigned long long hbase;
@@ -57,6 +57,17 @@ __host__ __device__ constexpr int dec_stage_bytes(int warps) {
   return warps >= 11 ? 2048 : warps == 10 ? 3072 : warps == 9 ? 4608 : 6144;
 }
 constexpr int kDecShapes[] = {11, 10, 9, 8};
+
+// Staging flavours of the decode kernel, each compiled separately so that no kernel
+// carries the code of a staging method it does not use.  Bit 0: the staged spans are
+// copied by all 32 lanes of a warp with 16-byte asynchronous copies (one copy group per
+// item) instead of lane 0's 1-D bulk copies on the item's barrier; bit 1: one item per
+// group of replicas (DecodeParams::group > 0, the 8-warp shape only).  The kernels for
+// R <= 4 are plain only.
+constexpr int kFlavPlain = 0;
+constexpr int kFlavLaneCopy = 1;
+constexpr int kFlavGroups = 2;
+constexpr int kFlavGroupsLaneCopy = kFlavGroups | kFlavLaneCopy;
 
 // Dense decode (the DiLoCo sync step's receiver; elementwise over groups of four).
 template <int MAXR>
@@ -112,8 +123,8 @@ cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps,
 // 16-bit format; -1, -2, -4 or -8 for those k with the ternary format), else 0.
 cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int kv, int active,
                                 int grid, cudaStream_t st);
-cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int kv, int active,
-                                int grid, cudaStream_t st);
+cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int kv, int flavor,
+                                int active, int grid, cudaStream_t st);
 
 // Set the dynamic shared-memory limit of every encode and decode kernel instantiation.
 cudaError_t prepare_encode_kernels();

@@ -44,6 +44,24 @@ def test_wire_ragged(mode, k, sign, R, wire):
     run_steps(RAGGED, R, k, mode, sign, steps, g_std=1e-3, period=2 if mode == "diloco" else 8, seed=11, wire=wire)
 
 
+# Receivers of many replicas in the compact formats: each staging method of the decode
+# (spans staged whole or a group of replicas per item, moved by bulk or lane copies; DeMo
+# payloads read directly, several replicas at a time) with a ragged last tile.
+MANY_CASES = [
+    ("demo", 4, True, 64, "ternary"), ("demo", 8, True, 33, "ternary"), ("demo", 1, True, 40, "ternary"),
+    ("demo", 1, False, 64, "bf16"), ("demo", 2, False, 64, "bf16"), ("demo", 4, False, 64, "bf16"),
+    ("demo", 8, False, 17, "f16"), ("demo", 3, False, 40, "f16"), ("demo", 4, False, 5, "bf16"),
+    ("random", 4, False, 64, "bf16"), ("random", 8, False, 20, "f16"), ("stride", 4, True, 64, "ternary"),
+    ("stride", 4, False, 8, "bf16"), ("random", 2, True, 37, "ternary"), ("demo", 5, True, 30, "f32"),
+]
+
+
+@pytest.mark.parametrize("mode,k,sign,R,wire", MANY_CASES, ids=lambda v: str(v))
+def test_wire_many_replicas(mode, k, sign, R, wire):
+    run_steps(RAGGED, R, k, mode, sign, 2, g_std=1e-3, seed=23, wire=wire)
+    torch.cuda.empty_cache()
+
+
 def _encode(n, mode, k, wire, g, m, step=0):
     v, i = dm.payload_buffers(mode, n, k, step=step, diloco_period=8, wire=wire)
     dm.encode(g, m, v, i, k=k, beta=0.9, mode=mode, sign=True, seed=5, step=step, diloco_period=8, wire=wire)
