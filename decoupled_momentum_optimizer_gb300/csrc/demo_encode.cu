@@ -114,6 +114,39 @@ struct PayloadOut {
   }
 };
 
+// Ternary bit-planes of a DeMo tile for k = K known at compile time: each ballot word is kept
+// by the lane with its index in the tile's block (value words [K][2], index words [K][5]), and
+// the block leaves with coalesced stores instead of one single-lane store per word.  put()
+// must be called by all 32 lanes for the same j, with j a compile-time index.
+template <int K>
+struct TernaryOut {
+  static constexpr int kIdxRegs = (5 * K + 31) / 32;
+  uint32_t* vw;  // the tile's value words
+  uint32_t* iw;  // the tile's index words
+  int lane;
+  bool valid;
+  uint32_t v_word, i_word[kIdxRegs];
+
+  __device__ __forceinline__ void put(int j, int u, float v) {
+    const uint32_t nz = __ballot_sync(0xffffffffu, valid && v != 0.0f);
+    const uint32_t ng = __ballot_sync(0xffffffffu, valid && v < 0.0f);
+    v_word = lane == 2 * j ? nz : (lane == 2 * j + 1 ? ng : v_word);
+#pragma unroll
+    for (int b = 0; b < 5; ++b) {
+      const uint32_t w = __ballot_sync(0xffffffffu, valid && ((u >> b) & 1));
+      const int at = 5 * j + b;
+      i_word[at / 32] = lane == at % 32 ? w : i_word[at / 32];
+    }
+  }
+
+  __device__ __forceinline__ void finish() {
+    if (lane < 2 * K) vw[lane] = v_word;
+#pragma unroll
+    for (int q = 0; q < kIdxRegs; ++q)
+      if (32 * q + lane < 5 * K) iw[32 * q + lane] = i_word[q];
+  }
+};
+
 // DiLoCo sync step: the whole row of 32 values of this lane's chunk, in the wire format.
 __device__ __forceinline__ void put_row(void* vals, int wire, long long c, long long tile, int lane, bool valid,
                                         const float (&v)[32]) {
@@ -149,7 +182,9 @@ __device__ __forceinline__ void put_row(void* vals, int wire, long long c, long 
 
 // KV > 0 (DeMo, a float32 or 16-bit format, k in {1, 2, 4, 8}): k is KV at compile
 // time, so the payload loop unrolls, each entry goes straight to its register and the
-// vector store needs no dispatch on k; KV = 0: k is the runtime value.
+// vector store needs no dispatch on k; KV < 0 (DeMo, the ternary format, k = -KV in
+// {1, 2, 4, 8}): the same for the tile's bit-plane words (TernaryOut); KV = 0: k is the
+// runtime value.
 template <int MODE, bool BF16, int WARPS, int KV>
 __global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_constant__ EncodeParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -222,10 +257,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_cons
     if constexpr (MODE == kModeDemo) {
       float X[32], Xs[32];
       dct32_forward(x, X);
-      const uint32_t M = topk_select(X, p.k, Xs);
+      const uint32_t M = topk_select(X, KV < 0 ? -KV : p.k, Xs);
 #pragma unroll
       for (int u = 0; u < 32; ++u) scratch[u * 32 + lane] = Xs[u];
-      const bool tern = KV > 0 ? false : p.wire == kWireTernary;
+      const bool tern = KV != 0 ? false : p.wire == kWireTernary;
       PayloadOut out{p.vals, p.idx, c, row0 >> 5, lane, KV > 0 ? KV : p.k, p.wire, valid,
                      KV > 0 ? true : vector_k(p.k) && !tern, {0, 0, 0, 0, 0, 0, 0, 0}, 0u, 0u, tern};
       uint32_t mm = M;
@@ -235,13 +270,28 @@ __global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_cons
         const float v = scratch[u * 32 + lane];
         out.put(j, u, p.sign ? sign3(v) : v);
       };
-      if constexpr (KV > 0) {
+      if constexpr (KV < 0) {
+        constexpr int K = -KV;
+        const long long tile = row0 >> 5;
+        TernaryOut<K> tw{static_cast<uint32_t*>(p.vals) + tile * K * 2, static_cast<uint32_t*>(p.idx) + tile * K * 5,
+                         lane, valid, 0u, {}};
 #pragma unroll
-        for (int j = 0; j < KV; ++j) entry(j);
+        for (int j = 0; j < K; ++j) {
+          const int u = __ffs(mm) - 1;
+          mm &= mm - 1;
+          const float v = scratch[u * 32 + lane];
+          tw.put(j, u, p.sign ? sign3(v) : v);
+        }
+        tw.finish();
       } else {
-        for (int j = 0; j < p.k; ++j) entry(j);
+        if constexpr (KV > 0) {
+#pragma unroll
+          for (int j = 0; j < KV; ++j) entry(j);
+        } else {
+          for (int j = 0; j < p.k; ++j) entry(j);
+        }
+        out.finish();
       }
-      out.finish();
       float q[32];
       dct32_inverse(Xs, q);
 #pragma unroll
@@ -292,10 +342,23 @@ __global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_cons
 // unless the selection needs them (DeMo from k = 7 on, the ternary format's ballots).
 // The k-compiled kernel issues fewer instructions and so wants fewer warps; bfloat16
 // gradients bring less data per tile for the same compute and want more.
+// The k-specialised ternary DeMo encode: warps per CTA by gradient dtype (float32, bfloat16)
+// and k (1, 2, 4, 8).  Measured on a 2^27 shard with float32 gradients: k = 1 6 warps 255 us
+// (runtime k, 11 warps: 284), k = 2 6 warps 244 us (8: 274), k = 4 8 warps 266 us (11: 286),
+// k = 8 11 warps 275 us (8: 300, runtime k: 354); with bfloat16 gradients k = 1, 2 8 warps
+// 222 / 219 us (6: 220 / 234, 11: 237 / 239), k = 4 11 warps 215 us (8: 222).  The seven
+// ballots per entry at k = 8 want the most warps in flight.
+constexpr int kTernaryEncodeWarps[2][4] = {{kStepWarpsLight, kStepWarpsLight, kStepWarpsMid, kStepWarps},
+                                           {kStepWarpsMid, kStepWarpsMid, kStepWarps, kStepWarps}};
+
 int encode_warps(int mode, int k, int wire, bool bf16, int* kv) {
   *kv = 0;
   if (mode == kModeDemo) {
-    if (wire == kWireTernary) return kStepWarps;
+    if (wire == kWireTernary) {
+      if (k != 1 && k != 2 && k != 4 && k != 8) return kStepWarps;
+      *kv = -k;
+      return kTernaryEncodeWarps[bf16 ? 1 : 0][k == 1 ? 0 : k == 2 ? 1 : k == 4 ? 2 : 3];
+    }
     if (k == 1 || k == 2 || k == 4 || k == 8) {
       if (!bf16 && k <= 2) {
         *kv = k;
@@ -321,6 +384,10 @@ static cudaError_t launch_encode_demo(const cudaLaunchConfig_t& cfg, const Encod
     case 2: return cudaLaunchKernelEx(&cfg, encode_kernel<kModeDemo, BF16, WARPS, 2>, p);
     case 4: return cudaLaunchKernelEx(&cfg, encode_kernel<kModeDemo, BF16, WARPS, 4>, p);
     case 8: return cudaLaunchKernelEx(&cfg, encode_kernel<kModeDemo, BF16, WARPS, 8>, p);
+    case -1: return cudaLaunchKernelEx(&cfg, encode_kernel<kModeDemo, BF16, WARPS, -1>, p);
+    case -2: return cudaLaunchKernelEx(&cfg, encode_kernel<kModeDemo, BF16, WARPS, -2>, p);
+    case -4: return cudaLaunchKernelEx(&cfg, encode_kernel<kModeDemo, BF16, WARPS, -4>, p);
+    case -8: return cudaLaunchKernelEx(&cfg, encode_kernel<kModeDemo, BF16, WARPS, -8>, p);
     default: return cudaLaunchKernelEx(&cfg, encode_kernel<kModeDemo, BF16, WARPS, 0>, p);
   }
 }
@@ -373,11 +440,19 @@ static cudaError_t prepare_encode_w() {
   DEMO_ATTR(kModeDemo, false, 2)
   DEMO_ATTR(kModeDemo, false, 4)
   DEMO_ATTR(kModeDemo, false, 8)
+  DEMO_ATTR(kModeDemo, false, -1)
+  DEMO_ATTR(kModeDemo, false, -2)
+  DEMO_ATTR(kModeDemo, false, -4)
+  DEMO_ATTR(kModeDemo, false, -8)
   DEMO_ATTR(kModeDemo, true, 0)
   DEMO_ATTR(kModeDemo, true, 1)
   DEMO_ATTR(kModeDemo, true, 2)
   DEMO_ATTR(kModeDemo, true, 4)
   DEMO_ATTR(kModeDemo, true, 8)
+  DEMO_ATTR(kModeDemo, true, -1)
+  DEMO_ATTR(kModeDemo, true, -2)
+  DEMO_ATTR(kModeDemo, true, -4)
+  DEMO_ATTR(kModeDemo, true, -8)
   DEMO_ATTR(kModeRandom, false, 0)
   DEMO_ATTR(kModeRandom, true, 0)
   DEMO_ATTR(kModeStride, false, 0)

@@ -114,7 +114,7 @@ cudaError_t launch_adamw(const AdamWParams& p, bool bf16, int grid, cudaStream_t
 // selection says otherwise (encode_warps, and the decode's staging shape).
 int encode_warps(int mode, int k, int wire, bool bf16, int* kv);
 // kv: DeMo's k when the encode is specialised for it (1, 2, 4 or 8 with a float32 or
-// 16-bit format), else 0.
+// 16-bit format; -1, -2, -4 or -8 for those k with the ternary format), else 0.
 // `warps` picks the build (shared-memory layout, register budget); `active` warps (1..warps)
 // run in each CTA.
 cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps, int kv, int active, int grid,

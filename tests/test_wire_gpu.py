@@ -62,6 +62,12 @@ def test_wire_many_replicas(mode, k, sign, R, wire):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("k", [1, 2, 4, 8])
+def test_ternary_with_bf16_gradients(k):
+    """The ternary DeMo encode compiled for k, fed bfloat16 gradients."""
+    run_steps(RAGGED, 2, k, "demo", True, 2, g_std=1e-3, seed=29, bf16=True, wire="ternary")
+
+
 def _encode(n, mode, k, wire, g, m, step=0):
     v, i = dm.payload_buffers(mode, n, k, step=step, diloco_period=8, wire=wire)
     dm.encode(g, m, v, i, k=k, beta=0.9, mode=mode, sign=True, seed=5, step=step, diloco_period=8, wire=wire)
