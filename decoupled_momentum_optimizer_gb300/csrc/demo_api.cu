@@ -180,6 +180,15 @@ int run_momentum(DeviceState* st, int64_t n, float beta, int R, const void* cons
   return to_status(e);
 }
 
+// DeMo's fused step compiled for k (the top-k and the payload loop unrolled), where it measured
+// faster than the runtime-k kernel: every k in {1, 2, 4, 8} with bfloat16 gradients (2^28,
+// R = 2: k = 4 1160 -> 1096 us, k = 8 1287 -> 1187; 2^26, R = 8: k = 4 1005 -> 891), and k = 1
+// and k = 8 with float32 gradients (k = 8 with eight warps: 1288 -> 1251 us).  With float32
+// gradients and k = 2 or 4 the compiled kernel was 2-4% slower and is not used.
+bool step_kv(int mode, int k, bool bf16) {
+  return mode == DEMO_MODE_DEMO && (k == 1 || k == 2 || k == 4 || k == 8) && (bf16 || k == 1 || k == 8);
+}
+
 template <int MAXR>
 int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float lr, int mode, int sign, int R,
              const void* const* g, int grad_dtype, float* const* m, int diloco_period, uint64_t seed, uint64_t step,
@@ -214,11 +223,13 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
   p.fault = st->fault;
   p.stall_at = st->stall_at.exchange(0);
   const TileShape sh = tile_shape(step_warps(mode, p.k, bf16, R, p.sync != 0), kStepWarps, p.ntiles, st);
+  // DeMo with k in {1, 2, 4, 8} runs the step compiled for its k
+  const int kv = step_kv(mode, k, bf16) ? k : 0;
   cudaError_t e;
   if constexpr (MAXR == kSmallReplicas) {
-    e = launch_step_small(p, mode, bf16, sh.inst, sh.active, sh.grid, stream);
+    e = launch_step_small(p, mode, bf16, sh.inst, kv, sh.active, sh.grid, stream);
   } else {
-    e = launch_step_large(p, mode, bf16, sh.inst, sh.active, sh.grid, stream);
+    e = launch_step_large(p, mode, bf16, sh.inst, kv, sh.active, sh.grid, stream);
   }
   return to_status(e);
 }
@@ -235,8 +246,10 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
 // directly.
 // How the spans move (measured on 2^24 and 2^26 shards with 8 to 64 replicas): with more
 // than four replicas, lane copies for spans up to 320 bytes (192 in the 11-warp shape), bulk
-// copies for longer ones; DeMo payloads with k in {1, 2, 4, 8} that no shape holds whole are
-// read directly, F replicas at a time, from 256-byte spans on, and staged in groups below.
+// copies for longer ones.  Payloads that no shape holds whole are read directly, F = 32 / k
+// replicas at a time, when k is 1, 2, 4 or 8 with a float32 or 16-bit format: DeMo's from
+// 256-byte spans on (staged in groups below), Random's and Striding's always (2^26, R = 64:
+// 1.1-2.2x faster than groups).
 constexpr size_t kLaneCopyMaxSpan = 320;
 constexpr size_t kLaneCopyMaxSpanWide = 192;
 constexpr size_t kDirectMinSpan = 256;
@@ -279,7 +292,8 @@ int stage_payloads(P& p, int mode, int k, int wire, int R, int* flavor) {
       // replicas): stage them a group at a time, one item per group, with the largest
       // staging area (8 warps, 6 KB), so that each item moves as much as it can.  Random
       // and Striding keep per-draw sums across the items for k <= 8 only.
-      const bool direct = kv_path && !ternary && span >= kDirectMinSpan;
+      const bool pow2 = k == 1 || k == 2 || k == 4 || k == 8;
+      const bool direct = kv_path ? (!ternary && span >= kDirectMinSpan) : (!demo && pow2 && !ternary);
       if (direct) {
         ns = 0;
       } else if (demo || k <= 8) {
@@ -355,7 +369,12 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
   // DeMo with k in {1, 2, 4, 8} runs the decode compiled for its k: kv = k for the float32 and
   // 16-bit formats, kv = -k for the ternary one
   const bool kv_ok = mode == DEMO_MODE_DEMO && (k == 1 || k == 2 || k == 4 || k == 8);
-  const int kv = kv_ok ? (wire == DEMO_WIRE_TERNARY ? -k : k) : 0;
+  // Random and Striding with many replicas, none staged (read directly, F at a time), and k in
+  // {1, 2, 4, 8} with a float32 or 16-bit format run the decode compiled for k as well
+  const bool scheme_kv = (mode == DEMO_MODE_RANDOM || mode == DEMO_MODE_STRIDE) && R > kSmallReplicas &&
+                         (k == 1 || k == 2 || k == 4 || k == 8) && wire != DEMO_WIRE_TERNARY && p.nstaged == 0 &&
+                         p.group == 0;
+  const int kv = kv_ok ? (wire == DEMO_WIRE_TERNARY ? -k : k) : (scheme_kv ? k : 0);
   cudaError_t e;
   if constexpr (MAXR == kSmallReplicas) {
     e = launch_decode_small(p, mode, sh.inst, kv, sh.active, sh.grid, stream);

@@ -122,6 +122,50 @@ __device__ __forceinline__ void load_payload(const void* vals, const void* idx, 
   }
 }
 
+// One chunk's KV values of a float32 or 16-bit payload (KV in {1, 2, 4, 8}), one vector load.
+template <int KV>
+__device__ __forceinline__ void load_values(const void* vals, int wire, long long c, float (&v)[KV]) {
+  if (wire == kWireF32) {
+    const float* row = static_cast<const float*>(vals) + c * KV;
+    if constexpr (KV == 1) {
+      v[0] = row[0];
+    } else if constexpr (KV == 2) {
+      const float2 a = *reinterpret_cast<const float2*>(row);
+      v[0] = a.x;
+      v[1] = a.y;
+    } else {
+#pragma unroll
+      for (int q = 0; q < KV / 4; ++q) {
+        const float4 a = reinterpret_cast<const float4*>(row)[q];
+        v[4 * q] = a.x;
+        v[4 * q + 1] = a.y;
+        v[4 * q + 2] = a.z;
+        v[4 * q + 3] = a.w;
+      }
+    }
+  } else {
+    const uint16_t* row = static_cast<const uint16_t*>(vals) + c * KV;
+    uint32_t h[(KV + 1) / 2];
+    if constexpr (KV == 1) {
+      h[0] = row[0];
+    } else if constexpr (KV == 2) {
+      h[0] = *reinterpret_cast<const uint32_t*>(row);
+    } else if constexpr (KV == 4) {
+      const uint2 a = *reinterpret_cast<const uint2*>(row);
+      h[0] = a.x;
+      h[1] = a.y;
+    } else {
+      const uint4 a = *reinterpret_cast<const uint4*>(row);
+      h[0] = a.x;
+      h[1] = a.y;
+      h[2] = a.z;
+      h[3] = a.w;
+    }
+#pragma unroll
+    for (int i = 0; i < KV; ++i) v[i] = wire_from_bits16((h[i / 2] >> (16 * (i & 1))) & 0xffffu, wire);
+  }
+}
+
 // Adds one replica's entries for chunk c (sum and count per slot u) to acc.
 // vals / idx address either the payload buffers (chunk c of tile `tile`) or a
 // staged copy of the tile's spans (c = lane, tile = 0).  `valid`: the chunk
@@ -568,21 +612,43 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
         }
         const bool reads = valid || p.wire == kWireTernary;  // rows past the end read nothing
         int r = ns;
-        for (; r + 4 <= p.R; r += 4) {
-          float pv[4][8];
+        if constexpr (KV > 0) {
+          // k compiled (the receiver of many replicas, none staged): 32 / k replicas' vector
+          // loads in flight together, k sums
+          constexpr int F = 32 / KV;
+          for (; r + F <= p.R; r += F) {
+            float pv[F][KV];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (reads) {
-              load_one(p.vals[r + q], c, tile, pv[q]);
-            } else {
+            for (int q = 0; q < F; ++q) {
+              if (reads) {
+                load_values<KV>(p.vals[r + q], p.wire, c, pv[q]);
+              } else {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) pv[q][j] = 0.0f;
+                for (int j = 0; j < KV; ++j) pv[q][j] = 0.0f;
+              }
             }
+#pragma unroll
+            for (int q = 0; q < F; ++q)
+#pragma unroll
+              for (int j = 0; j < KV; ++j) sum[j] += pv[q][j];
           }
+        } else {
+          for (; r + 4 <= p.R; r += 4) {
+            float pv[4][8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 4; ++q) {
+              if (reads) {
+                load_one(p.vals[r + q], c, tile, pv[q]);
+              } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) sum[j] += pv[q][j];
+                for (int j = 0; j < 8; ++j) pv[q][j] = 0.0f;
+              }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+              for (int j = 0; j < 8; ++j) sum[j] += pv[q][j];
+          }
         }
         for (; r < p.R; ++r) {
           float pv[8];
@@ -642,6 +708,12 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
   }
 }
 
+// Random and Striding decodes compiled for k (kv in {1, 2, 4, 8}, float32 or 16-bit values)
+// exist only where they run: the many-replica kernels of the 11-warp plain shape, whose
+// replicas are all read directly; every other kernel takes k at run time (kv = 0).
+template <int MAXR, int WARPS, int FLAV>
+constexpr bool kSchemeKV = MAXR > kSmallReplicas && WARPS == kDecShapes[0] && FLAV == kFlavPlain;
+
 template <int MAXR, int WARPS, int FLAV>
 static cudaError_t launch_decode_w(const DecodeParams<MAXR>& p, int mode, int kv, int active, int grid,
                                    cudaStream_t st) {
@@ -668,8 +740,28 @@ static cudaError_t launch_decode_w(const DecodeParams<MAXR>& p, int mode, int kv
         case -8: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS, -8, FLAV>, p);
         default: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeDemo, MAXR, WARPS, 0, FLAV>, p);
       }
-    case kModeRandom: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeRandom, MAXR, WARPS, 0, FLAV>, p);
-    case kModeStride: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeStride, MAXR, WARPS, 0, FLAV>, p);
+    case kModeRandom:
+      if constexpr (kSchemeKV<MAXR, WARPS, FLAV>) {
+        switch (kv) {
+          case 1: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeRandom, MAXR, WARPS, 1, FLAV>, p);
+          case 2: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeRandom, MAXR, WARPS, 2, FLAV>, p);
+          case 4: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeRandom, MAXR, WARPS, 4, FLAV>, p);
+          case 8: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeRandom, MAXR, WARPS, 8, FLAV>, p);
+          default: break;
+        }
+      }
+      return cudaLaunchKernelEx(&cfg, decode_kernel<kModeRandom, MAXR, WARPS, 0, FLAV>, p);
+    case kModeStride:
+      if constexpr (kSchemeKV<MAXR, WARPS, FLAV>) {
+        switch (kv) {
+          case 1: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeStride, MAXR, WARPS, 1, FLAV>, p);
+          case 2: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeStride, MAXR, WARPS, 2, FLAV>, p);
+          case 4: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeStride, MAXR, WARPS, 4, FLAV>, p);
+          case 8: return cudaLaunchKernelEx(&cfg, decode_kernel<kModeStride, MAXR, WARPS, 8, FLAV>, p);
+          default: break;
+        }
+      }
+      return cudaLaunchKernelEx(&cfg, decode_kernel<kModeStride, MAXR, WARPS, 0, FLAV>, p);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -705,6 +797,16 @@ static cudaError_t prepare_decode_w() {
   if (e == cudaSuccess) e = set_smem(decode_kernel<kModeDemo, MAXR, WARPS, -8, FLAV>, bytes);
   if (e == cudaSuccess) e = set_smem(decode_kernel<kModeRandom, MAXR, WARPS, 0, FLAV>, bytes);
   if (e == cudaSuccess) e = set_smem(decode_kernel<kModeStride, MAXR, WARPS, 0, FLAV>, bytes);
+  if constexpr (kSchemeKV<MAXR, WARPS, FLAV>) {
+    if (e == cudaSuccess) e = set_smem(decode_kernel<kModeRandom, MAXR, WARPS, 1, FLAV>, bytes);
+    if (e == cudaSuccess) e = set_smem(decode_kernel<kModeRandom, MAXR, WARPS, 2, FLAV>, bytes);
+    if (e == cudaSuccess) e = set_smem(decode_kernel<kModeRandom, MAXR, WARPS, 4, FLAV>, bytes);
+    if (e == cudaSuccess) e = set_smem(decode_kernel<kModeRandom, MAXR, WARPS, 8, FLAV>, bytes);
+    if (e == cudaSuccess) e = set_smem(decode_kernel<kModeStride, MAXR, WARPS, 1, FLAV>, bytes);
+    if (e == cudaSuccess) e = set_smem(decode_kernel<kModeStride, MAXR, WARPS, 2, FLAV>, bytes);
+    if (e == cudaSuccess) e = set_smem(decode_kernel<kModeStride, MAXR, WARPS, 4, FLAV>, bytes);
+    if (e == cudaSuccess) e = set_smem(decode_kernel<kModeStride, MAXR, WARPS, 8, FLAV>, bytes);
+  }
   return e;
 }
 

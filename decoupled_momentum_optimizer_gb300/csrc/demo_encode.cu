@@ -370,10 +370,17 @@ int encode_warps(int mode, int k, int wire, bool bf16, int* kv) {
     if (bf16) return k == 1 ? kStepWarpsMid : kStepWarps;
     return k <= 6 ? kStepWarpsMid : kStepWarps;
   }
-  // Random with float32 gradients: k <= 2 draws per chunk are light enough for six warps
-  // (1-3% faster than eight on 2^26-2^28 shards and the ViT-B shard); k = 8 wants eight.
-  if (mode == kModeRandom) return bf16 ? kStepWarps : (k <= 2 ? kStepWarpsLight : kStepWarpsMid);
-  if (mode == kModeStride) return bf16 ? kStepWarpsLight : kStepWarps;
+  // Random with float32 gradients: k <= 4 draws per chunk are light enough for six warps
+  // (k <= 2: 1-3% faster than eight on 2^26-2^28 shards and the ViT-B shard; k = 4 on a 2^27
+  // shard 247 us against 282 us with eight); k = 8 wants eight (six: 363 us, eight: 276).
+  // With bfloat16 gradients k <= 2 take six (201 / 206 us against 216 / 225 with eleven), k = 4
+  // eight (222 against 243), k = 8 eleven (241; eight: 275).
+  if (mode == kModeRandom) {
+    if (bf16) return k <= 2 ? kStepWarpsLight : k == 4 ? kStepWarpsMid : kStepWarps;
+    return k <= 4 ? kStepWarpsLight : kStepWarpsMid;
+  }
+  // Striding with float32 gradients: eleven warps, but six for k = 8 (2^27: 277 us against 285).
+  if (mode == kModeStride) return bf16 ? kStepWarpsLight : (k == 8 ? kStepWarpsLight : kStepWarps);
   return bf16 ? kStepWarpsLight : kStepWarpsMid;
 }
 

@@ -47,10 +47,11 @@ constexpr int kStepWarpsMid = 8;
 constexpr int kStepWarpsLight = 6;
 int step_warps(int mode, int k, bool bf16, int R, bool sync);
 // `warps` picks the build (its shared-memory layout and register budget); `active` warps
-// (1..warps) run in each CTA.
-cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, bool bf16, int warps, int active,
+// (1..warps) run in each CTA.  kv: DeMo's k when the step is compiled for it (1, 2, 4 or 8),
+// else 0.
+cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, bool bf16, int warps, int kv, int active,
                               int grid, cudaStream_t st);
-cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int warps, int active,
+cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int warps, int kv, int active,
                               int grid, cudaStream_t st);
 
 // The tile kernels are persistent: each assumes one CTA per SM (its grid is at most one CTA

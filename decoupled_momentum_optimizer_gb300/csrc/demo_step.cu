@@ -36,7 +36,9 @@ struct alignas(1024) StepWarpSmem {
 constexpr size_t step_smem(int warps) { return 1024 + warps * sizeof(StepWarpSmem) + warps * 16 + 272; }
 static_assert(step_smem(kStepWarps) <= 232448, "shared memory per CTA");
 
-template <int MODE, bool BF16, int MAXR, int WARPS>
+// KV > 0 (DeMo, k in {1, 2, 4, 8}): k is KV at compile time, so the top-k and the payload
+// loop unroll; KV = 0: k is the runtime value.
+template <int MODE, bool BF16, int MAXR, int WARPS, int KV>
 __global__ void __launch_bounds__(WARPS * 32, 1) step_kernel(const __grid_constant__ StepParams<MAXR> p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte aligned start (the TMA swizzle patterns are relative to 1024-byte boundaries),
@@ -155,14 +157,16 @@ __global__ void __launch_bounds__(WARPS * 32, 1) step_kernel(const __grid_consta
       if constexpr (MODE == kModeDemo) {
         float X[32], Xs[32];
         dct32_forward(x, X);
-        const uint32_t M = topk_select(X, p.k, Xs);
+        const int kk = KV > 0 ? KV : p.k;
+        const uint32_t M = topk_select(X, kk, Xs);
         __syncwarp();  // every lane has read its g row: the g tile becomes the stash
         float* stash = ws.gbuf[s];
 #pragma unroll
         for (int u = 0; u < 32; ++u) stash[u * 32 + lane] = Xs[u];
         uint32_t mm = M;
         if (p.wire >= kWireBF16) {
-          for (int j = 0; j < p.k; ++j) {  // payload in ascending u, rounded as the wire format rounds it
+#pragma unroll
+          for (int j = 0; j < kk; ++j) {  // payload in ascending u, rounded as the wire format rounds it
             const int u = __ffs(mm) - 1;
             mm &= mm - 1;
             float v = stash[u * 32 + lane];
@@ -170,7 +174,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) step_kernel(const __grid_consta
             ws.acc[u * 32 + lane] += wire_round(v, p.wire);
           }
         } else {
-          for (int j = 0; j < p.k; ++j) {  // payload in ascending u
+#pragma unroll
+          for (int j = 0; j < kk; ++j) {  // payload in ascending u
             const int u = __ffs(mm) - 1;
             mm &= mm - 1;
             float v = stash[u * 32 + lane];
@@ -262,11 +267,23 @@ int step_warps(int mode, int k, bool bf16, int R, bool sync) {
   if (mode == kModeDiloco) return sync ? kStepWarpsLight : kStepWarpsMid;
   if (mode == kModeRandom) return k <= R + 1 ? kStepWarpsLight : kStepWarpsMid;
   if (k == 1 && !bf16) return kStepWarpsLight;
+  if (k == 8 && !bf16) return kStepWarpsMid;  // the step compiled for k = 8 (float32 gradients)
   return k <= 6 ? kStepWarpsMid : kStepWarps;
 }
 
+template <int MAXR, int WARPS, bool BF16>
+static cudaError_t launch_step_demo(const cudaLaunchConfig_t& cfg, const StepParams<MAXR>& p, int kv) {
+  switch (kv) {
+    case 1: return cudaLaunchKernelEx(&cfg, step_kernel<kModeDemo, BF16, MAXR, WARPS, 1>, p);
+    case 2: return cudaLaunchKernelEx(&cfg, step_kernel<kModeDemo, BF16, MAXR, WARPS, 2>, p);
+    case 4: return cudaLaunchKernelEx(&cfg, step_kernel<kModeDemo, BF16, MAXR, WARPS, 4>, p);
+    case 8: return cudaLaunchKernelEx(&cfg, step_kernel<kModeDemo, BF16, MAXR, WARPS, 8>, p);
+    default: return cudaLaunchKernelEx(&cfg, step_kernel<kModeDemo, BF16, MAXR, WARPS, 0>, p);
+  }
+}
+
 template <int MAXR, int WARPS>
-static cudaError_t launch_step_w(const StepParams<MAXR>& p, int mode, bool bf16, int active, int grid,
+static cudaError_t launch_step_w(const StepParams<MAXR>& p, int mode, bool bf16, int kv, int active, int grid,
                                  cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -278,10 +295,10 @@ static cudaError_t launch_step_w(const StepParams<MAXR>& p, int mode, bool bf16,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (mode == kModeDemo)
+    return bf16 ? launch_step_demo<MAXR, WARPS, true>(cfg, p, kv) : launch_step_demo<MAXR, WARPS, false>(cfg, p, kv);
 #define DEMO_LAUNCH(M, B) \
-  if (mode == M && bf16 == B) return cudaLaunchKernelEx(&cfg, step_kernel<M, B, MAXR, WARPS>, p);
-  DEMO_LAUNCH(kModeDemo, false)
-  DEMO_LAUNCH(kModeDemo, true)
+  if (mode == M && bf16 == B) return cudaLaunchKernelEx(&cfg, step_kernel<M, B, MAXR, WARPS, 0>, p);
   DEMO_LAUNCH(kModeRandom, false)
   DEMO_LAUNCH(kModeRandom, true)
   DEMO_LAUNCH(kModeStride, false)
@@ -293,40 +310,48 @@ static cudaError_t launch_step_w(const StepParams<MAXR>& p, int mode, bool bf16,
 }
 
 template <int MAXR>
-static cudaError_t launch_step_t(const StepParams<MAXR>& p, int mode, bool bf16, int warps, int active, int grid,
-                                 cudaStream_t st) {
+static cudaError_t launch_step_t(const StepParams<MAXR>& p, int mode, bool bf16, int warps, int kv, int active,
+                                 int grid, cudaStream_t st) {
   if (active < 1 || active > warps) return cudaErrorInvalidValue;
-  if (warps == kStepWarpsLight) return launch_step_w<MAXR, kStepWarpsLight>(p, mode, bf16, active, grid, st);
-  if (warps == kStepWarpsMid) return launch_step_w<MAXR, kStepWarpsMid>(p, mode, bf16, active, grid, st);
-  if (warps == kStepWarps) return launch_step_w<MAXR, kStepWarps>(p, mode, bf16, active, grid, st);
+  if (warps == kStepWarpsLight) return launch_step_w<MAXR, kStepWarpsLight>(p, mode, bf16, kv, active, grid, st);
+  if (warps == kStepWarpsMid) return launch_step_w<MAXR, kStepWarpsMid>(p, mode, bf16, kv, active, grid, st);
+  if (warps == kStepWarps) return launch_step_w<MAXR, kStepWarps>(p, mode, bf16, kv, active, grid, st);
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, bool bf16, int warps, int active,
+cudaError_t launch_step_small(const StepParams<kSmallReplicas>& p, int mode, bool bf16, int warps, int kv, int active,
                               int grid, cudaStream_t st) {
-  return launch_step_t(p, mode, bf16, warps, active, grid, st);
+  return launch_step_t(p, mode, bf16, warps, kv, active, grid, st);
 }
 
-cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int warps, int active,
+cudaError_t launch_step_large(const StepParams<kMaxReplicas>& p, int mode, bool bf16, int warps, int kv, int active,
                               int grid, cudaStream_t st) {
-  return launch_step_t(p, mode, bf16, warps, active, grid, st);
+  return launch_step_t(p, mode, bf16, warps, kv, active, grid, st);
 }
 
 template <int MAXR, int WARPS>
 static cudaError_t prepare_w() {
   cudaError_t e = cudaSuccess;
-#define DEMO_ATTR(M, B)                                                                                  \
-  if (e == cudaSuccess)                                                                                  \
-    e = cudaFuncSetAttribute(step_kernel<M, B, MAXR, WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+#define DEMO_ATTR(M, B, KV)                                                                                  \
+  if (e == cudaSuccess)                                                                                      \
+    e = cudaFuncSetAttribute(step_kernel<M, B, MAXR, WARPS, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                              static_cast<int>(persistent_smem(step_smem(WARPS))));
-  DEMO_ATTR(kModeDemo, false)
-  DEMO_ATTR(kModeDemo, true)
-  DEMO_ATTR(kModeRandom, false)
-  DEMO_ATTR(kModeRandom, true)
-  DEMO_ATTR(kModeStride, false)
-  DEMO_ATTR(kModeStride, true)
-  DEMO_ATTR(kModeDiloco, false)
-  DEMO_ATTR(kModeDiloco, true)
+  DEMO_ATTR(kModeDemo, false, 0)
+  DEMO_ATTR(kModeDemo, false, 1)
+  DEMO_ATTR(kModeDemo, false, 2)
+  DEMO_ATTR(kModeDemo, false, 4)
+  DEMO_ATTR(kModeDemo, false, 8)
+  DEMO_ATTR(kModeDemo, true, 0)
+  DEMO_ATTR(kModeDemo, true, 1)
+  DEMO_ATTR(kModeDemo, true, 2)
+  DEMO_ATTR(kModeDemo, true, 4)
+  DEMO_ATTR(kModeDemo, true, 8)
+  DEMO_ATTR(kModeRandom, false, 0)
+  DEMO_ATTR(kModeRandom, true, 0)
+  DEMO_ATTR(kModeStride, false, 0)
+  DEMO_ATTR(kModeStride, true, 0)
+  DEMO_ATTR(kModeDiloco, false, 0)
+  DEMO_ATTR(kModeDiloco, true, 0)
 #undef DEMO_ATTR
   return e;
 }

@@ -142,6 +142,8 @@ CASES = [
     ("demo", 8, False, 3, False), ("demo", 4, True, 2, True), ("demo", 5, True, 2, False),
     ("demo", 16, False, 2, False), ("demo", 32, False, 1, False),
     ("demo", 8, True, 2, False), ("demo", 4, True, 4, False),  # decode stages every replica in 3 KB
+    # the DeMo step compiled for k with bfloat16 gradients (R = 5: the many-replica kernels)
+    ("demo", 1, False, 2, True), ("demo", 2, True, 3, True), ("demo", 8, True, 5, True), ("demo", 8, False, 2, True),
     ("random", 1, True, 2, False), ("random", 8, False, 2, False), ("random", 8, True, 3, True),
     ("random", 3, False, 1, False), ("random", 32, True, 2, False),
     ("stride", 1, True, 2, False), ("stride", 4, False, 2, False), ("stride", 8, True, 5, True),
