@@ -184,9 +184,11 @@ int run_momentum(DeviceState* st, int64_t n, float beta, int R, const void* cons
 // faster than the runtime-k kernel: every k in {1, 2, 4, 8} with bfloat16 gradients (2^28,
 // R = 2: k = 4 1160 -> 1096 us, k = 8 1287 -> 1187; 2^26, R = 8: k = 4 1005 -> 891), and k = 1
 // and k = 8 with float32 gradients (k = 8 with eight warps: 1288 -> 1251 us).  With float32
-// gradients and k = 2 or 4 the compiled kernel was 2-4% slower and is not used.
-bool step_kv(int mode, int k, bool bf16) {
-  return mode == DEMO_MODE_DEMO && (k == 1 || k == 2 || k == 4 || k == 8) && (bf16 || k == 1 || k == 8);
+// gradients and k = 2 or 4 the compiled kernel was 2-4% slower on large shards and is used only
+// on small ones (at most kLatencyTilesPerWarp tiles per warp), where its fewer instructions win
+// (2^21, R = 8, k = 4: 47.1 -> 43.9 us).
+bool step_kv(int mode, int k, bool bf16, bool small) {
+  return mode == DEMO_MODE_DEMO && (k == 1 || k == 2 || k == 4 || k == 8) && (bf16 || small || k == 1 || k == 8);
 }
 
 template <int MAXR>
@@ -224,7 +226,10 @@ int run_step(DeviceState* st, float* theta, int64_t n, int k, float beta, float 
   p.stall_at = st->stall_at.exchange(0);
   const TileShape sh = tile_shape(step_warps(mode, p.k, bf16, R, p.sync != 0), kStepWarps, p.ntiles, st);
   // DeMo with k in {1, 2, 4, 8} runs the step compiled for its k
-  const int kv = step_kv(mode, k, bf16) ? k : 0;
+  // small shards (at most kLatencyTilesPerWarp tiles per warp of the widest build) are bound by
+  // the issue rate of a few warps, not by HBM
+  const bool small = (p.ntiles + st->sms * kStepWarps - 1) / (st->sms * kStepWarps) <= kLatencyTilesPerWarp;
+  const int kv = step_kv(mode, k, bf16, small) ? k : 0;
   cudaError_t e;
   if constexpr (MAXR == kSmallReplicas) {
     e = launch_step_small(p, mode, bf16, sh.inst, kv, sh.active, sh.grid, stream);
