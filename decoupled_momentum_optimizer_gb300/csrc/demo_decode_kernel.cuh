@@ -430,8 +430,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
   // Items are loaded strictly in order: the loads keep their own (tile, item) cursor.  The
   // whole warp runs issue(); lane 0 starts the theta tile's copy (and, without lane copies,
   // the spans' bulk copies) on the slot's barrier.  With lane copies every call commits one
-  // copy group, empty past the last item, so the item i is always the group two behind the
-  // newest when it is consumed.
+  // copy group, empty past the last item: when item i is consumed, groups up to i + 1 are
+  // committed, and waiting for all but the newest one completes item i's.
   long long ld_t = gw, ld_item = 0;
   int ld_g = 0, ld_slot = 0;
   auto issue = [&]() {
