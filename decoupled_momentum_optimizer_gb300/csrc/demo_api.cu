@@ -264,6 +264,8 @@ int stage_payloads(P& p, int mode, int k, int wire, int R, int* flavor) {
   p.nstaged = 0;
   p.group = 0;
   p.vspan = p.ispan = 0;
+  p.sstride = 0;
+  p.lane_unit = 16;
   *flavor = kFlavPlain;
   if (mode == DEMO_MODE_DILOCO) return kDecShapes[0];
   const bool demo = mode == DEMO_MODE_DEMO;
@@ -278,15 +280,22 @@ int stage_payloads(P& p, int mode, int k, int wire, int R, int* flavor) {
   const bool kv_path = demo && (k == 1 || k == 2 || k == 4 || k == 8);
   const bool ternary = wire == DEMO_WIRE_TERNARY;
   const size_t span = vs + is;
+  // Ternary spans that are not 16-byte multiples (odd k, and DeMo's index planes for k = 1, 2)
+  // are 4-byte multiples: lane copies of 4-byte units stage them, each replica at a 16-byte
+  // aligned stride (2^26 decode, DeMo k = 1: R = 2 112 -> 88 us, R = 64 1365 -> 375 us, against
+  // reading their words directly on each tile).  The float32 and 16-bit spans are always
+  // 16-byte multiples.
+  const bool units4 = ternary && (vs % 16 || is % 16);
+  const size_t stride = (span + 15) / 16 * 16;
   const size_t small = static_cast<size_t>(dec_stage_bytes(kDecShapes[0]));
-  if (vs % 16 || is % 16 || span > small) return kDecShapes[0];
+  if ((!units4 && (vs % 16 || is % 16)) || vs % 4 || is % 4 || stride > small) return kDecShapes[0];
   int aligned = 0;  // leading replicas with 16-byte aligned buffers
   while (aligned < R && aligned16(p.vals[aligned]) && (!demo || aligned16(p.idx[aligned]))) ++aligned;
   int warps = kDecShapes[0];
-  int ns = static_cast<int>(std::min<size_t>(aligned, small / span));
+  int ns = static_cast<int>(std::min<size_t>(aligned, small / stride));
   if (ns < R && aligned == R) {
     for (int w : kDecShapes) {
-      if (R * span <= static_cast<size_t>(dec_stage_bytes(w))) {
+      if (R * stride <= static_cast<size_t>(dec_stage_bytes(w))) {
         warps = w;
         ns = R;
         break;
@@ -303,14 +312,17 @@ int stage_payloads(P& p, int mode, int k, int wire, int R, int* flavor) {
         ns = 0;
       } else if (demo || k <= 8) {
         warps = kDecShapes[3];
-        p.group = static_cast<int>(static_cast<size_t>(dec_stage_bytes(warps)) / span);
+        p.group = static_cast<int>(static_cast<size_t>(dec_stage_bytes(warps)) / stride);
         ns = 0;
       }
     }
   }
   p.nstaged = ns;
-  const bool lane_copy = R > kSmallReplicas && (ns > 0 || p.group > 0) &&
-                         span <= (warps == kDecShapes[0] ? kLaneCopyMaxSpanWide : kLaneCopyMaxSpan);
+  const bool staged = ns > 0 || p.group > 0;
+  const bool lane_copy = staged && (units4 || (R > kSmallReplicas &&
+                                               span <= (warps == kDecShapes[0] ? kLaneCopyMaxSpanWide : kLaneCopyMaxSpan)));
+  p.sstride = static_cast<unsigned int>(stride);
+  p.lane_unit = units4 ? 4 : 16;
   *flavor = (p.group > 0 ? kFlavGroups : kFlavPlain) | (lane_copy ? kFlavLaneCopy : kFlavPlain);
   p.vspan = static_cast<unsigned int>(vs);
   p.ispan = static_cast<unsigned int>(is);
@@ -382,7 +394,7 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
   const int kv = kv_ok ? (wire == DEMO_WIRE_TERNARY ? -k : k) : (scheme_kv ? k : 0);
   cudaError_t e;
   if constexpr (MAXR == kSmallReplicas) {
-    e = launch_decode_small(p, mode, sh.inst, kv, sh.active, sh.grid, stream);
+    e = launch_decode_small(p, mode, sh.inst, kv, flavor, sh.active, sh.grid, stream);
   } else {
     e = launch_decode_large(p, mode, sh.inst, kv, flavor, sh.active, sh.grid, stream);
   }

@@ -25,8 +25,10 @@
 
 namespace demo {
 
-cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int kv, int active,
-                                int grid, cudaStream_t st) {
+cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int kv, int flavor,
+                                int active, int grid, cudaStream_t st) {
+  if (flavor == kFlavLaneCopy) return launch_decode_lane_copy_small(p, mode, warps, kv, active, grid, st);
+  if (flavor != kFlavPlain) return cudaErrorInvalidValue;
   return launch_decode_shapes<kSmallReplicas, kFlavPlain>(p, mode, warps, kv, active, grid, st);
 }
 

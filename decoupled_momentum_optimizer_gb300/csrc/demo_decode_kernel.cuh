@@ -41,6 +41,10 @@ __device__ __forceinline__ bool vector_kd(int k) { return k == 1 || k == 2 || k 
 __device__ __forceinline__ void lane_copy16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
+// The same for a 4-byte unit (both addresses 4-byte aligned), cached in L1 and L2.
+__device__ __forceinline__ void lane_copy4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
 __device__ __forceinline__ void lane_copy_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void lane_copy_wait() {
@@ -420,13 +424,16 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
   __syncwarp();
 
   const uint32_t span = p.vspan + p.ispan;  // staged bytes per replica
+  const uint32_t stride = p.sstride;         // their distance in the staging area (span rounded up to 16)
   constexpr bool lane_copy = (FLAV & kFlavLaneCopy) != 0;
   constexpr bool kVecWords = (FLAV & kFlavGroups) == 0;  // ternary words as vectors (see demo_read)
-  // Lane copies: the staged spans of an item are 16-byte units u = 0, 1, ... (replica
-  // u / P, byte 16 (u % P) of its span); lane l copies the units l, l + 32, ...
-  const int P = static_cast<int>(span >> 4);
-  const int step_r = P ? 32 / P : 0, step_o = P ? (32 % P) * 16 : 0;
-  const int lane_r = P ? lane / P : 0, lane_o = P ? (lane % P) * 16 : 0;
+  // Lane copies: the staged spans of an item are units of US bytes (16, or 4 for the ternary
+  // spans that are not 16-byte multiples) u = 0, 1, ... (replica u / P, byte US (u % P) of its
+  // span, stored at that replica's stride); lane l copies the units l, l + 32, ...
+  const int US = p.lane_unit;
+  const int P = US > 0 ? static_cast<int>(span) / US : 0;
+  const int step_r = P ? 32 / P : 0, step_o = P ? (32 % P) * US : 0;
+  const int lane_r = P ? lane / P : 0, lane_o = P ? (lane % P) * US : 0;
   // Items are loaded strictly in order: the loads keep their own (tile, item) cursor.  The
   // whole warp runs issue(); lane 0 starts the theta tile's copy (and, without lane copies,
   // the spans' bulk copies) on the slot's barrier.  With lane copies every call commits one
@@ -447,7 +454,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
         if (last) tma_load_2d(ws.tbuf[ld_slot], &p.theta, bar, 0, static_cast<int>(ld_t * 32));
         if (!lane_copy) {
           for (int r = r0; r < r1; ++r) {
-            unsigned char* d = ws.stage[ld_slot] + (r - r0) * span;
+            unsigned char* d = ws.stage[ld_slot] + (r - r0) * stride;
             bulk_load(d, static_cast<const unsigned char*>(p.vals[r]) + ld_t * p.vspan, p.vspan, bar);
             if (p.ispan)
               bulk_load(d + p.vspan, static_cast<const unsigned char*>(p.idx[r]) + ld_t * p.ispan, p.ispan, bar);
@@ -463,7 +470,12 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
               o < static_cast<int>(p.vspan)
                   ? static_cast<const unsigned char*>(p.vals[r]) + ld_t * p.vspan + o
                   : static_cast<const unsigned char*>(p.idx[r]) + ld_t * p.ispan + (o - static_cast<int>(p.vspan));
-          lane_copy16(ws.stage[ld_slot] + u * 16, src);
+          unsigned char* dst = ws.stage[ld_slot] + rr * stride + o;
+          if (US == 16) {
+            lane_copy16(dst, src);
+          } else {
+            lane_copy4(dst, src);
+          }
           rr += step_r;
           o += step_o;
           if (o >= static_cast<int>(span)) {
@@ -540,7 +552,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
       if (G > 0 && p.k <= 8) {
         for (int r = r0; r < ns; ++r) {
           float pv[8];
-          load_draws(ws.stage[s] + (r - r0) * span, lane, 0, pv);
+          load_draws(ws.stage[s] + (r - r0) * stride, lane, 0, pv);
 #pragma unroll
           for (int j = 0; j < 8; ++j) rsum[j] += pv[j];
         }
@@ -549,12 +561,12 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
     if constexpr (MODE == kModeDemo) {
       if constexpr (KV < 0) {
         demo_add_replicas<KV>(ws.acc, lane, r0, ns, true, [&](int r, DemoEntries<KV>& e) {
-          const unsigned char* sv = ws.stage[s] + (r - r0) * span;
+          const unsigned char* sv = ws.stage[s] + (r - r0) * stride;
           demo_read<KV, kVecWords>(e, sv, sv + p.vspan, p.wire, lane, 0, lane);
         });
       } else {
         for (int r = r0; r < ns; ++r) {
-          const unsigned char* sv = ws.stage[s] + (r - r0) * span;
+          const unsigned char* sv = ws.stage[s] + (r - r0) * stride;
           demo_accumulate<KV>(ws.acc, lane, sv, sv + p.vspan, p.wire, p.k, lane, 0, true, true);
         }
       }
@@ -643,7 +655,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
         if (G == 0) {
           for (int r = 0; r < ns; ++r) {
             float pv[8];
-            load_one(ws.stage[s] + r * span, lane, 0, pv);
+            load_one(ws.stage[s] + r * stride, lane, 0, pv);
 #pragma unroll
             for (int j = 0; j < 8; ++j) sum[j] += pv[j];
           }
@@ -720,7 +732,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_kernel(const __grid_cons
         const bool reads = valid || p.wire == kWireTernary;  // as in the DeMo branch
         auto take = [&](int j, int pos) {
           float sum = 0.0f;
-          for (int r = 0; r < ns; ++r) sum += payload_value(ws.stage[s] + r * span, p.wire, lane, 0, lane, p.k, j);
+          for (int r = 0; r < ns; ++r) sum += payload_value(ws.stage[s] + r * stride, p.wire, lane, 0, lane, p.k, j);
           for (int r = ns; r < p.R; ++r) sum += reads ? payload_value(p.vals[r], p.wire, c, tile, lane, p.k, j) : 0.0f;
           if (valid) qs[pos * 32 + lane] = sum * p.rcpR;
         };
@@ -862,6 +874,8 @@ cudaError_t launch_decode_lane_copy(const DecodeParams<kMaxReplicas>& p, int mod
                                     int grid, cudaStream_t st);
 cudaError_t launch_decode_groups(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int kv, int flavor,
                                  int active, int grid, cudaStream_t st);
+cudaError_t launch_decode_lane_copy_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int kv,
+                                          int active, int grid, cudaStream_t st);
 cudaError_t prepare_decode_lane_copy();
 cudaError_t prepare_decode_groups();
 

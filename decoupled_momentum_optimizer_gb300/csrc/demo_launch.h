@@ -38,6 +38,11 @@ struct DecodeParams {
   // with the theta tile; the others, and a ragged last tile, are read directly.
   int nstaged;
   unsigned int vspan, ispan;
+  // Staged replica r of an item sits at r * sstride in the staging area: vspan + ispan rounded
+  // up to 16 bytes (equal to it for bulk copies, which need 16-byte multiples).  Lane copies
+  // move lane_unit bytes per copy: 16, or 4 for ternary spans that are not 16-byte multiples.
+  unsigned int sstride;
+  int lane_unit;
   // More replicas than a staging area holds: each full tile is visited as ceil(R / group)
   // items, item i staging replicas [i * group, (i + 1) * group) and the last one also the
   // theta tile; 0 = one item per tile.
@@ -121,8 +126,8 @@ cudaError_t launch_encode(const EncodeParams& p, int mode, bool bf16, int warps,
                           cudaStream_t st);
 // kv: DeMo's k when the decode is specialised for it (1, 2, 4 or 8 with a float32 or
 // 16-bit format; -1, -2, -4 or -8 for those k with the ternary format), else 0.
-cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int kv, int active,
-                                int grid, cudaStream_t st);
+cudaError_t launch_decode_small(const DecodeParams<kSmallReplicas>& p, int mode, int warps, int kv, int flavor,
+                                int active, int grid, cudaStream_t st);
 cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, int warps, int kv, int flavor,
                                 int active, int grid, cudaStream_t st);
 

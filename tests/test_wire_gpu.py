@@ -53,6 +53,10 @@ MANY_CASES = [
     ("demo", 8, False, 17, "f16"), ("demo", 3, False, 40, "f16"), ("demo", 4, False, 5, "bf16"),
     ("random", 4, False, 64, "bf16"), ("random", 8, False, 20, "f16"), ("stride", 4, True, 64, "ternary"),
     ("stride", 4, False, 8, "bf16"), ("random", 2, True, 37, "ternary"), ("demo", 5, True, 30, "f32"),
+    # ternary spans that are not 16-byte multiples, staged by 4-byte lane copies: R <= 4, R > 4
+    # whole, and in groups (k = 7, R = 50)
+    ("demo", 2, True, 4, "ternary"), ("random", 3, True, 2, "ternary"), ("stride", 1, True, 3, "ternary"),
+    ("demo", 3, True, 6, "ternary"), ("demo", 7, True, 50, "ternary"),
 ]
 
 
