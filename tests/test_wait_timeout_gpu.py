@@ -83,3 +83,33 @@ def test_a_cancelled_request_stalls_nothing():
     dm.test_stall_next_launch(-1)
     dm.step(theta, gs, ms, k=4, beta=0.9, lr=1e-2, mode="demo", sign=True)
     assert dm.device_fault() == 0
+
+
+@pytest.mark.parametrize("mode,k,wire,R,item", [
+    ("demo", 1, "ternary", 2, 0),   # lane copies of 4-byte units (R <= 4)
+    ("demo", 1, "f32", 8, 0),       # lane copies of 16-byte units
+    ("demo", 3, "f32", 64, 1),      # groups of 12 replicas by bulk copies: the tile's second of six items
+    ("demo", 1, "f32", 64, 0),      # groups of 38 replicas by lane copies: the first of two items (no theta)
+    ("random", 4, "f32", 64, 0),    # every replica read directly
+])
+def test_every_decode_staging_flavour_gives_up_cleanly(mode, k, wire, R, item):
+    """The decode's staging flavours each give up the same way: the stalled barrier times out,
+    the warp waits for its own copies (bulk or lane copies) and returns, the fault word reads
+    1 once, and the next step is right."""
+    dm.init(0)
+    assert dm.device_fault() == 0
+    theta, ms, gs = state(R, 400)
+    kw = dict(k=k, mode=mode, seed=1, step=0, wire=wire)
+    bufs = [dm.payload_buffers(mode, N, k, wire=wire) for _ in range(R)]
+    vals = [b[0] for b in bufs]
+    idx = [b[1] for b in bufs] if mode == "demo" else None
+    for r in range(R):
+        dm.encode(gs[r], ms[r], vals[r], idx[r] if idx else None, beta=0.9, sign=True, **kw)
+    torch.cuda.synchronize()
+    dm.test_stall_next_launch(item)
+    dm.decode_update(theta, vals, idx, lr=1e-2, **kw)
+    expect_one_timeout()
+    theta, ms, gs = state(R, 500)
+    check_step(theta, ms, gs, k=k, beta=0.9, lr=1e-2, mode=mode, sign=True, seed=1, step=1, wire=wire)
+    assert dm.device_fault() == 0
+    torch.cuda.empty_cache()
