@@ -63,6 +63,16 @@ __device__ __forceinline__ float payload_value(const void* vals, int wire, long 
   return wire_from_bits16(static_cast<const uint16_t*>(vals)[c * kv + j], wire);
 }
 
+// Bit `lane` of plane word w moved to bit b, masked to that bit.  ROT: one funnel-shift rotation
+// right by lane - b and a masked OR per bit; measured faster where the words are loaded one or
+// two at a time (2^26 decode, R = 64 in groups: k = 4 936 -> 878 us; k = 1, 2 at every R) and
+// slower beside the 16-byte vector reads of k >= 4 (R = 16, k = 4: 246 -> 253 us).
+template <bool ROT>
+__device__ __forceinline__ uint32_t plane_bit(uint32_t w, int lane, int b) {
+  if constexpr (ROT) return __funnelshift_r(w, w, static_cast<uint32_t>(lane - b) & 31u) & (1u << b);
+  return ((w >> lane) & 1u) << b;
+}
+
 // Index j of chunk c in a DeMo payload (uint8, or 5 ternary bit-planes); used modulo 32.
 __device__ __forceinline__ int payload_index(const void* idx, int wire, long long c, long long tile, int lane, int k,
                                              int j) {
@@ -70,7 +80,7 @@ __device__ __forceinline__ int payload_index(const void* idx, int wire, long lon
     const uint32_t* w = static_cast<const uint32_t*>(idx) + (tile * k + j) * 5;
     int u = 0;
 #pragma unroll
-    for (int b = 0; b < 5; ++b) u |= static_cast<int>((w[b] >> lane) & 1u) << b;
+    for (int b = 0; b < 5; ++b) u |= static_cast<int>(plane_bit<true>(w[b], lane, b));
     return u;
   }
   return static_cast<const uint8_t*>(idx)[c * k + j] & 31;
@@ -289,7 +299,7 @@ __device__ __forceinline__ void demo_read(DemoEntries<KV>& e, const void* vals, 
           e.pv[j] = nz ? (ng ? -1.0f : 1.0f) : 0.0f;
           int u = 0;
 #pragma unroll
-          for (int b = 0; b < 5; ++b) u |= static_cast<int>((iwd[5 * j + b] >> lane) & 1u) << b;
+          for (int b = 0; b < 5; ++b) u |= static_cast<int>(plane_bit<false>(iwd[5 * j + b], lane, b));
           e.uu[j] = u;
         }
         return;
@@ -302,7 +312,7 @@ __device__ __forceinline__ void demo_read(DemoEntries<KV>& e, const void* vals, 
       e.pv[j] = nz ? (ng ? -1.0f : 1.0f) : 0.0f;
       int u = 0;
 #pragma unroll
-      for (int b = 0; b < 5; ++b) u |= static_cast<int>((iw[5 * j + b] >> lane) & 1u) << b;
+      for (int b = 0; b < 5; ++b) u |= static_cast<int>(plane_bit<true>(iw[5 * j + b], lane, b));
       e.uu[j] = u;
     }
   } else {
