@@ -301,7 +301,14 @@ __global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_cons
         float sv[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) sv[i] = p.sign ? sign3(x[i]) : x[i];
-        put_row(p.vals, p.wire, c, row0 >> 5, lane, valid, sv);
+        if (p.wire == kWireF32) {
+          // a float32 payload row has the momentum's layout: it leaves through the (free) g slot
+          // with the same coalesced stores (2^27 encode: 355 -> 328 us, 89% -> 97% of the copy
+          // peak, against each lane storing its own row)
+          store_tile_coalesced(ws.gbuf[s], lane, sv, static_cast<float*>(p.vals), row0, p.nc);
+        } else {
+          put_row(p.vals, p.wire, c, row0 >> 5, lane, valid, sv);
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = 0.0f;
       }
