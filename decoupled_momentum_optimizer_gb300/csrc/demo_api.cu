@@ -168,14 +168,12 @@ int run_momentum(DeviceState* st, int64_t n, float beta, int R, const void* cons
   p.n4 = n / 4;
   p.R = R;
   p.beta = beta;
-  const long long want = (p.n4 + 255) / 256;
-  const int grid = static_cast<int>(want < 8LL * st->sms ? want : 8LL * st->sms);
   const bool bf16 = grad_dtype == DEMO_GRAD_BF16;
   cudaError_t e;
   if constexpr (MAXR == kSmallReplicas) {
-    e = launch_momentum_small(p, bf16, grid, stream);
+    e = launch_momentum_small(p, bf16, st->sms, stream);
   } else {
-    e = launch_momentum_large(p, bf16, grid, stream);
+    e = launch_momentum_large(p, bf16, st->sms, stream);
   }
   return to_status(e);
 }
@@ -330,7 +328,7 @@ int stage_payloads(P& p, int mode, int k, int wire, int R, int* flavor) {
 }
 
 // The DiLoCo sync step's decode is elementwise (every replica sends its whole
-// momentum): one grid-stride pass over groups of four parameters.
+// momentum): one grid-stride pass over the parameters.
 template <int MAXR>
 int run_dense_decode(DeviceState* st, float* theta, int64_t n, float lr, int R, const void* const* vals, int wire,
                      cudaStream_t stream) {
@@ -343,13 +341,11 @@ int run_dense_decode(DeviceState* st, float* theta, int64_t n, float lr, int R, 
   p.wire = wire;
   p.lr = lr;
   p.rcpR = 1.0f / static_cast<float>(R);
-  const int64_t want = (p.n4 + 255) / 256;
-  const int grid = static_cast<int>(want < 8LL * st->sms ? want : 8LL * st->sms);
   cudaError_t e;
   if constexpr (MAXR == kSmallReplicas) {
-    e = launch_dense_small(p, grid, stream);
+    e = launch_dense_small(p, st->sms, stream);
   } else {
-    e = launch_dense_large(p, grid, stream);
+    e = launch_dense_large(p, st->sms, stream);
   }
   return to_status(e);
 }
@@ -505,7 +501,7 @@ int demo_init(int device) {
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0)
     return DEMO_ECUDA;
   if (prepare_step_kernels() != cudaSuccess || prepare_encode_kernels() != cudaSuccess ||
-      prepare_decode_kernels() != cudaSuccess)
+      prepare_decode_kernels() != cudaSuccess || prepare_dense_kernels() != cudaSuccess)
     return DEMO_ECUDA;
   void* fault = nullptr;
   if (cudaGetSymbolAddress(&fault, g_fault_word) != cudaSuccess) return DEMO_ECUDA;

@@ -74,7 +74,9 @@ constexpr int kFlavLaneCopy = 1;
 constexpr int kFlavGroups = 2;
 constexpr int kFlavGroupsLaneCopy = kFlavGroups | kFlavLaneCopy;
 
-// Dense decode (the DiLoCo sync step's receiver; elementwise over groups of four).
+// Dense decode (the DiLoCo sync step's receiver; elementwise over groups of four).  The
+// launchers of it and of the momentum pass size their grid themselves (one wave of resident
+// CTAs on `sms` SMs).
 template <int MAXR>
 struct DenseParams {
   float* theta;
@@ -84,8 +86,8 @@ struct DenseParams {
   float lr, rcpR;
 };
 
-cudaError_t launch_dense_small(const DenseParams<kSmallReplicas>& p, int grid, cudaStream_t st);
-cudaError_t launch_dense_large(const DenseParams<kMaxReplicas>& p, int grid, cudaStream_t st);
+cudaError_t launch_dense_small(const DenseParams<kSmallReplicas>& p, int sms, cudaStream_t st);
+cudaError_t launch_dense_large(const DenseParams<kMaxReplicas>& p, int sms, cudaStream_t st);
 
 // Momentum only (DiLoCo between syncs): m_r <- beta m_r + g_r for every replica.
 template <int MAXR>
@@ -97,8 +99,8 @@ struct MomentumParams {
   float beta;
 };
 
-cudaError_t launch_momentum_small(const MomentumParams<kSmallReplicas>& p, bool bf16, int grid, cudaStream_t st);
-cudaError_t launch_momentum_large(const MomentumParams<kMaxReplicas>& p, bool bf16, int grid, cudaStream_t st);
+cudaError_t launch_momentum_small(const MomentumParams<kSmallReplicas>& p, bool bf16, int sms, cudaStream_t st);
+cudaError_t launch_momentum_large(const MomentumParams<kMaxReplicas>& p, bool bf16, int sms, cudaStream_t st);
 
 // Decoupled AdamW (elementwise, grid-stride over groups of four parameters).
 struct AdamWParams {
@@ -134,5 +136,7 @@ cudaError_t launch_decode_large(const DecodeParams<kMaxReplicas>& p, int mode, i
 // Set the dynamic shared-memory limit of every encode and decode kernel instantiation.
 cudaError_t prepare_encode_kernels();
 cudaError_t prepare_decode_kernels();
+// Find the resident CTAs per SM of the dense decode and momentum kernels (their grids).
+cudaError_t prepare_dense_kernels();
 
 }  // namespace demo

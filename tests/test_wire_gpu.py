@@ -66,6 +66,21 @@ def test_wire_many_replicas(mode, k, sign, R, wire):
     torch.cuda.empty_cache()
 
 
+# DiLoCo with many replicas in every format, on a shard whose chunk count leaves a ragged last
+# tile (1001 chunks) and whose groups of four parameters leave a ragged last row of every
+# elementwise unit: the sync step's dense decode (the ternary format's per-chunk byte counters
+# up to R = 64) and the momentum pass of the step between syncs (period 2: one of each).
+N_ODD = 32 * 1001
+DILOCO_MANY = [(True, 64, "ternary"), (True, 5, "ternary"), (True, 1, "ternary"), (False, 17, "bf16"),
+               (False, 64, "f16"), (False, 1, "bf16"), (False, 9, "f32"), (False, 1, "f32")]
+
+
+@pytest.mark.parametrize("sign,R,wire", DILOCO_MANY, ids=lambda v: str(v))
+def test_diloco_many_replicas(sign, R, wire):
+    run_steps(N_ODD, R, 1, "diloco", sign, 3, g_std=1e-3, period=2, seed=31, wire=wire)
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("k", [1, 2, 4, 8])
 def test_ternary_with_bf16_gradients(k):
     """The ternary DeMo encode compiled for k, fed bfloat16 gradients."""
