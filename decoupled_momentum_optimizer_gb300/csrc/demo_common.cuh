@@ -145,8 +145,9 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
 // this grid frees, and griddep_wait blocks until the previous grid has completed and its
 // memory operations are visible.  Each tile kernel waits before its first global-memory
 // access, so every read and write stays ordered after the previous kernel, and since every
-// kernel in the chain waits, after all earlier ones.  Without the launch attribute both are
-// no-ops.
+// kernel in the chain waits, after all earlier ones.  (The one exception is an encode the
+// host marks as sharing no buffers with the kernels around it: it waits only before exiting,
+// see encode_kernel.)  Without the launch attribute both are no-ops.
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

@@ -21,11 +21,14 @@ namespace demo {
 constexpr int kDenseThreads = 256;
 constexpr int kDenseWarps = kDenseThreads / 32;
 
-// One wave of resident CTAs, or fewer when the units do not fill it.
+// One wave of resident CTAs, or one CTA per eight units of work where that is at most two
+// waves: on a small shard every lane then runs a single iteration, and the CTAs of the second
+// wave start as soon as the first ones end (momentum pass, 2^20 parameters, 64 replicas:
+// 138 us with one wave of two iterations per lane, 131 us with this).
 int one_wave(int per_sm, int sms, long long units) {
   const long long want = (units + kDenseWarps - 1) / kDenseWarps;
   const long long wave = static_cast<long long>(per_sm) * sms;
-  const long long g = want < wave ? want : wave;
+  const long long g = want <= 2 * wave ? want : wave;
   return static_cast<int>(g > 0 ? g : 1);
 }
 

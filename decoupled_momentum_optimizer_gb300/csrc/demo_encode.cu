@@ -195,14 +195,27 @@ __global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_cons
   const int lane = threadIdx.x & 31;
   EncWarpSmem& ws = reinterpret_cast<EncWarpSmem*>(base)[warp];
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + WARPS * sizeof(EncWarpSmem)) + 2 * warp;
-  griddep_launch_dependents();
+  // Programmatic launch.  By default the kernel lets the next one start at once and waits for
+  // the previous one before its first global access.  With defer_wait (set by the host only
+  // inside a sequence of its own launches whose kernels share no buffers), the loads and the
+  // work overlap the previous kernel's tail and the wait moves to the end, so this grid still
+  // completes after the previous one and every event recorded behind it covers both; the next
+  // kernel is let start only once this one's own wait has passed when it does wait first, so
+  // a deferred successor never starts ahead of the work before the sequence.
+  if (p.defer_wait) griddep_launch_dependents();
 
   // The launch may run fewer warps than the shared-memory layout holds: warps are counted
   // from the block size.
   const int nw = static_cast<int>(blockDim.x >> 5);
   const long long gw = static_cast<long long>(blockIdx.x) * nw + warp;
   const long long TW = static_cast<long long>(gridDim.x) * nw;
-  if (gw >= p.ntiles) return;
+  if (gw >= p.ntiles) {
+    if (!p.defer_wait) {
+      griddep_wait();
+      griddep_launch_dependents();
+    }
+    return;
+  }
   const long long nitems = (p.ntiles - 1 - gw) / TW + 1;
 
   if (lane == 0) {
@@ -213,7 +226,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_cons
     fence_mbar_init();
   }
   __syncwarp();
-  griddep_wait();  // the previous kernel's writes (m, an earlier payload's readers) are done
+  if (!p.defer_wait) {
+    griddep_wait();  // the previous kernel's writes (m, an earlier payload's readers) are done
+    griddep_launch_dependents();
+  }
 
   auto issue = [&](long long item) {
     if (item >= nitems) return;
@@ -243,6 +259,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_cons
           mbar_wait_bounded(&bars[it & 1], static_cast<uint32_t>((it >> 1) & 1));
       }
       __syncwarp();
+      if (p.defer_wait) griddep_wait();
       return;
     }
 
@@ -340,6 +357,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) encode_kernel(const __grid_cons
     __syncwarp();
     if (lane == 0) issue(item + 2);
   }
+  if (p.defer_wait) griddep_wait();  // complete only after the previous kernel
 }
 
 // Resident warps per SM for one encode, and whether DeMo runs the kernel compiled for

@@ -21,6 +21,9 @@ struct EncodeParams {
   unsigned long long hbase;
   unsigned int* fault;
   long long stall_at;  // test hook of the bounded waits (see stall_extra), 0 = off
+  // 1: the previous kernel of the stream is one of this library's encodes or decodes that
+  // touches none of this kernel's buffers; wait for it only before exiting (see encode_kernel)
+  int defer_wait;
 };
 
 template <int MAXR>
