@@ -441,8 +441,9 @@ class _Null:
 
 
 def time_split(dm, case, mode, k, sign, seed, steps, warmup, stream, diloco_period=8, step0=0, wire="f32"):
-    """Mean time (ms) of R demo_encode calls + one demo_decode_update (the wire-format path); each step
-    timed alone after an L2 flush when it is smaller than twice the L2."""
+    """Mean time (ms) of the split path, every replica's encode (one demo_encode_replicas call) + one
+    demo_decode_update, in the wire format; each step timed alone after an L2 flush when it is smaller
+    than twice the L2."""
     import torch
 
     wl, n, R = case.wl, case.n, case.R
@@ -452,11 +453,12 @@ def time_split(dm, case, mode, k, sign, seed, steps, warmup, stream, diloco_peri
     vals = [b[0] for b in bufs]
     idx = [b[1] for b in bufs] if mode == "demo" else None
 
+    sends = mode != "diloco" or diloco_period == 1
+
     def one(t):
         g = case.ring[t % len(case.ring)]
-        for r in range(R):
-            dm.encode(g[r], case.ms[r], vals[r], idx[r] if idx else None, k=k, beta=wl.beta, mode=mode, sign=sign,
-                      diloco_period=diloco_period, seed=seed, step=t, wire=wire, stream=stream)
+        dm.encode_replicas(g, case.ms, vals if sends else None, idx, k=k, beta=wl.beta, mode=mode, sign=sign,
+                           diloco_period=diloco_period, seed=seed, step=t, wire=wire, stream=stream)
         dm.decode_update(case.theta, vals, idx, k=k, lr=wl.lr, mode=mode, diloco_period=diloco_period, seed=seed,
                          step=t, wire=wire, stream=stream)
 
@@ -494,7 +496,7 @@ def _timed_steps(fn, steps, stream, flush, dev):
 
 
 def time_split_graph(dm, case, mode, k, sign, seed, steps, warmup, stream, wire="f32"):
-    """Mean time (ms) of the split path (R demo_encode + one demo_decode_update) captured once into a
+    """Mean time (ms) of the split path (demo_encode_replicas + demo_decode_update) captured once into a
     CUDA graph and replayed (each replay timed alone after an L2 flush when the step is smaller than
     twice the L2); the graph keeps its captured step index."""
     import torch
@@ -507,9 +509,8 @@ def time_split_graph(dm, case, mode, k, sign, seed, steps, warmup, stream, wire=
     g = case.ring[0]
 
     def one():
-        for r in range(R):
-            dm.encode(g[r], case.ms[r], vals[r], idx[r] if idx else None, k=k, beta=wl.beta, mode=mode, sign=sign,
-                      seed=seed, step=1, wire=wire)
+        dm.encode_replicas(g, case.ms, vals, idx, k=k, beta=wl.beta, mode=mode, sign=sign, seed=seed, step=1,
+                           wire=wire)
         dm.decode_update(case.theta, vals, idx, k=k, lr=wl.lr, mode=mode, seed=seed, step=1, wire=wire)
 
     one()  # the first call of each kernel shape happens outside the capture

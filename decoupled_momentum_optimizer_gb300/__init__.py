@@ -37,6 +37,9 @@ _SIGS = {
     "demo_encode_wire": (ctypes.c_int, [_c_vp, ctypes.c_int, _c_vp, _c_i64, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_u64, _c_u64,
                                         ctypes.c_int, _c_vp, _c_vp, _c_vp]),
+    "demo_encode_replicas": (ctypes.c_int, [_c_vp, ctypes.c_int, _c_vp, _c_i64, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            _c_u64, _c_u64, ctypes.c_int, _c_vp, _c_vp, _c_vp]),
     "demo_decode_update_wire": (ctypes.c_int, [_c_vp, _c_i64, ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                                ctypes.c_int, ctypes.c_int, _c_vp, _c_vp, ctypes.c_int, _c_u64, _c_u64,
                                                ctypes.c_int, _c_vp]),
@@ -250,6 +253,29 @@ def encode(g, m, vals, idx=None, *, k, beta, mode="demo", sign=True, diloco_peri
         ip = _ptr(idx, _idx_dtypes(w), "idx", None, d.index) if idx is not None else None
         _check(lib().demo_encode_wire(gp, gd, mp, n, CHUNK, k, beta, _mode(mode), int(bool(sign)), diloco_period,
                                       seed, step, w, vp, ip, _stream(stream, d.index)), "demo_encode")
+
+
+def encode_replicas(gs, ms, vals, idx=None, *, k, beta, mode="demo", sign=True, diloco_period=8, seed=0, step=0,
+                    wire="f32", stream=None):
+    """Every replica's encode in one call (demo_encode_replicas): updates each m_r in place, writes
+    vals[r] (and idx[r] for DeMo).  ``vals`` / ``idx`` are lists of R tensors, or None where the
+    step sends nothing (DiLoCo between syncs) / carries no indices."""
+    import torch
+
+    with _OnDevice(ms[0].device) as d:
+        n = ms[0].numel()
+        R = len(ms)
+        if len(gs) != R or (vals is not None and len(vals) != R) or (idx is not None and len(idx) != R):
+            raise ValueError("need one gradient, payload and index buffer per replica")
+        w = _wire(wire)
+        gd = _grad_dtype(gs[0])
+        garr = _ptrs(gs, (gs[0].dtype,), "g", n, d.index)
+        marr = _ptrs(ms, (torch.float32,), "m", n, d.index)
+        varr = _ptrs(vals, _val_dtypes(w), "vals", None, d.index) if vals is not None else None
+        iarr = _ptrs(idx, _idx_dtypes(w), "idx", None, d.index) if idx is not None else None
+        _check(lib().demo_encode_replicas(garr, gd, marr, n, CHUNK, k, beta, _mode(mode), int(bool(sign)), R,
+                                          diloco_period, seed, step, w, varr, iarr, _stream(stream, d.index)),
+               "demo_encode_replicas")
 
 
 def decode_update(theta, vals, idx=None, *, k, lr, mode="demo", diloco_period=8, seed=0, step=0, wire="f32",

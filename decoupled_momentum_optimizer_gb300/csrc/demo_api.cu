@@ -449,6 +449,39 @@ struct PayloadLayout {
   size_t idx_end(int64_t c1) const { return idx_per_tile ? ((c1 + 31) / 32) * idx_per_tile : c1 * idx_per_chunk; }
 };
 
+// Argument checks of one replica's encode (demo_encode_wire); *sends tells whether the step
+// sends a payload.
+int check_encode(const void* g, int grad_dtype, const float* m, int64_t n, int chunk, int k, float beta, int mode,
+                 int sign, int diloco_period, uint64_t step, int wire, const void* vals, const void* idx,
+                 bool* sends_out) {
+  const int s = check_shape(n, chunk, k, mode, diloco_period);
+  if (s != DEMO_OK) return s;
+  if (grad_dtype != DEMO_GRAD_F32 && grad_dtype != DEMO_GRAD_BF16) return DEMO_EINVAL;
+  if (sign != 0 && sign != 1) return DEMO_EINVAL;
+  if (!valid_wire(wire) || (wire == DEMO_WIRE_TERNARY && !sign)) return DEMO_EINVAL;
+  if (!std::isfinite(beta)) return DEMO_EINVAL;
+  const bool sends = mode != DEMO_MODE_DILOCO || diloco_sync(step, diloco_period);
+  *sends_out = sends;
+  if (g == nullptr || m == nullptr) return DEMO_EINVAL;
+  if (sends && vals == nullptr) return DEMO_EINVAL;
+  if (mode == DEMO_MODE_DEMO && idx == nullptr) return DEMO_EINVAL;
+  if (!aligned16(g) || !aligned16(m)) return DEMO_EALIGN;
+  if (sends && !aligned16(vals)) return DEMO_EALIGN;
+  if (mode == DEMO_MODE_DEMO && !aligned16(idx)) return DEMO_EALIGN;
+  const size_t gb = static_cast<size_t>(n) * (grad_dtype == DEMO_GRAD_BF16 ? 2 : 4);
+  const size_t fb = static_cast<size_t>(n) * 4;
+  if (overlap(g, gb, m, fb)) return DEMO_EINVAL;
+  if (sends) {
+    // the payload is written: it may overlap neither the gradient, the momentum nor itself
+    size_t ib = 0;
+    const size_t vb = demo_payload_bytes_wire(mode, n, DEMO_CHUNK, k, step, diloco_period, wire, &ib);
+    if (overlap(vals, vb, g, gb) || overlap(vals, vb, m, fb)) return DEMO_EINVAL;
+    if (mode == DEMO_MODE_DEMO && (overlap(idx, ib, g, gb) || overlap(idx, ib, m, fb) || overlap(idx, ib, vals, vb)))
+      return DEMO_EINVAL;
+  }
+  return DEMO_OK;
+}
+
 PayloadLayout payload_layout(int mode, int k, int wire) {
   PayloadLayout L;
   const size_t kv = mode == DEMO_MODE_DILOCO ? DEMO_CHUNK : static_cast<size_t>(k);
@@ -554,35 +587,60 @@ size_t demo_payload_bytes(int mode, int64_t n, int chunk, int k, uint64_t step, 
 int demo_encode_wire(const void* g, int grad_dtype, float* m, int64_t n, int chunk, int k, float beta, int mode,
                      int sign, int diloco_period, uint64_t seed, uint64_t step, int wire, void* vals, void* idx,
                      void* stream) {
-  int s = check_shape(n, chunk, k, mode, diloco_period);
+  bool sends = false;
+  int s = check_encode(g, grad_dtype, m, n, chunk, k, beta, mode, sign, diloco_period, step, wire, vals, idx, &sends);
   if (s != DEMO_OK) return s;
-  if (grad_dtype != DEMO_GRAD_F32 && grad_dtype != DEMO_GRAD_BF16) return DEMO_EINVAL;
-  if (sign != 0 && sign != 1) return DEMO_EINVAL;
-  if (!valid_wire(wire) || (wire == DEMO_WIRE_TERNARY && !sign)) return DEMO_EINVAL;
-  if (!std::isfinite(beta)) return DEMO_EINVAL;
-  const bool sends = mode != DEMO_MODE_DILOCO || diloco_sync(step, diloco_period);
-  if (g == nullptr || m == nullptr) return DEMO_EINVAL;
-  if (sends && vals == nullptr) return DEMO_EINVAL;
-  if (mode == DEMO_MODE_DEMO && idx == nullptr) return DEMO_EINVAL;
-  if (!aligned16(g) || !aligned16(m)) return DEMO_EALIGN;
-  if (sends && !aligned16(vals)) return DEMO_EALIGN;
-  if (mode == DEMO_MODE_DEMO && !aligned16(idx)) return DEMO_EALIGN;
-  const size_t gb = static_cast<size_t>(n) * (grad_dtype == DEMO_GRAD_BF16 ? 2 : 4);
-  const size_t fb = static_cast<size_t>(n) * 4;
-  if (overlap(g, gb, m, fb)) return DEMO_EINVAL;
-  if (sends) {
-    // the payload is written: it may overlap neither the gradient, the momentum nor itself
-    size_t ib = 0;
-    const size_t vb = demo_payload_bytes_wire(mode, n, DEMO_CHUNK, k, step, diloco_period, wire, &ib);
-    if (overlap(vals, vb, g, gb) || overlap(vals, vb, m, fb)) return DEMO_EINVAL;
-    if (mode == DEMO_MODE_DEMO && (overlap(idx, ib, g, gb) || overlap(idx, ib, m, fb) || overlap(idx, ib, vals, vb)))
-      return DEMO_EINVAL;
-  }
   DeviceState* st = nullptr;
   s = current_state(&st);
   if (s != DEMO_OK) return s;
   return run_encode(st, g, grad_dtype, m, n, k, beta, mode, sign, sends, seed, step, wire, vals, idx, 0,
                     static_cast<cudaStream_t>(stream));
+}
+
+int demo_encode_replicas(const void* const* g, int grad_dtype, float* const* m, int64_t n, int chunk, int k,
+                         float beta, int mode, int sign, int R, int diloco_period, uint64_t seed, uint64_t step,
+                         int wire, void* const* vals, void* const* idx, void* stream) {
+  if (R < 1 || R > DEMO_MAX_REPLICAS || g == nullptr || m == nullptr) return DEMO_EINVAL;
+  bool sends = false;
+  const bool demo = mode == DEMO_MODE_DEMO;
+  for (int r = 0; r < R; ++r) {
+    void* v = vals ? vals[r] : nullptr;
+    void* ix = idx ? idx[r] : nullptr;
+    const int s = check_encode(g[r], grad_dtype, m[r], n, chunk, k, beta, mode, sign, diloco_period, step, wire, v,
+                               ix, &sends);
+    if (s != DEMO_OK) return s;
+  }
+  // every m, vals and idx is written: none may overlap another replica's buffers (each replica's
+  // own were checked above)
+  const size_t fb = static_cast<size_t>(n) * 4;
+  const size_t gb = static_cast<size_t>(n) * (grad_dtype == DEMO_GRAD_BF16 ? 2 : 4);
+  size_t ib = 0;
+  const size_t vb = sends ? demo_payload_bytes_wire(mode, n, DEMO_CHUNK, k, step, diloco_period, wire, &ib) : 0;
+  for (int r = 0; r < R; ++r) {
+    for (int q = 0; q < R; ++q) {
+      if (q == r) continue;
+      if (overlap(m[r], fb, m[q], fb) || overlap(m[r], fb, g[q], gb)) return DEMO_EINVAL;
+      if (sends) {
+        if (overlap(vals[r], vb, g[q], gb) || overlap(vals[r], vb, m[q], fb) || overlap(vals[r], vb, vals[q], vb))
+          return DEMO_EINVAL;
+        if (demo && (overlap(idx[r], ib, g[q], gb) || overlap(idx[r], ib, m[q], fb) ||
+                     overlap(idx[r], ib, vals[q], vb) || overlap(idx[r], ib, idx[q], ib)))
+          return DEMO_EINVAL;
+      }
+    }
+  }
+  DeviceState* st = nullptr;
+  int s = current_state(&st);
+  if (s != DEMO_OK) return s;
+  // The replicas share no buffers, so every encode after the first may start while the previous
+  // one finishes and wait for it only before exiting (EncodeParams::defer_wait).
+  for (int r = 0; r < R; ++r) {
+    s = run_encode(st, g[r], grad_dtype, m[r], n, k, beta, mode, sign, sends, seed, step, wire,
+                   sends ? vals[r] : nullptr, demo ? idx[r] : nullptr, 0, static_cast<cudaStream_t>(stream),
+                   kDeferEncodeWait && r > 0);
+    if (s != DEMO_OK) return s;
+  }
+  return DEMO_OK;
 }
 
 int demo_encode(const void* g, int grad_dtype, float* m, int64_t n, int chunk, int k, float beta, int mode,

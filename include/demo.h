@@ -58,7 +58,7 @@
  *     for the device.  demo_step_pipelined enqueues each call's work under a
  *     per-device lock (it shares a pool of events); the kernels of calls that
  *     overlap on the GPU are ordered only by the caller's streams.
- *   - demo_encode(_wire), demo_decode_update(_wire), demo_step(_wire),
+ *   - demo_encode(_wire), demo_encode_replicas, demo_decode_update(_wire), demo_step(_wire),
  *     demo_step_pipelined and demo_adamw_step make only kernel launches, event
  *     records and waits and asynchronous device copies on the given streams, so
  *     they may be captured into a CUDA graph (after demo_init).  A captured call
@@ -211,6 +211,24 @@ int demo_encode_wire(const void* g, int grad_dtype, float* m, int64_t n, int chu
 int demo_decode_update_wire(float* theta, int64_t n, int chunk, int k, float lr, int mode, int R,
                             const void* const* vals, const void* const* idx, int diloco_period,
                             uint64_t seed, uint64_t step, int wire, void* stream);
+
+/*
+ * demo_encode_replicas -- demo_encode_wire for every replica r = 0..R-1 of the
+ * replication group (1 <= R <= 64) in one call, enqueued in that order on `stream`
+ * ("1. FlexDeMo", Algorithm 1, steps 3-5, which each member of the group runs).
+ *   g[r], m[r], vals[r], idx[r]   replica r's buffers, each as demo_encode_wire
+ *                                 takes them (vals / idx may be NULL where that
+ *                                 call allows it: the whole array, or entries)
+ * Results are bit-identical to R calls of demo_encode_wire.  Every m, vals and
+ * idx is written, so none may overlap another replica's buffers (DEMO_EINVAL; the
+ * gradients, read only, may be shared).  Because the replicas share no buffers,
+ * each encode kernel after the first starts while the previous one finishes and
+ * waits for it only before exiting; separate calls cannot, as the library cannot
+ * know that successive calls touch different buffers.
+ */
+int demo_encode_replicas(const void* const* g, int grad_dtype, float* const* m, int64_t n, int chunk,
+                         int k, float beta, int mode, int sign, int R, int diloco_period, uint64_t seed,
+                         uint64_t step, int wire, void* const* vals, void* const* idx, void* stream);
 int demo_step_wire(float* theta, int64_t n, int chunk, int k, float beta, float lr, int mode, int sign,
                    int R, const void* const* g, int grad_dtype, float* const* m, int diloco_period,
                    uint64_t seed, uint64_t step, int wire, void* stream);

@@ -83,6 +83,24 @@ def gpu_split(theta, ms, gs, *, k, beta, lr, mode, sign, seed, step, period, wir
                   step=step, wire=wire)
         vals.append(v)
         idxs.append(i)
+    # the same encodes as one demo_encode_replicas call: bit-identical momenta and payloads
+    ms3 = [m.clone() for m in ms]
+    bufs3 = [dm.payload_buffers(mode, n, k, step=step, diloco_period=period, wire=wire) for _ in ms]
+    for b in bufs3:
+        for t in b:
+            if t is not None:
+                t.fill_(0)
+    vals3 = [b[0] for b in bufs3] if vals[0] is not None else None
+    idx3 = [b[1] for b in bufs3] if mode == "demo" else None
+    dm.encode_replicas(gs, ms3, vals3, idx3, k=k, beta=beta, mode=mode, sign=sign, diloco_period=period, seed=seed,
+                       step=step, wire=wire)
+    same = lambda a, b: torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
+    for r in range(len(ms)):
+        assert same(ms3[r], ms2[r]), f"encode_replicas: m of replica {r} differs from demo_encode's"
+        if vals3 is not None:
+            assert same(vals3[r], vals[r]), f"encode_replicas: payload of replica {r} differs"
+        if idx3 is not None:
+            assert same(idx3[r], idxs[r]), f"encode_replicas: indices of replica {r} differ"
     th2 = theta.clone()
     dvals = vals if vals[0] is not None else [torch.zeros(4, device=theta.device)] * len(ms)
     if vals[0] is None and wire != "f32":

@@ -176,6 +176,33 @@ def test_pipelined_buffer_checks(L):
     assert pipelined_call(L, [0x100000, 0x31000], si, rv, ri) == EINVAL  # send values inside g[0]
 
 
+def replicas_call(L, gs=None, ms=None, vals=None, idx=None, R=2, mode=0, step=0):
+    arr = lambda xs: (ctypes.c_void_p * R)(*xs) if xs is not None else None
+    gs = gs if gs is not None else [0x100000 * (r + 1) for r in range(R)]
+    ms = ms if ms is not None else [0x1000000 * (r + 1) for r in range(R)]
+    return L.demo_encode_replicas(arr(gs), 0, arr(ms), 64, 32, 4, 0.9, mode, 1, R, 8, 0, step, 0, arr(vals), arr(idx),
+                                  None)
+
+
+def test_encode_replicas_buffer_checks(L):
+    # n = 64, DeMo k = 4: 32 bytes of values and 8 of indices per replica
+    sv, si = [0x30000, 0x31000], [0x32000, 0x33000]
+    assert replicas_call(L, vals=sv, idx=si) in (ENOTINIT, ENODEV)
+    assert replicas_call(L, gs=[0x100000, 0x100000], vals=sv, idx=si) in (ENOTINIT, ENODEV)  # shared gradients
+    assert replicas_call(L, R=0, gs=[], ms=[], vals=[], idx=[]) == EINVAL
+    assert replicas_call(L, ms=[0x1000000, 0x1000000], vals=sv, idx=si) == EINVAL  # one momentum for two replicas
+    assert replicas_call(L, ms=[0x1000000, 0x100000], vals=sv, idx=si) == EINVAL  # m[1] is g[0]
+    assert replicas_call(L, vals=[0x30000, 0x30010], idx=si) == EINVAL  # two replicas' values overlap
+    assert replicas_call(L, vals=sv, idx=[0x31010, 0x33000]) == EINVAL  # indices inside another replica's values
+    assert replicas_call(L, vals=[0x1000000 + 64, 0x31000], idx=si) == EINVAL  # values inside m[0]
+    assert replicas_call(L, vals=[0x30000, 0x2000000], idx=si) == EINVAL  # values inside m[1]: a replica's own
+    assert replicas_call(L, vals=sv, idx=None) == EINVAL  # DeMo needs indices
+    assert replicas_call(L, vals=[0x30008, 0x31000], idx=si) == EALIGN
+    # DiLoCo between syncs sends nothing: no payload buffers
+    assert replicas_call(L, mode=3, vals=None, idx=None) in (ENOTINIT, ENODEV)
+    assert replicas_call(L, mode=3, step=7, vals=None, idx=None) == EINVAL  # a sync step needs them
+
+
 def test_validate_payload_host(L):
     import torch
 

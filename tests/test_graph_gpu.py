@@ -75,10 +75,14 @@ def test_fused_step_replay(mode, k, sign, R, wire, bf16):
         assert_same(ms, ms_e)
 
 
-@pytest.mark.parametrize("mode,k,wire", [("demo", 4, "f32"), ("demo", 2, "ternary"), ("random", 4, "bf16")],
+@pytest.mark.parametrize("mode,k,wire,together", [("demo", 4, "f32", False), ("demo", 2, "ternary", False),
+                                                   ("random", 4, "bf16", False), ("demo", 4, "f32", True),
+                                                   ("stride", 8, "ternary", True)],
                          ids=lambda v: str(v))
-def test_split_path_replay(mode, k, wire):
-    """R encodes and the decode captured together, against the same calls made eagerly."""
+def test_split_path_replay(mode, k, wire, together):
+    """R encodes (R calls, or one demo_encode_replicas call, whose later encodes wait for their
+    predecessor only at their end) and the decode captured together, against the same calls made
+    eagerly."""
     R = 3
     kw = dict(k=k, mode=mode, seed=4, step=2, wire=wire)
     theta = cuda_normal(N, 2e-2, 1)
@@ -89,8 +93,12 @@ def test_split_path_replay(mode, k, wire):
     pay_e = [dm.payload_buffers(mode, N, k, step=2, wire=wire) for _ in range(R)]
 
     def split(th, mm, gg, pp):
-        for r in range(R):
-            dm.encode(gg[r], mm[r], pp[r][0], pp[r][1], beta=0.99, sign=True, **kw)
+        if together:
+            dm.encode_replicas(gg, mm, [p[0] for p in pp], [p[1] for p in pp] if mode == "demo" else None,
+                               beta=0.99, sign=True, **kw)
+        else:
+            for r in range(R):
+                dm.encode(gg[r], mm[r], pp[r][0], pp[r][1], beta=0.99, sign=True, **kw)
         dm.decode_update(th, [p[0] for p in pp], [p[1] for p in pp] if mode == "demo" else None, lr=1e-2, **kw)
 
     graph = capture(lambda: split(theta, ms, gbuf, pay))
