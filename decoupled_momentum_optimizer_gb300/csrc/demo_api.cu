@@ -632,12 +632,17 @@ int demo_encode_replicas(const void* const* g, int grad_dtype, float* const* m, 
   DeviceState* st = nullptr;
   int s = current_state(&st);
   if (s != DEMO_OK) return s;
+  // DiLoCo between syncs: only the momenta move, all R in one elementwise pass
+  if (!sends) {
+    return R <= kSmallReplicas
+               ? run_momentum<kSmallReplicas>(st, n, beta, R, g, grad_dtype, m, static_cast<cudaStream_t>(stream))
+               : run_momentum<kMaxReplicas>(st, n, beta, R, g, grad_dtype, m, static_cast<cudaStream_t>(stream));
+  }
   // The replicas share no buffers, so every encode after the first may start while the previous
   // one finishes and wait for it only before exiting (EncodeParams::defer_wait).
   for (int r = 0; r < R; ++r) {
-    s = run_encode(st, g[r], grad_dtype, m[r], n, k, beta, mode, sign, sends, seed, step, wire,
-                   sends ? vals[r] : nullptr, demo ? idx[r] : nullptr, 0, static_cast<cudaStream_t>(stream),
-                   kDeferEncodeWait && r > 0);
+    s = run_encode(st, g[r], grad_dtype, m[r], n, k, beta, mode, sign, true, seed, step, wire, vals[r],
+                   demo ? idx[r] : nullptr, 0, static_cast<cudaStream_t>(stream), kDeferEncodeWait && r > 0);
     if (s != DEMO_OK) return s;
   }
   return DEMO_OK;
@@ -842,17 +847,21 @@ int demo_step_pipelined(float* theta, int64_t n, int chunk, int k, float beta, f
   // touch none of its buffers (each reads and writes its own block of g_r, m_r and the send
   // buffers; the decodes read the receive buffers and theta): it may load and work while the
   // previous kernel finishes and wait for it only before exiting.
+  // DiLoCo between syncs sends nothing: the step is the momenta alone, one elementwise pass
+  if (!sends) {
+    return R <= kSmallReplicas ? run_momentum<kSmallReplicas>(st, n, beta, R, g, grad_dtype, m, cs)
+                               : run_momentum<kMaxReplicas>(st, n, beta, R, g, grad_dtype, m, cs);
+  }
   for (int b = 0; b < B; ++b) {
     const int64_t c0 = chunk_lo(b), c1 = chunk_hi(b);
     const int64_t nb = (c1 - c0) * DEMO_CHUNK;
     for (int r = 0; r < R; ++r) {
       const void* gb_ptr = at(g[r], static_cast<size_t>(c0) * DEMO_CHUNK * (grad_dtype == DEMO_GRAD_BF16 ? 2 : 4));
-      s = run_encode(st, gb_ptr, grad_dtype, m[r] + c0 * DEMO_CHUNK, nb, k, beta, mode, sign, sends, seed, step, wire,
-                     sends ? at(send_vals[r], L.vals_at(c0)) : nullptr,
-                     sends && demo ? at(send_idx[r], L.idx_at(c0)) : nullptr, c0, cs, kDeferEncodeWait && (b > 0 || r > 0));
+      s = run_encode(st, gb_ptr, grad_dtype, m[r] + c0 * DEMO_CHUNK, nb, k, beta, mode, sign, true, seed, step, wire,
+                     at(send_vals[r], L.vals_at(c0)), demo ? at(send_idx[r], L.idx_at(c0)) : nullptr, c0, cs,
+                     kDeferEncodeWait && (b > 0 || r > 0));
       if (s != DEMO_OK) return s;
     }
-    if (!sends) continue;
     // the exchange of block b: a loopback copy of every replica's payload block on the communication stream
     if (cudaEventRecord(st->ev_enc[b], cs) != cudaSuccess || cudaStreamWaitEvent(xs, st->ev_enc[b], 0) != cudaSuccess)
       return DEMO_ECUDA;
@@ -872,12 +881,8 @@ int demo_step_pipelined(float* theta, int64_t n, int chunk, int k, float beta, f
       if (s != DEMO_OK) return s;
     }
   }
-  if (sends) {
-    if (cudaStreamWaitEvent(cs, st->ev_xch[B - 1], 0) != cudaSuccess) return DEMO_ECUDA;
-    s = decode_block(B - 1);
-    if (s != DEMO_OK) return s;
-  }
-  return DEMO_OK;
+  if (cudaStreamWaitEvent(cs, st->ev_xch[B - 1], 0) != cudaSuccess) return DEMO_ECUDA;
+  return decode_block(B - 1);
 }
 
 }  // extern "C"
