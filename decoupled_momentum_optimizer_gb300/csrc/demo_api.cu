@@ -257,6 +257,16 @@ constexpr size_t kLaneCopyMaxSpan = 320;
 constexpr size_t kLaneCopyMaxSpanWide = 192;
 constexpr size_t kDirectMinSpan = 256;
 
+// Whether a decode of R <= 4 staged replicas is light enough per tile to run best with the
+// fewest warps (measured over every scheme, k in {1, 4, 8}, R in {2, 4} and every wire format;
+// DeMo only for k = 4 with float32 payloads and two replicas, 2^27: 197 -> 190 us; its other
+// cases measured 3-15% slower with eight warps).
+bool few_warps_decode(int mode, int k, int wire, int R) {
+  if (mode == DEMO_MODE_STRIDE) return wire != DEMO_WIRE_TERNARY || R <= 2;
+  if (mode == DEMO_MODE_RANDOM) return (wire == DEMO_WIRE_F32 && k <= 4) || (k == 1 && R <= 2);
+  return k == 4 && wire == DEMO_WIRE_F32 && R <= 2;
+}
+
 template <class P>
 int stage_payloads(P& p, int mode, int k, int wire, int R, int* flavor) {
   p.nstaged = 0;
@@ -377,7 +387,17 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
   p.fault = st->fault;
   p.stall_at = st->stall_at.exchange(0);
   int flavor;
-  const int warps = stage_payloads(p, mode, k, wire, R, &flavor);
+  int warps = stage_payloads(p, mode, k, wire, R, &flavor);
+  // Receivers of at most four replicas, all staged, on large shards: the shape with the fewest
+  // warps (and the largest staging, so every span still fits) where the per-tile work is light,
+  // and the widest where the Random draws or the ternary bit extraction are heavy (2^27, R = 2,
+  // 11 -> 8 warps: Striding k = 4 f32 200 -> 190 us, bf16 190 -> 176, ternary 176 -> 162;
+  // Random k = 1 f32 182 -> 167, k = 4 207 -> 184; but Random k = 8 f32 202 -> 242 and Random
+  // k = 4 ternary 174 -> 203).  Below 16 tiles per warp of the widest shape the fewer warps hide
+  // less latency (2^24, DeMo k = 4: 99.8 -> 102.4 us for the split step).
+  const bool many_tiles = p.ntiles >= 16LL * st->sms * kDecShapes[0];
+  if (many_tiles && p.nstaged == R && R <= kSmallReplicas && k <= 8 && few_warps_decode(mode, k, wire, R))
+    warps = kDecShapes[3];
   const TileShape sh = tile_shape(warps, warps, p.ntiles, st);
   // DeMo with k in {1, 2, 4, 8} runs the decode compiled for its k: kv = k for the float32 and
   // 16-bit formats, kv = -k for the ternary one
@@ -397,13 +417,14 @@ int run_decode(DeviceState* st, float* theta, int64_t n, int k, float lr, int mo
   return to_status(e);
 }
 
-// One replica's encode over n elements whose first chunk is chunk0 of the shard (arguments checked).
-// Deferred grid-dependency waits for the encodes inside demo_step_pipelined
-// (EncodeParams::defer_wait).  T5-base shard, DeMo k = 4, R = 2: 16 blocks 1.616 -> 1.534 ms,
-// 8 blocks 1.401 -> 1.342, 4 blocks 1.342 -> 1.310; the same for the decodes measured no
-// change (each decode follows a wait on the exchange's event, which orders it fully).
+// Deferred grid-dependency waits for the encodes after the first of demo_step_pipelined and
+// demo_encode_replicas (EncodeParams::defer_wait).  T5-base shard, DeMo k = 4, R = 2, pipelined:
+// 16 blocks 1.616 -> 1.534 ms, 8 blocks 1.401 -> 1.342, 4 blocks 1.342 -> 1.310; the same for the
+// pipelined decodes measured no change (each follows a wait on the exchange's event, which
+// orders it fully).
 constexpr bool kDeferEncodeWait = true;
 
+// One replica's encode over n elements whose first chunk is chunk0 of the shard (arguments checked).
 int run_encode(DeviceState* st, const void* g, int grad_dtype, float* m, int64_t n, int k, float beta, int mode,
                int sign, bool sends, uint64_t seed, uint64_t step, int wire, void* vals, void* idx, int64_t chunk0,
                cudaStream_t stream, bool defer_wait = false) {
