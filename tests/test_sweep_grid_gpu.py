@@ -50,16 +50,16 @@ def test_grid_combination(mode, k, R, regime):
 # Receivers of at most four replicas on shards of at least 16 tiles per warp of the widest
 # decode shape run with eight warps where the per-tile work is light (Striding, Random with
 # float32 payloads and k <= 4 or k = 1 on two replicas, DeMo k = 4 with float32 payloads on
-# two): a 2^25-parameter shard (32,768 tiles), checked on sampled chunks, in every wire format
-# the rule covers and in two it leaves at eleven warps.
-LIGHT_DECODES = [("random", 1, 2, "f32"), ("random", 4, 4, "f32"), ("random", 1, 2, "ternary"),
-                 ("stride", 4, 2, "bf16"), ("stride", 8, 2, "ternary"), ("stride", 1, 3, "f16"),
-                 ("demo", 4, 2, "f32"), ("random", 8, 2, "f32"), ("stride", 4, 4, "ternary")]
+# two): 2^25- and 2^27-parameter shards, checked on sampled chunks, in every wire format the
+# rule covers and in cases it leaves at eleven warps.
+LIGHT_DECODES = [("random", 1, 2, "f32", 25), ("random", 4, 4, "f32", 25), ("random", 1, 2, "ternary", 25),
+                 ("stride", 4, 2, "bf16", 25), ("stride", 8, 2, "ternary", 25), ("stride", 1, 3, "f16", 25),
+                 ("demo", 4, 2, "f32", 25), ("demo", 4, 2, "f32", 27), ("random", 8, 2, "f32", 25), ("stride", 4, 4, "ternary", 25)]
 
 
-@pytest.mark.parametrize("mode,k,R,wire", LIGHT_DECODES, ids=lambda v: str(v))
-def test_decode_shapes_on_a_large_shard(mode, k, R, wire):
-    n = 1 << 25
+@pytest.mark.parametrize("mode,k,R,wire,log_n", LIGHT_DECODES, ids=lambda v: str(v))
+def test_decode_shapes_on_a_large_shard(mode, k, R, wire, log_n):
+    n = 1 << log_n
     rows = sample_rows(n // 32, count=2048)
     stats = {}
     run_steps(n, R, k, mode, True, 2, g_std=1e-3, seed=19, rows=rows, stats=stats, wire=wire)
