@@ -4,9 +4,10 @@
  * It shows that the header is valid C (no C++ types or keywords leak through
  * the extern "C" block) and that a C program links against the library and
  * calls its host-only entry points: status names, payload sizes, the payload
- * validator, and the device probe.  It prints one "key value" line per result;
- * the Python side compares them with the oracle's payload sizes and with the
- * header's stated conventions.  No call here launches a kernel.
+ * validator, the argument checks of the multi-replica encode, and the device
+ * probe.  It prints one "key value" line per result; the Python side compares
+ * them with the oracle's payload sizes and with the header's stated
+ * conventions.  No call here launches a kernel.
  */
 #include <stdio.h>
 #include <stdint.h>
@@ -55,6 +56,29 @@ int main(void) {
   idx[4 * 1 + 3] = 32; /* chunk 1 holds an index past the chunk */
   rc = demo_validate_payload(3 * DEMO_CHUNK, DEMO_CHUNK, 4, DEMO_WIRE_F32, idx, &bad);
   printf("validate_range %d %ld\n", rc, (long)bad);
+
+  {
+    /* demo_encode_replicas refuses before any launch: no replicas, and two replicas sharing one
+       momentum buffer (the addresses are never dereferenced) */
+    const void* g[2];
+    float* m[2];
+    void* v[2];
+    void* ix[2];
+    g[0] = (const void*)(uintptr_t)0x100000u;
+    g[1] = (const void*)(uintptr_t)0x200000u;
+    m[0] = (float*)(uintptr_t)0x1000000u;
+    m[1] = (float*)(uintptr_t)0x1000000u;
+    v[0] = (void*)(uintptr_t)0x30000u;
+    v[1] = (void*)(uintptr_t)0x31000u;
+    ix[0] = (void*)(uintptr_t)0x32000u;
+    ix[1] = (void*)(uintptr_t)0x33000u;
+    rc = demo_encode_replicas(g, DEMO_GRAD_F32, m, 64, DEMO_CHUNK, 4, 0.9f, DEMO_MODE_DEMO, 1, 0, 8, 0, 0,
+                              DEMO_WIRE_F32, v, ix, NULL);
+    printf("replicas_none %d\n", rc);
+    rc = demo_encode_replicas(g, DEMO_GRAD_F32, m, 64, DEMO_CHUNK, 4, 0.9f, DEMO_MODE_DEMO, 1, 2, 8, 0, 0,
+                              DEMO_WIRE_F32, v, ix, NULL);
+    printf("replicas_shared_m %d\n", rc);
+  }
 
   init = demo_init(0);
   printf("init %d\n", init);

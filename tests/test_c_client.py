@@ -69,6 +69,11 @@ def test_payload_size_errors_and_wire_from_c(client_output):
                                                                      wire=ref.WIRE_TERNARY)[0]
 
 
+def test_encode_replicas_refusals_from_c(client_output):
+    assert client_output["replicas_none"] == [EINVAL]
+    assert client_output["replicas_shared_m"] == [EINVAL]
+
+
 def test_validate_payload_from_c(client_output):
     assert client_output["validate_ok"] == [0]
     assert client_output["validate_dup"] == [EINVAL, 2]
