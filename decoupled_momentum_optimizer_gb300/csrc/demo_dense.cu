@@ -260,8 +260,15 @@ cudaError_t launch_momentum(const MomentumParams<MAXR>& p, bool bf16, int sms, c
 }
 
 cudaError_t prepare_dense_kernels() {
-  const cudaError_t e = prepare_dense_replicas<kSmallReplicas>();
-  return e != cudaSuccess ? e : prepare_dense_replicas<kMaxReplicas>();
+  // The table is the same on every device the library accepts (one architecture): it is filled
+  // once, so a later device's initialisation never writes it while launches read it.  The
+  // caller (demo_init) holds the library's lock.
+  static bool filled = false;
+  if (filled) return cudaSuccess;
+  cudaError_t e = prepare_dense_replicas<kSmallReplicas>();
+  if (e == cudaSuccess) e = prepare_dense_replicas<kMaxReplicas>();
+  if (e == cudaSuccess) filled = true;
+  return e;
 }
 
 cudaError_t launch_momentum_small(const MomentumParams<kSmallReplicas>& p, bool bf16, int sms, cudaStream_t st) {
